@@ -1,0 +1,378 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (CPU only).
+
+Every oracle function is checked against something other than itself: the
+pages' worked example and asserts (tests/golden/), hand-derived closed forms,
+brute force on tiny inputs, exact rational arithmetic, invariants and special
+cases.  A plausible mistake (dropped term, wrong sign, wrong rounding, wrong
+nibble order, transposed operand) fails at least one of these.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import int4_g128, linear, mxfp4, uniform
+from bit_weight_quantized_wq_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Symmetric routine: the lesson's worked example and asserts
+# ---------------------------------------------------------------------------
+
+def test_lesson6_worked_example():
+    g = _golden("lesson6_blockwise_symmetric.json")["worked_example"]
+    restored, scales = uniform.blockwise_symmetric_fake_quant(g["values"], g["block_size"], g["qmax"])
+    assert scales == [g["scale_num"] / g["scale_den"]]
+    s = scales[0]
+    codes = [round(r / s) for r in restored]
+    assert codes == g["codes"]
+    assert [round(r, 3) for r in restored] == g["restored_printed_3dp"]
+    assert restored[-1] == 8.0  # the block maximum is restored exactly
+
+
+def test_lesson6_asserts():
+    g = _golden("lesson6_blockwise_symmetric.json")
+    a = g["asserts"][0]
+    restored, scales = uniform.blockwise_symmetric_fake_quant(a["values"], a["block_size"], a["qmax"])
+    assert scales == [n / d for n, d in a["scales_exact"]]
+    assert abs(restored[1] - a["restored_index_1"]) < a["abs_tol"]
+    assert abs(restored[-1] - a["restored_index_last"]) < a["abs_tol"]
+    b = g["asserts"][1]
+    assert uniform.blockwise_symmetric_fake_quant(b["values"], b["block_size"], b["qmax"]) == (
+        b["restored_exact"], b["scales_exact_float"])
+    for bad in g["invalid_geometry"]:
+        with pytest.raises(ValueError):
+            uniform.blockwise_symmetric_fake_quant([1.0], bad["block_size"], bad["qmax"])
+
+
+def test_lesson6_finer_blocks_do_not_increase_error():
+    # 第 6 课 "检查方法": compare error and scale count for block size 2 vs 4.
+    vals = [0.0, 1.0, -2.0, 8.0]
+    r2, s2 = uniform.blockwise_symmetric_fake_quant(vals, 2, 7)
+    r4, s4 = uniform.blockwise_symmetric_fake_quant(vals, 4, 7)
+    e2 = sum(abs(a - b) for a, b in zip(vals, r2))
+    e4 = sum(abs(a - b) for a, b in zip(vals, r4))
+    assert len(s2) == 2 and len(s4) == 1
+    # by hand: size 2 -> blocks [0,1] (exact) and [-2,8] (s=8/7, |-2+16/7| = 2/7);
+    # size 4 -> s = 8/7 for all: errors 1/7 (x=1) and 2/7 (x=-2)
+    assert abs(e2 - 2 / 7) < 1e-12 and abs(e4 - 3 / 7) < 1e-12
+
+
+def test_symmetric_int8_scale_and_ties():
+    # scale = max|x| / 127 (推理优化与量化算子深度技术调研 §1.2); max 127 -> scale 1, so
+    # the codes are the values rounded half to even: 0.5 -> 0, 1.5 -> 2.
+    codes, scale = uniform.symmetric_quantize(np.array([-127.0, 0.5, 1.5, 2.5], np.float32), 8)
+    assert scale == 1.0
+    assert codes.tolist() == [-127, 0, 2, 2]
+    codes, scale = uniform.symmetric_quantize(np.array([0.0, 0.0], np.float32), 8)
+    assert scale == 1.0 and codes.tolist() == [0, 0]
+
+
+# ---------------------------------------------------------------------------
+# Asymmetric INT4 g128
+# ---------------------------------------------------------------------------
+
+def test_int4_linspace_closed_form():
+    g = _golden("hand_derived_int4.json")["linspace_group"]
+    x = np.linspace(-1, 2, 128, dtype=np.float32)[None, :]
+    Wq, s, z = int4_g128.quantize(x)
+    assert s.view(np.uint16)[0, 0] == int(g["scale_fp16_hex"], 16)
+    assert float(s[0, 0]) == g["scale"]
+    assert float(z[0, 0]) == g["zero"]
+    q = int4_g128.unpack(Wq)[0]
+    assert q[0] == g["code_first"] and q[-1] == g["code_last"]
+
+
+def test_int4_constant_positive_group_includes_zero_in_range():
+    g = _golden("hand_derived_int4.json")["constant_positive_group"]
+    x = np.full((1, 128), 0.3, np.float32)
+    Wq, s, z = int4_g128.quantize(x)
+    assert s.view(np.uint16)[0, 0] == int(g["scale_fp16_hex"], 16)
+    assert float(z[0, 0]) == g["zero"]
+    assert (int4_g128.unpack(Wq) == g["code"]).all()
+
+
+def test_int4_packing_order():
+    g = _golden("hand_derived_int4.json")["packing"]
+    q = np.array([g["codes"]], dtype=np.uint32)
+    w = int4_g128.pack(q)
+    assert int(w.view(np.uint32)[0, 0]) == int(g["word_hex"], 16)
+    assert int4_g128.unpack(w).tolist() == [g["codes"]]
+
+
+def test_int4_zero_group_and_negative_zero():
+    x = np.zeros((2, 256), np.float32)
+    x[1, :128] = -0.0
+    Wq, s, z = int4_g128.quantize(x)
+    assert (s == 1).all() and (z == 0).all() and (z.view(np.uint16) == 0).all()
+    assert (int4_g128.unpack(Wq) == 0).all()
+
+
+def _special_groups(rng):
+    """Adversarial groups: constant, all positive, all negative, one outlier, ties, tiny, +-0."""
+    g = []
+    g.append(np.full(128, 0.37, np.float32))
+    g.append(np.abs(rng.standard_normal(128).astype(np.float32)))
+    g.append(-np.abs(rng.standard_normal(128).astype(np.float32)))
+    o = (rng.standard_normal(128) * 0.02).astype(np.float32); o[17] = 3.0; g.append(o)
+    t = (np.arange(128, dtype=np.float32) - 40) * np.float32(0.25); g.append(t)  # many exact ties
+    g.append((rng.standard_normal(128) * 1e-7).astype(np.float32))                  # fp16-subnormal scale
+    g.append((rng.standard_normal(128) * 1e-9).astype(np.float32))                  # scale underflows -> 1
+    z = np.zeros(128, np.float32); z[::2] = -0.0; z[5] = 1e-3; g.append(z)
+    return np.stack(g)
+
+
+def test_int4_matches_per_group_generic_routine():
+    # The vectorised quantizer equals the plain per-group asymmetric routine with
+    # b = 4 and fp16 scale storage, run group by group (brute force on small inputs).
+    rng = np.random.default_rng(5)
+    W = np.concatenate([_special_groups(rng).reshape(-1, 256),
+                        (rng.standard_normal((3, 256)) * 0.05).astype(np.float32)])
+    Wq, s, z = int4_g128.quantize(W)
+    q = int4_g128.unpack(Wq)
+    for n in range(W.shape[0]):
+        for gi in range(W.shape[1] // 128):
+            qq, ss, zz = uniform.asymmetric_quantize(W[n, 128 * gi:128 * gi + 128], 4, np.float16)
+            assert ss == np.float32(s[n, gi]) and zz == np.float32(z[n, gi])
+            assert (qq == q[n, 128 * gi:128 * gi + 128]).all()
+
+
+def test_int4_code_is_nearest_grid_point():
+    # Brute force: each code's dequantized value is the nearest of the 16 grid
+    # points (j - z)*s, j = 0..15 (clamping included).
+    rng = np.random.default_rng(7)
+    W = np.concatenate([_special_groups(rng)[:6].reshape(-1, 128),
+                        inputs.weights(11, 8, 256, 0.02).reshape(-1, 128)])
+    Wq, s, z = int4_g128.quantize(W)
+    q = int4_g128.unpack(Wq).astype(np.int64)
+    for n in range(W.shape[0]):
+        sv, zv = float(s[n, 0]), float(z[n, 0])
+        grid = (np.arange(16) - zv) * sv
+        for k in range(128):
+            x = float(W[n, k])
+            d = np.abs(grid - x)
+            assert d[q[n, k]] == d.min(), (n, k, x, q[n, k])
+
+
+def test_int4_error_bound_and_codes_in_range():
+    # 第 1 章 §4.1: step Δ = s, so inside the grid's range |x - x_hat| <= s/2.
+    W = inputs.weights(3, 64, 1024, 0.02)
+    Wq, s, z = int4_g128.quantize(W)
+    q = int4_g128.unpack(Wq)
+    assert q.max() <= 15 and (z >= 0).all() and (z <= 15).all()
+    W_hat = int4_g128.dequantize(Wq, s, z)
+    sg = np.repeat(s.astype(np.float64), 128, axis=1)
+    zg = np.repeat(z.astype(np.float64), 128, axis=1)
+    lo, hi = -zg * sg, (15 - zg) * sg
+    inside = (W >= lo) & (W <= hi)
+    assert inside.mean() > 0.95   # group extremes may sit just outside when fp16 shrinks s
+    err = np.abs(W.astype(np.float64) - W_hat)
+    assert (err[inside] <= sg[inside] / 2 * (1 + 1e-12)).all()
+    # outside the grid (fp16 rounding of s shrank it) the excess is at most 15*|s32 - s|
+    x = W.reshape(64, 8, 128)
+    s32 = (np.maximum(x.max(-1), 0) - np.minimum(x.min(-1), 0)) / np.float32(15)
+    slack = np.repeat(np.abs(s32.astype(np.float64) - s.astype(np.float64)) * 16, 128, axis=1)
+    assert (err <= sg / 2 + slack + 1e-12).all()
+
+
+def test_int4_on_grid_weights_roundtrip_exactly():
+    # Weights already on a grid (j - z)*s with j spanning 0..15 quantize without error.
+    rng = np.random.default_rng(9)
+    N, K = 4, 256
+    W = np.empty((N, K), np.float32)
+    for n in range(N):
+        for gi in range(K // 128):
+            sv = float(np.float16(rng.uniform(0.001, 0.1)))
+            zv = int(rng.integers(0, 16))
+            j = rng.integers(0, 16, 128); j[0], j[1] = 0, 15
+            W[n, 128 * gi:128 * gi + 128] = (j - zv) * sv
+    Wq, s, z = int4_g128.quantize(W)
+    assert (int4_g128.dequantize(Wq, s, z) == W.astype(np.float64)).all()
+
+
+def test_int4_group_size_sweep_error_monotone():
+    # 第 6 课 "检查方法" analogue for the asymmetric routine: smaller groups, no larger error.
+    W = inputs.weights(21, 32, 1024, 0.02)
+    errs = []
+    for gs in (32, 64, 128):
+        e = 0.0
+        for n in range(W.shape[0]):
+            for g0 in range(0, W.shape[1], gs):
+                x = W[n, g0:g0 + gs]
+                q, s, z = uniform.asymmetric_quantize(x, 4, np.float16)
+                e += float(np.sum((x - uniform.asymmetric_dequantize(q, s, z)) ** 2))
+        errs.append(e)
+    assert errs[0] <= errs[1] <= errs[2]
+
+
+def test_asymmetric_int8_roundtrip():
+    # b = 8 instance of the same formula (推理优化与量化算子深度技术调研 §1.2).
+    x = np.array([-1.0, -0.5, 0.0, 0.25, 3.0], np.float32)
+    q, s, z = uniform.asymmetric_quantize(x, 8)
+    assert s == np.float32(np.float32(4.0) / np.float32(255))
+    assert z == 64.0           # rint(1/s) = rint(63.75) = 64
+    assert q[0] == 0 and q[-1] == 255 and q[2] == 64
+    assert np.abs(x - uniform.asymmetric_dequantize(q, s, z)).max() <= s / 2 + 1e-9
+
+
+# ---------------------------------------------------------------------------
+# MXFP4
+# ---------------------------------------------------------------------------
+
+def test_e2m1_value_set_and_decode():
+    g = _golden("mxfp4_e2m1_ties.json")
+    vals = mxfp4.decode_e2m1(np.arange(16, dtype=np.uint8))
+    assert vals[:8].tolist() == g["grid"]
+    assert vals[8:].tolist() == [-v for v in g["grid"]]
+
+
+def test_e2m1_ties_to_even_code():
+    g = _golden("mxfp4_e2m1_ties.json")
+    a = np.array([c[0] for c in g["cases"]])
+    assert mxfp4.e2m1_round_magnitude(a).tolist() == [c[1] for c in g["cases"]]
+
+
+def test_e8m0_exponent_exact():
+    # amax / 2^e in (3, 6] for amax > 0 (exact rationals), boundary 6*2^j -> e = j.
+    rng = np.random.default_rng(13)
+    amax = np.concatenate([np.abs(rng.standard_normal(2000)).astype(np.float32) * np.float32(0.05),
+                           np.float32(2.0) ** rng.integers(-60, 60, 500).astype(np.float32)])
+    for a in amax:
+        r = np.float32(a) / np.float32(6)
+        e = mxfp4.e8m0_exponent(r)
+        ratio = Fraction(float(a)) / (Fraction(2) ** e)
+        assert Fraction(3) < ratio <= Fraction(6), (a, e)
+    for j in range(-100, 100, 7):
+        a = np.float32(6.0 * 2.0 ** j)
+        assert mxfp4.e8m0_exponent(a / np.float32(6)) == j
+        a_up = np.nextafter(a, np.float32(np.inf))
+        assert mxfp4.e8m0_exponent(a_up / np.float32(6)) == j + 1
+    assert (mxfp4.e8m0_exponents(np.array([0.0, 1.0, 1.5, 2.0 ** -140])) == [-127, 0, 1, -127]).all()
+
+
+def test_mxfp4_packing_order():
+    g = _golden("mxfp4_e2m1_ties.json")["packing"]
+    c = np.array([g["codes"] + [0] * 6], dtype=np.uint8)
+    w = mxfp4.pack(c)
+    assert w.view(np.uint8)[0, 0] == int(g["byte_hex"], 16)
+    assert mxfp4.unpack(w).tolist() == c.tolist()
+
+
+def test_mxfp4_zero_block_and_signed_zero():
+    W = np.zeros((1, 64), np.float32)
+    W[0, 33] = 1.0
+    W[0, 34] = -0.0
+    W[0, 35] = -1e-30       # rounds to magnitude 0 but keeps its sign
+    W[0, 0] = -0.0          # inside an all-zero block
+    Wq, sc = mxfp4.quantize(W)
+    codes = mxfp4.unpack(Wq)[0]
+    assert sc[0, 0] == 0 and (codes[:32] == 0).all()
+    assert codes[34] == 8 and codes[35] == 8 and codes[36] == 0
+    assert sc[0, 1] == 127 - 2     # amax 1: r = 1/6, ceil(log2 r) = -2
+    assert codes[33] == 6          # 1 * 2^2 = 4.0 -> magnitude code 6
+
+
+def test_mxfp4_code_is_nearest_representable():
+    # Brute force over the 16 signed values times 2^e: the chosen code is a nearest
+    # one, and on a tie the magnitude code is even.
+    W = inputs.weights(17, 4, 256, 0.02)
+    Wq, sc = mxfp4.quantize(W)
+    codes = mxfp4.unpack(Wq)
+    cand = mxfp4.decode_e2m1(np.arange(16, dtype=np.uint8))
+    for n in range(4):
+        for k in range(256):
+            f = 2.0 ** (int(sc[n, k // 32]) - 127)
+            x = float(W[n, k])
+            d = np.abs(cand * f - x)
+            c = int(codes[n, k])
+            assert d[c] == d.min()
+            ties = np.flatnonzero(d == d.min())
+            if len({int(t) & 7 for t in ties}) > 1:
+                assert (c & 7) % 2 == 0
+
+
+def test_mxfp4_error_bound_and_grid_roundtrip():
+    W = inputs.weights(19, 16, 512, 0.02)
+    Wq, sc = mxfp4.quantize(W)
+    W_hat = mxfp4.dequantize(Wq, sc)
+    f = np.repeat(np.exp2(sc.astype(np.float64) - 127), 32, axis=1)
+    assert (np.abs(W - W_hat) <= f + 1e-300).all()        # half the widest spacing (2) times 2^e
+    assert (np.abs(W_hat) <= 6 * f).all()
+    # on-grid blocks (grid value * 2^e, block max 6 * 2^e) round-trip exactly
+    rng = np.random.default_rng(23)
+    e = rng.integers(-20, 5, (3, 4))
+    idx = rng.integers(0, 16, (3, 128))
+    G = mxfp4.decode_e2m1(idx.astype(np.uint8)).reshape(3, 4, 32)
+    G[:, :, 0] = 6.0
+    Wg = (G * np.exp2(e)[..., None]).reshape(3, 128).astype(np.float32)
+    Wq, sc = mxfp4.quantize(Wg)
+    assert (sc.astype(np.int64) - 127 == e).all()
+    assert (mxfp4.dequantize(Wq, sc) == Wg.astype(np.float64)).all()
+
+
+# ---------------------------------------------------------------------------
+# The linear layer
+# ---------------------------------------------------------------------------
+
+def test_linear_brute_force_fractions():
+    rng = np.random.default_rng(29)
+    for fmt in ("int4_g128", "mxfp4"):
+        M, K, N = 3, 256, 5
+        W = inputs.weights(31, N, K, 0.05)
+        _, X = inputs.activations(37, M, K)
+        if fmt == "int4_g128":
+            Wq, s, z = int4_g128.quantize(W)
+            W_hat = int4_g128.dequantize(Wq, s, z)
+            Y = linear.linear_w4a16(fmt, X, Wq, s, z)
+        else:
+            Wq, s = mxfp4.quantize(W)
+            W_hat = mxfp4.dequantize(Wq, s)
+            Y = linear.linear_w4a16(fmt, X, Wq, s)
+        assert Y.shape == (M, N)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(Fraction(float(X[m, k])) * Fraction(float(W_hat[n, k])) for k in range(K))
+                assert abs(Fraction(float(Y[m, n])) - exact) <= Fraction(1, 10 ** 12) * (1 + abs(exact))
+
+
+def test_linear_special_cases():
+    M, K, N = 4, 256, 6
+    _, X = inputs.activations(41, M, K)
+    Wq, s, z = int4_g128.quantize(np.zeros((N, K), np.float32))
+    assert (linear.linear_w4a16("int4_g128", X, Wq, s, z) == 0).all()
+    # on-grid weights: the quantized layer equals the unquantized product
+    W = ((np.arange(N * K).reshape(N, K) % 16) - 3).astype(np.float32) * np.float32(0.125)
+    Wq, s, z = int4_g128.quantize(W)
+    assert (linear.linear_w4a16("int4_g128", X, Wq, s, z) == X.astype(np.float64) @ W.T.astype(np.float64)).all()
+    rows = [5, 0, 3]
+    full = linear.linear_w4a16("int4_g128", X, Wq, s, z)
+    assert (linear.linear_rows("int4_g128", X, Wq, s, z, rows) == full[:, rows]).all()
+
+
+@pytest.mark.parametrize("outliers,bar", [(0.0, 0.99), (0.01, 0.95)])
+def test_linear_sanity_against_unquantized(outliers, bar):
+    # 量化与加速 deployment checklist: no NaN/Inf, cosine similarity > 0.99 vs the fp32
+    # layer.  With 1 % of input columns x10 (the salient channels of 推理优化与量化算子深度技术调研
+    # §1.3), plain round-to-nearest loses more (about 0.98) -- the gap AWQ scaling closes.
+    M, K, N = 4, 1024, 64
+    W = inputs.weights(43, N, K, 0.02, outlier_frac=outliers)
+    _, X = inputs.activations(43, M, K)
+    ref = X.astype(np.float64) @ W.T.astype(np.float64)
+    for fmt in ("int4_g128", "mxfp4"):
+        if fmt == "int4_g128":
+            Y = linear.linear_w4a16(fmt, X, *int4_g128.quantize(W))
+        else:
+            Y = linear.linear_w4a16(fmt, X, *mxfp4.quantize(W))
+        assert np.isfinite(Y).all()
+        cos = float((Y * ref).sum() / math.sqrt((Y * Y).sum() * (ref * ref).sum()))
+        assert cos > bar, (fmt, cos)
