@@ -1,0 +1,219 @@
+"""Thin ctypes binding of libwq.so (include/wq.h): argument marshalling only.
+
+Every step of the quantized layer runs in the library's CUDA kernels; this module only
+turns torch CUDA tensors into raw device pointers and the current torch stream into a
+``cudaStream_t``.  PyTorch supplies device memory and streams.  There is no CPU fallback:
+if the library is missing or the device is not a GB300-class part, calls raise.
+
+Function names follow the C ABI (``wq_quantize_int4_g128`` -> ``quantize_int4_g128`` ...).
+A non-OK status raises ``ValueError`` (argument errors, as the lesson's
+``blockwise_symmetric_fake_quant`` does for invalid geometry) or ``RuntimeError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libwq.so")
+
+FMT_INT4_G128 = 0
+FMT_MXFP4 = 1
+_FMT_NAMES = {"int4_g128": FMT_INT4_G128, "mxfp4": FMT_MXFP4}
+
+_STATUS = {0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_ALIGN", 4: "WQ_ERR_WORKSPACE",
+           5: "WQ_ERR_UNSUPPORTED_ARCH", 6: "WQ_ERR_CUDA", 7: "WQ_ERR_ARG"}
+
+EXPORTED = [
+    "wq_quantize_int4_g128", "wq_quantize_mxfp4", "wq_gemm_workspace_bytes", "wq_gemm_w4a16",
+    "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
+    "wq_status_str", "wq_read_error_flags", "wq_check_device",
+]
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libwq.so and declares the C signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError("libwq.so not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                           "(or python -m bit_weight_quantized_wq_gb300.build)")
+    lib = ctypes.CDLL(path)
+    P, I64, SZ, I32, U32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32
+    sig = {
+        "wq_quantize_int4_g128": (I32, [P, I64, I64, P, P, P, P]),
+        "wq_quantize_mxfp4": (I32, [P, I64, I64, P, P, P]),
+        "wq_gemm_workspace_bytes": (SZ, [I32, I64, I64, I64]),
+        "wq_gemm_w4a16": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_gemv_w4a16": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_gemm_tc_w4a16": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_dispatch_threshold": (I64, [I32, I64, I64]),
+        "wq_set_dispatch_threshold": (I32, [I32, I64, I64, I64]),
+        "wq_status_str": (ctypes.c_char_p, [I32]),
+        "wq_read_error_flags": (I32, [ctypes.POINTER(U32)]),
+        "wq_check_device": (I32, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load_library().wq_status_str(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status == 0:
+        return
+    msg = "%s failed: %s" % (what, status_str(status))
+    if status in (1, 2, 3, 4, 7):
+        raise ValueError(msg)
+    raise RuntimeError(msg)
+
+
+def _fmt(fmt) -> int:
+    if isinstance(fmt, str):
+        return _FMT_NAMES[fmt]
+    return int(fmt)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def check_device() -> None:
+    _check(load_library().wq_check_device(), "wq_check_device")
+
+
+def quantize_int4_g128(W: torch.Tensor, stream=None):
+    """W float32 [N, K] (CUDA) -> (Wq int32 [N, K/8], scales fp16 [N, K/128], zeros fp16 [N, K/128])."""
+    _need(W, torch.float32, "W")
+    N, K = W.shape
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    _check(load_library().wq_quantize_int4_g128(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _ptr(zeros), _stream(stream)),
+           "wq_quantize_int4_g128")
+    return Wq, scales, zeros
+
+
+def quantize_mxfp4(W: torch.Tensor, stream=None):
+    """W float32 [N, K] (CUDA) -> (Wq int32 [N, K/8], scales uint8 [N, K/32])."""
+    _need(W, torch.float32, "W")
+    N, K = W.shape
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, K // 32), dtype=torch.uint8, device=W.device)
+    _check(load_library().wq_quantize_mxfp4(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _stream(stream)),
+           "wq_quantize_mxfp4")
+    return Wq, scales
+
+
+def gemm_workspace_bytes(fmt, M: int, K: int, N: int) -> int:
+    return int(load_library().wq_gemm_workspace_bytes(_fmt(fmt), M, K, N))
+
+
+class Workspace:
+    """A zero-initialised device scratch buffer that grows on demand (one per stream)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = None
+
+    def get(self, nbytes: int):
+        if nbytes == 0:
+            return None
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(((nbytes + 255) // 256) * 256, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace_for(device, nbytes, workspace):
+    if workspace is not None:
+        return workspace
+    key = (str(device), torch.cuda.current_stream(device).cuda_stream)
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(device)
+    return ws.get(nbytes)
+
+
+def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream):
+    f = _fmt(fmt)
+    _need(X, torch.bfloat16, "X")
+    _need(Wq, torch.int32, "Wq")
+    if f == FMT_INT4_G128:
+        _need(scales, torch.float16, "scales")
+        _need(zeros, torch.float16, "zeros")
+    else:
+        _need(scales, torch.uint8, "scales")
+        if zeros is not None:
+            raise ValueError("zeros must be None for MXFP4")
+    M, K = X.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] * 8 != K:
+        raise ValueError("Wq must be [N, K/8]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    else:
+        _need(out, torch.bfloat16, "out")
+    nbytes = gemm_workspace_bytes(f, M, K, N)
+    ws = _workspace_for(X.device, nbytes, workspace)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    fn = getattr(load_library(), cname)
+    _check(fn(f, _ptr(X), M, K, N, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(out), _ptr(ws), ws_bytes,
+              _stream(stream)), cname)
+    return out
+
+
+def gemm_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """Y = X * dequant(Wq)^T (bf16 [M, N]); dispatches between the decode and tensor-core kernels."""
+    return _linear("wq_gemm_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
+
+
+def gemv_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """The decode kernel alone (M <= 16)."""
+    return _linear("wq_gemv_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
+
+
+def gemm_tc_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """The tcgen05 tensor-core kernel alone (any M)."""
+    return _linear("wq_gemm_tc_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
+
+
+def dispatch_threshold(fmt, K: int, N: int) -> int:
+    return int(load_library().wq_dispatch_threshold(_fmt(fmt), K, N))
+
+
+def set_dispatch_threshold(fmt, K: int, N: int, T: int) -> None:
+    _check(load_library().wq_set_dispatch_threshold(_fmt(fmt), K, N, T), "wq_set_dispatch_threshold")
+
+
+def read_error_flags() -> int:
+    v = ctypes.c_uint32(0)
+    _check(load_library().wq_read_error_flags(ctypes.byref(v)), "wq_read_error_flags")
+    return int(v.value)

@@ -1,0 +1,219 @@
+// The C ABI (include/wq.h): argument validation, per-shape dispatch, TMA descriptor
+// encoding, status strings and the device error word.
+#include <mutex>
+
+#include "../../include/wq.h"
+#include "internal.h"
+
+namespace wq {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                         uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                         CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace wq
+
+namespace {
+
+constexpr int kMaxOverrides = 256;
+struct ThresholdOverride {
+  int fmt;
+  int64_t K, N, T;
+};
+std::mutex g_thr_mu;
+ThresholdOverride g_thr[kMaxOverrides];
+int g_thr_n = 0;
+int64_t g_thr_default[2] = {16, 16};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+wq_status check_device_cached() {
+  // Compute capability 10.3 (GB300) only: the kernels use sm_103a-specific instructions.
+  static int ok_dev[64] = {0};  // 0 unknown, 1 ok, 2 bad
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WQ_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && ok_dev[dev]) return ok_dev[dev] == 1 ? WQ_OK : WQ_ERR_UNSUPPORTED_ARCH;
+  int maj = 0, min = 0;
+  if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return WQ_ERR_CUDA;
+  const bool ok = (maj == 10 && min == 3);
+  if (dev >= 0 && dev < 64) ok_dev[dev] = ok ? 1 : 2;
+  return ok ? WQ_OK : WQ_ERR_UNSUPPORTED_ARCH;
+}
+
+wq_status check_linear_args(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                            const void* scales, const uint16_t* zeros, uint16_t* Y) {
+  if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return WQ_ERR_ARG;
+  if (!X || !Wq || !scales || !Y) return WQ_ERR_NULL;
+  if (fmt == WQ_FMT_INT4_G128_ASYM && !zeros) return WQ_ERR_NULL;
+  if (fmt == WQ_FMT_MXFP4 && zeros) return WQ_ERR_ARG;
+  if (M < 1 || N < 1 || K < 1) return WQ_ERR_SHAPE;
+  if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return WQ_ERR_SHAPE;
+  if (K % (fmt == WQ_FMT_INT4_G128_ASYM ? 128 : 32) != 0) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(Y) || (zeros && !aligned16(zeros)))
+    return WQ_ERR_ALIGN;
+  return WQ_OK;
+}
+
+wq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+wq_status wq_quantize_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq, uint16_t* scales,
+                                uint16_t* zeros, void* stream) {
+  if (!W || !Wq || !scales || !zeros) return WQ_ERR_NULL;
+  if (N < 1 || K < 128 || K % 128 != 0 || N > (1LL << 31) || K > (1LL << 31)) return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zeros)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_quant_int4_g128(W, N, K, Wq, scales, zeros, static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_quantize_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq, uint8_t* scales, void* stream) {
+  if (!W || !Wq || !scales) return WQ_ERR_NULL;
+  if (N < 1 || K < 32 || K % 32 != 0 || N > (1LL << 31) || K > (1LL << 31)) return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(Wq) || !aligned16(scales)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_quant_mxfp4(W, N, K, Wq, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t wq_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N) {
+  if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return -1;
+  std::lock_guard<std::mutex> lk(g_thr_mu);
+  for (int i = 0; i < g_thr_n; ++i)
+    if (g_thr[i].fmt == fmt && g_thr[i].K == K && g_thr[i].N == N) return g_thr[i].T;
+  return g_thr_default[fmt];
+}
+
+wq_status wq_set_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N, int64_t T) {
+  if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return WQ_ERR_ARG;
+  if (T < 0 || T > 16 || K < 0 || N < 0) return WQ_ERR_SHAPE;
+  std::lock_guard<std::mutex> lk(g_thr_mu);
+  if (K == 0 && N == 0) {
+    g_thr_default[fmt] = T;
+    return WQ_OK;
+  }
+  for (int i = 0; i < g_thr_n; ++i)
+    if (g_thr[i].fmt == fmt && g_thr[i].K == K && g_thr[i].N == N) {
+      g_thr[i].T = T;
+      return WQ_OK;
+    }
+  if (g_thr_n >= kMaxOverrides) return WQ_ERR_SHAPE;
+  g_thr[g_thr_n++] = {static_cast<int>(fmt), K, N, T};
+  return WQ_OK;
+}
+
+size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N) {
+  if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return 0;
+  if (M < 1 || N < 1 || K < 1) return 0;
+  size_t a = M <= 16 ? wq::gemv_workspace_bytes(fmt, M, K, N) : 0;
+  size_t b = wq::gemm_tc_workspace_bytes(fmt, M, K, N);
+  return a > b ? a : b;
+}
+
+wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                        const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  if (M > 16) return WQ_ERR_SHAPE;
+  const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_gemm_tc_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                           const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  const size_t need = wq::gemm_tc_workspace_bytes(fmt, M, K, N);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gemm_tc(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                        const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace, size_t ws_bytes,
+                        void* stream) {
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  if (M <= wq_dispatch_threshold(fmt, K, N))
+    return wq_gemv_w4a16(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
+  return wq_gemm_tc_w4a16(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
+}
+
+const char* wq_status_str(wq_status s) {
+  switch (s) {
+    case WQ_OK: return "WQ_OK";
+    case WQ_ERR_NULL: return "WQ_ERR_NULL: a required pointer is NULL";
+    case WQ_ERR_SHAPE: return "WQ_ERR_SHAPE: size out of range or not a required multiple";
+    case WQ_ERR_ALIGN: return "WQ_ERR_ALIGN: pointer not 16-byte aligned";
+    case WQ_ERR_WORKSPACE: return "WQ_ERR_WORKSPACE: workspace missing or too small";
+    case WQ_ERR_UNSUPPORTED_ARCH: return "WQ_ERR_UNSUPPORTED_ARCH: device is not compute capability 10.3";
+    case WQ_ERR_CUDA: return "WQ_ERR_CUDA: CUDA call failed";
+    case WQ_ERR_ARG: return "WQ_ERR_ARG: argument out of range";
+  }
+  return "unknown wq_status";
+}
+
+wq_status wq_read_error_flags(uint32_t* out) {
+  if (!out) return WQ_ERR_NULL;
+  if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
+  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error();
+  return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+wq_status wq_check_device(void) { return check_device_cached(); }
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Declarations shared between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace wq {
+
+// Format codes (same values as wq_fmt in include/wq.h).
+enum Fmt : int { kInt4G128 = 0, kMxfp4 = 1 };
+
+// Encodes a 2-D tiled TMA descriptor through the driver entry point (no libcuda link).
+// dims/strides in elements/bytes, innermost first.
+cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
+                         uint64_t dim1, uint64_t stride1_bytes, uint32_t box0, uint32_t box1,
+                         CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo);
+
+int device_sm_count();
+
+// quantize.cu
+cudaError_t launch_quant_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq, uint16_t* scales,
+                                   uint16_t* zeros, cudaStream_t stream);
+cudaError_t launch_quant_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq, uint8_t* scales,
+                               cudaStream_t stream);
+
+// gemv.cu -- decode kernel, M <= 16
+size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                        const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                        cudaStream_t stream);
+uint32_t gemv_read_and_clear_error();
+
+// gemm_tc.cu -- tcgen05 kernel, any M
+size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                           const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+uint32_t gemm_tc_read_and_clear_error();
+
+}  // namespace wq

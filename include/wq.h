@@ -1,0 +1,160 @@
+/*
+ * wq.h -- C ABI of the GB300 (sm_103a) weight-only 4-bit quantized linear layer.
+ *
+ * Library: libwq.so (built from bit_weight_quantized_wq_gb300/csrc/).
+ *
+ * Two weight formats, both 0.53125 bytes per weight:
+ *   WQ_FMT_INT4_G128_ASYM  asymmetric INT4, group of 128 along K, eight codes per int32
+ *                          (low nibble first), one fp16 scale and one fp16 zero point per
+ *                          (row, group).
+ *   WQ_FMT_MXFP4           OCP MXFP4: E2M1 codes two per byte (element 2j in the low
+ *                          nibble of byte j), one E8M0 scale byte per 32 elements along K.
+ *
+ * Conventions shared by every entry point
+ *   - Row-major everywhere.  W is [N, K] (N output features, K input features), X is [M, K],
+ *     Y is [M, N].  Wq is [N, K/8] int32 (equivalently [N, K/2] bytes).
+ *   - fp16 and bf16 values cross the boundary as uint16_t bit patterns.
+ *   - Every pointer is a DEVICE pointer on the current CUDA device, owned by the caller, and
+ *     must be 16-byte aligned.  The library never allocates or frees device memory, never
+ *     synchronizes, and enqueues work only on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).
+ *   - Argument errors are detected on the host before anything is enqueued and returned as
+ *     a wq_status; nothing is launched then.  Launch failures return WQ_ERR_CUDA.  Device-side
+ *     faults surface, as usual in CUDA, at the caller's next synchronization.
+ *   - Every wait inside a kernel is bounded; a wait that runs out records a code readable
+ *     with wq_read_error_flags() and the kernel returns early (its output is then invalid).
+ *   - Non-finite weights give unspecified (but memory-safe) results.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  WQ_OK = 0,
+  WQ_ERR_NULL = 1,             /* a required pointer is NULL                         */
+  WQ_ERR_SHAPE = 2,            /* a size is out of range or not a multiple required  */
+  WQ_ERR_ALIGN = 3,            /* a pointer is not 16-byte aligned                   */
+  WQ_ERR_WORKSPACE = 4,        /* workspace missing or smaller than required         */
+  WQ_ERR_UNSUPPORTED_ARCH = 5, /* current device is not compute capability 10.3      */
+  WQ_ERR_CUDA = 6,             /* a CUDA runtime/driver call failed                  */
+  WQ_ERR_ARG = 7               /* an enum argument is out of range                   */
+} wq_status;
+
+typedef enum { WQ_FMT_INT4_G128_ASYM = 0, WQ_FMT_MXFP4 = 1 } wq_fmt;
+
+/*
+ * Asymmetric INT4 quantize + pack, group size 128 along K.
+ * Defined by: 推理优化与量化算子深度技术调研 §1.2 (asymmetric scale = (max-min)/(2^b-1),
+ * zero_point = round(-min/scale), q = clamp(round(x/scale)+zp, 0, 2^b-1)) and
+ * 第 1 章：推理加速全景 §4.1 (the b-bit form), with b = 4; packing per
+ * 第 6 课：量化源码走读 (源码分层架构与生命周期: 8 INT4 codes in one int32 plus scale and zero
+ * point tensors).  Per (row n, group g), float32 arithmetic:
+ *   lo = min(min x, 0), hi = max(max x, 0); s32 = (hi - lo) / 15;
+ *   s = fp16_rn(s32), and s = 1 if that is 0; z = rint(-lo / s);
+ *   q = clamp(rint(x / s) + z, 0, 15).
+ *   W       [N, K]    float32 input.
+ *   Wq      [N, K/8]  int32 output; code k = 8j+i in bits 4i..4i+3 of word j.
+ *   scales  [N, K/128] fp16 bits output.
+ *   zeros   [N, K/128] fp16 bits output (small non-negative integers).
+ * Errors: WQ_ERR_SHAPE unless N >= 1 and K >= 128, K % 128 == 0.
+ */
+wq_status wq_quantize_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq,
+                                uint16_t* scales, uint16_t* zeros, void* stream);
+
+/*
+ * OCP MXFP4 quantize + pack, one E8M0 scale per 32 elements along K.
+ * Defined by: 大模型量化推理引擎全景大复盘 (里程碑六 / 方程 3: 32 four-bit elements share one
+ * E8M0 scale; the simulator's scale 2^ceil(log2(amax/6)) on float32).  Per (row n, block b):
+ *   amax = max|x|; r = amax / 6 (float32); e = ceil(log2 r) exactly, clamped to [-127, 127]
+ *   (e = -127 when r == 0); v = x * 2^-e; magnitude code = nearest of
+ *   {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code, saturating at 6; code = sign(x)<<3 |
+ *   magnitude (sign bit of x kept, so -0 -> 8); an all-zero block has scale byte 0, codes 0.
+ *   W       [N, K]    float32 input.
+ *   Wq      [N, K/8]  int32 output == [N, K/2] bytes, element 2j in the low nibble of byte j.
+ *   scales  [N, K/32] uint8 output, E8M0 byte e + 127.
+ * Errors: WQ_ERR_SHAPE unless N >= 1 and K >= 32, K % 32 == 0.
+ */
+wq_status wq_quantize_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq,
+                            uint8_t* scales, void* stream);
+
+/*
+ * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
+ * The workspace must be zero-filled once before its first use (it holds reduction
+ * counters); every call that completes leaves those counters at zero again.  One workspace
+ * must not be used by two calls that can run at the same time.  Returns 0 for invalid
+ * arguments.
+ */
+size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N);
+
+/*
+ * Y = X * dequant(Wq)^T, bf16 activations, fp32 accumulation, bf16 output.
+ * Defined by: 推理优化与量化算子深度技术调研 §1.2 (dequantization fused into the GEMM,
+ * x_deq = (q - zp) * scale, before the multiply) and 第 6 课：量化源码走读 (W4A16 layer; the
+ * "apply" step chooses a bandwidth kernel for small batch and a compute kernel for large
+ * batch).  Dispatches on M: M <= T(fmt, K, N) runs the decode GEMV (T <= 16), otherwise the
+ * tcgen05 tensor-core GEMM.
+ *   X       [M, K] bf16 bits.
+ *   Wq      [N, K/8] int32 (format fmt).
+ *   scales  INT4: [N, K/128] fp16 bits; MXFP4: [N, K/32] uint8.
+ *   zeros   INT4: [N, K/128] fp16 bits; MXFP4: must be NULL.
+ *   Y       [M, N] bf16 bits output.
+ *   workspace / ws_bytes: device scratch of at least wq_gemm_workspace_bytes(fmt, M, K, N)
+ *           bytes (see there); may be NULL when that is 0.
+ * Errors: WQ_ERR_SHAPE unless M >= 1, N >= 1, K % 128 == 0 (INT4) or K % 32 == 0 (MXFP4);
+ *         WQ_ERR_NULL, WQ_ERR_ALIGN, WQ_ERR_WORKSPACE, WQ_ERR_ARG, WQ_ERR_UNSUPPORTED_ARCH,
+ *         WQ_ERR_CUDA.
+ */
+wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                        const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                        uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 16).
+ * Streams the packed weights with TMA, unpacks in registers and applies the group scale in
+ * fp32 after exact integer-valued tensor-core products; the zero point enters as (q - z),
+ * the cross term of 第 6 课：量化源码走读 §3.
+ */
+wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                        const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                        uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The tensor-core (tcgen05, TMEM accumulator) kernel alone, for any M >= 1 (same arguments
+ * and errors as wq_gemm_w4a16).
+ */
+wq_status wq_gemm_tc_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                           const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                           uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Dispatch threshold T(fmt, K, N): wq_gemm_w4a16 uses the decode kernel when M <= T.
+ * wq_set_dispatch_threshold overrides it for one (fmt, K, N) (T in [0, 16]; K = N = 0 sets
+ * the default for the format).  Returns WQ_ERR_ARG / WQ_ERR_SHAPE on bad input.  Host-side
+ * state, process-wide, not thread-safe against concurrent calls.
+ */
+int64_t wq_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N);
+wq_status wq_set_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N, int64_t T);
+
+/* Human-readable name of a status. */
+const char* wq_status_str(wq_status s);
+
+/*
+ * Reads (and clears) the device-side error word of the current device: 0 when no bounded
+ * wait ran out since the last read.  Synchronizes the device.
+ */
+wq_status wq_read_error_flags(uint32_t* out);
+
+/* WQ_OK when the current device is a GB300-class part (compute capability 10.3). */
+wq_status wq_check_device(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

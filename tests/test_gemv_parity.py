@@ -1,0 +1,96 @@
+"""Decode kernel (M <= 16) against the float64 oracle on the same dequantized weights."""
+import numpy as np
+import pytest
+
+from bit_weight_quantized_wq_gb300 import inputs
+from oracle import int4_g128, linear, mxfp4
+from tests._util import assert_close, to_dev, x_to_dev, y_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import torch
+    from bit_weight_quantized_wq_gb300 import binding
+    binding.check_device()
+    torch.cuda.init()
+    return binding
+
+
+def _pack(fmt, W):
+    return int4_g128.quantize(W) if fmt == "int4_g128" else mxfp4.quantize(W)
+
+
+def _run(B, fn, fmt, xbits, pk):
+    X = x_to_dev(xbits)
+    d = [to_dev(a) for a in pk]
+    if fmt == "int4_g128":
+        return fn(fmt, X, d[0], d[1], d[2])
+    return fn(fmt, X, d[0], d[1])
+
+
+CASES = [(16, 128), (1, 128), (256, 256), (1000, 512), (300, 1152), (777, 2048)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16])
+@pytest.mark.parametrize("N,K", CASES)
+def test_gemv_small(B, fmt, M, N, K):
+    W = inputs.weights(N * 7 + K, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M + N, M, K)
+    Y = _run(B, B.gemv_w4a16, fmt, xb, pk)
+    ref = linear.linear_w4a16(fmt, xf, *pk)
+    assert_close(y_to_host(Y), ref, "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("K", [32, 96, 160, 1056])
+def test_gemv_mxfp4_k_tail(B, M, K):
+    # MXFP4 only needs K % 32 == 0: the last 128-k unit is partial.
+    N = 300
+    W = inputs.weights(K + 11, N, K, 0.05)
+    pk = mxfp4.quantize(W)
+    xb, xf = inputs.activations(K, M, K)
+    Y = _run(B, B.gemv_w4a16, "mxfp4", xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16("mxfp4", xf, *pk), "mxfp4 K=%d" % K)
+
+
+def test_gemv_mxfp4_large_activations(B):
+    # Activations beyond the fp16 range: the per-row power-of-two scaling keeps them exact.
+    M, N, K = 4, 512, 1024
+    W = inputs.weights(5, N, K, 0.05)
+    pk = mxfp4.quantize(W)
+    xb, xf = inputs.activations(6, M, K, scale=3.0e5)
+    Y = _run(B, B.gemv_w4a16, "mxfp4", xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16("mxfp4", xf, *pk), "mxfp4 big X")
+
+
+def test_gemv_deterministic_and_workspace_reusable(B):
+    M, N, K = 4, 4096, 4096
+    W = inputs.weights(9, N, K, 0.02)
+    pk = int4_g128.quantize(W)
+    xb, _ = inputs.activations(9, M, K)
+    y1 = y_to_host(_run(B, B.gemv_w4a16, "int4_g128", xb, pk))
+    y2 = y_to_host(_run(B, B.gemv_w4a16, "int4_g128", xb, pk))
+    assert (y1 == y2).all()
+    assert B.read_error_flags() == 0
+
+
+# Full-size decode shapes (K, N) at M in {1, 4, 16}; the oracle checks 384 sampled output
+# columns (all M rows) by dequantizing only those weight rows.
+DECODE = [(4096, 4096), (4096, 6144), (4096, 28672), (14336, 4096), (8192, 8192)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("K,N", DECODE)
+def test_gemv_full_size_sampled(B, fmt, K, N):
+    W = inputs.weights(1000 + K % 91 + N % 89, N, K, 0.02)
+    pk = _pack(fmt, W)
+    rows = np.sort(np.random.default_rng(K + N).choice(N, 384, replace=False))
+    for M in (1, 4, 16):
+        xb, xf = inputs.activations(M * 13 + K, M, K)
+        Y = y_to_host(_run(B, B.gemv_w4a16, fmt, xb, pk))
+        ref = linear.linear_rows(fmt, xf, pk[0], pk[1], pk[2] if fmt == "int4_g128" else None, rows)
+        assert_close(Y[:, rows], ref, "%s K=%d N=%d M=%d" % (fmt, K, N, M))

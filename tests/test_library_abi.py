@@ -1,0 +1,104 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every entry point the header
+declares, and its host-side logic (argument validation, dispatch table, workspace size)
+behaves as documented.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_weight_quantized_wq_gb300 import binding
+from bit_weight_quantized_wq_gb300 import build as wqbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wq.h")
+
+
+def _stale():
+    lib = binding.LIB_PATH
+    if not os.path.exists(lib):
+        return True
+    t = os.path.getmtime(lib)
+    srcs = [os.path.join(wqbuild.CSRC, f) for f in os.listdir(wqbuild.CSRC)] + [HEADER]
+    return any(os.path.getmtime(s) > t for s in srcs)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if _stale():
+        wqbuild.build()
+    return binding.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(wq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("wq_quantize_int4_g128", "wq_quantize_mxfp4", "wq_gemm_w4a16", "wq_gemm_workspace_bytes",
+              "wq_status_str", "wq_set_dispatch_threshold"):
+        assert n in names
+    assert set(names) == set(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert binding.status_str(s).startswith("WQ_")
+    assert "unknown" in binding.status_str(99)
+
+
+FAKE = ctypes.c_void_p(0x10000)       # aligned, never dereferenced: validation fails first
+ODD = ctypes.c_void_p(0x10008)
+
+
+def _gemm(lib, fmt=0, X=FAKE, M=1, K=128, N=8, Wq=FAKE, s=FAKE, z=FAKE, Y=FAKE, ws=None, wsb=0):
+    return lib.wq_gemm_w4a16(fmt, X, M, K, N, Wq, s, z, Y, ws, wsb, None)
+
+
+def test_validation_errors(lib):
+    assert _gemm(lib, X=None) == 1                      # NULL
+    assert _gemm(lib, z=None) == 1                      # INT4 needs zeros
+    assert _gemm(lib, fmt=1) == 7                       # MXFP4 must not get zeros
+    assert _gemm(lib, fmt=5) == 7                       # bad format
+    assert _gemm(lib, M=0) == 2
+    assert _gemm(lib, N=0) == 2
+    assert _gemm(lib, K=64) == 2                        # INT4: K % 128
+    assert _gemm(lib, fmt=1, z=None, K=48) == 2         # MXFP4: K % 32
+    assert _gemm(lib, X=ODD) == 3                       # alignment
+    assert _gemm(lib, Y=ODD) == 3
+    assert lib.wq_gemv_w4a16(0, FAKE, 17, 128, 8, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 2  # decode: M <= 16
+    assert lib.wq_quantize_int4_g128(None, 4, 128, FAKE, FAKE, FAKE, None) == 1
+    assert lib.wq_quantize_int4_g128(FAKE, 4, 96, FAKE, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_mxfp4(FAKE, 4, 48, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_mxfp4(FAKE, 0, 64, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_mxfp4(ODD, 4, 64, FAKE, FAKE, None) == 3
+
+
+def test_workspace_checked_before_launch(lib):
+    need = lib.wq_gemm_workspace_bytes(0, 1, 4096, 4096)
+    assert need > 0
+    r = lib.wq_gemv_w4a16(0, FAKE, 1, 4096, 4096, FAKE, FAKE, FAKE, FAKE, None, 0, None)
+    assert r == 4
+    r = lib.wq_gemv_w4a16(0, FAKE, 1, 4096, 4096, FAKE, FAKE, FAKE, FAKE, FAKE, need - 1, None)
+    assert r == 4
+    assert lib.wq_gemm_workspace_bytes(9, 1, 128, 128) == 0
+    assert lib.wq_gemm_workspace_bytes(0, 0, 128, 128) == 0
+
+
+def test_dispatch_threshold_table(lib):
+    assert binding.dispatch_threshold("int4_g128", 4096, 4096) == 16
+    binding.set_dispatch_threshold("int4_g128", 4096, 4096, 4)
+    assert binding.dispatch_threshold("int4_g128", 4096, 4096) == 4
+    assert binding.dispatch_threshold("int4_g128", 4096, 8192) == 16
+    assert binding.dispatch_threshold("mxfp4", 4096, 4096) == 16
+    binding.set_dispatch_threshold("int4_g128", 4096, 4096, 16)
+    with pytest.raises(ValueError):
+        binding.set_dispatch_threshold("int4_g128", 4096, 4096, 17)
+    assert lib.wq_set_dispatch_threshold(3, 0, 0, 1) == 7
