@@ -1,4 +1,25 @@
-// Prefill kernel (tcgen05 / TMEM tensor cores): under construction.
+// Prefill kernel: Y[M, N] = X[M, K] * dequant(Wq)^T on the 5th-generation tensor cores.
+//
+// Compute-bound (第 1 章：推理加速全景 §1.3: prefill GEMMs run at 55-100 FLOP/B), so this is a
+// dense contraction on tcgen05 with the dequantization fused in front of the tensor core
+// (推理优化与量化算子深度技术调研 §1.2: "x_deq = (q - zp) * scale", done before the MMA).
+//
+// Swap-AB formulation, one 128 (weights) x 256 (activations) tile per CTA:
+//   D[n, m] = sum_k What[n, k] * X[m, k]            (D = Y^T, fp32 in tensor memory)
+//   A = What tile [128 x 64] -- dequantized by 128 threads (one per weight row = one TMEM
+//       lane) and written straight into tensor memory with tcgen05.st: no shared-memory
+//       round trip for the dequantized operand.
+//   B = X tile [256 x 64]    -- TMA, 128-byte swizzle, K-major, read by the MMA from smem.
+//   MMA = tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, issued by one thread.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2-5 dequant
+// (then epilogue: tcgen05.ld -> scale -> bf16 -> global).
+//
+// Operand types.  MXFP4: w_hat = E2M1 * 2^e is exact in bf16, so the MMA runs in bf16 on X
+// as given.  INT4: (q - z) * s needs up to 15 significant bits; rounding it to bf16 (8 bits)
+// would put the layer outside 1e-2 (1 + |y|) of the float64 result at K = 4096..29568, so
+// the MMA runs in fp16 (11 bits): a pre-pass converts X exactly to fp16, each row scaled by a
+// power of two 2^-k_m chosen so that |x| 2^-k_m < 2^15 (k_m = 0 for ordinary activations),
+// and the epilogue multiplies row m of Y by 2^k_m.
 #include "internal.h"
 
 namespace wq {
@@ -12,11 +33,444 @@ uint32_t gemm_tc_read_and_clear_error() {
   return v;
 }
 
-size_t gemm_tc_workspace_bytes(int, int64_t, int64_t, int64_t) { return 0; }
+namespace tc {
 
-cudaError_t launch_gemm_tc(int, const uint16_t*, int64_t, int64_t, int64_t, const int32_t*, const void*,
-                           const uint16_t*, uint16_t*, void*, size_t, cudaStream_t) {
-  return cudaErrorNotSupported;
+constexpr int BN = 128;          // weight rows per tile (MMA M)
+constexpr int BM = 256;          // activation rows per tile (MMA N)
+constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of 16-bit X)
+constexpr int kStages = 4;
+constexpr int kXBytes = BM * BK * 2;        // 32 KB
+constexpr int kWBytes = BN * BK / 2;        // 4 KB packed weights
+constexpr int kThreads = 192;               // 6 warps
+constexpr int kTmemCols = 512;
+constexpr int kAccCol = 0;                  // D: columns [0, 256)
+constexpr int kACol = 256;                  // A stage s: columns [256 + 32 s, +32)
+constexpr int kGroupM = 8;                  // tile raster: 8 activation tiles per group
+
+struct Smem {
+  uint8_t x[kStages][kXBytes];    // 1024-aligned (SWIZZLE_128B atoms)
+  uint8_t w[kStages][kWBytes];
+  uint64_t full[kStages];
+  uint64_t a_ready[kStages];
+  uint64_t empty[kStages];
+  uint64_t accum_full;
+  uint32_t tmem_base;
+};
+
+struct Params {
+  const void* scales;
+  const uint16_t* zeros;
+  const float* xscale;   // INT4: 2^k_m per activation row (nullptr for MXFP4)
+  uint16_t* Y;
+  int M, K, N;
+  int KB;                // MXFP4 scale bytes per row (K / 32)
+  int G;                 // INT4 groups per row (K / 128)
+  int tiles_n, tiles_m;
+  int k_stages;          // ceil(K / BK)
+};
+
+// ------------------------------------------------------------------------ tcgen05 helpers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Each thread stores 32 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3ffffu) >> 4);      // start address
+  d |= static_cast<uint64_t>(16 >> 4) << 16;                 // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                       // descriptor version (sm_100 family)
+  d |= static_cast<uint64_t>(2) << 61;                       // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A/B K-major, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt /*0 f16, 1 bf16*/) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t(BM) >> 3) << 17) | ((uint32_t(BN) >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t d;
+  const unsigned short h = static_cast<unsigned short>(byte);
+  asm("{\n\t.reg .b8 t, u;\n\tmov.b16 {t, u}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(d) : "h"(h));
+  return d;
+}
+__device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
+  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+// Tile index -> (n tile, m tile), grouped so that a wave of CTAs shares activation tiles
+// (kGroupM of them) and weight tiles in L2.
+__device__ __forceinline__ void tile_coords(int t, int tiles_n, int tiles_m, int& tn, int& tm) {
+  const int per_group = kGroupM * tiles_n;
+  const int grp = t / per_group;
+  const int first_m = grp * kGroupM;
+  const int gsize = min(tiles_m - first_m, kGroupM);
+  const int r = t % per_group;
+  tm = first_m + r % gsize;
+  tn = r / gsize;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+              const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int tn, tm;
+  tile_coords(blockIdx.x, p.tiles_n, p.tiles_m, tn, tm);
+  const int n0 = tn * BN, m0 = tm * BM;
+  const int KS = p.k_stages;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.a_ready[s], 128);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.accum_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_x);
+      tma_prefetch_desc(&tmap_w);
+      const uint64_t pol_x = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_last();
+      int i = 0;
+      for (; i < KS; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!mbar_wait(&sm.empty[s], ph ^ 1, &g_gemm_err, kErrWaitEmpty)) break;
+        mbar_arrive_expect_tx(&sm.full[s], kXBytes + kWBytes);
+        tma_load_2d(&sm.x[s][0], &tmap_x, i * BK, m0, &sm.full[s], pol_x);
+        tma_load_2d(&sm.w[s][0], &tmap_w, i * (BK / 2), n0, &sm.full[s], pol_w);
+      }
+      for (int j = i - kStages; j < i; ++j) {  // drain: the last fill of each slot landed
+        if (j < 0) continue;
+        mbar_wait(&sm.full[j % kStages], (j / kStages) & 1, &g_gemm_err, kErrDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u);
+      bool ok = true;
+      for (int i = 0; i < KS; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        if (!mbar_wait(&sm.full[s], ph, &g_gemm_err, kErrWaitFull) ||
+            !mbar_wait(&sm.a_ready[s], ph, &g_gemm_err, kErrWaitFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t bdesc = smem_desc_sw128(smem_u32(&sm.x[s][0]));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          tc_mma_ts(tmem + kAccCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&sm.empty[s]);
+      }
+      // Always commit: the epilogue (normal path) and the TMEM release below (any path)
+      // must not run before every issued MMA has completed.
+      tc_commit(&sm.accum_full);
+      mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum);
+      (void)ok;
+    }
+  } else {
+    // -------------------------------------------------------------- dequant, then epilogue
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;            // weight row inside the tile == TMEM lane
+    const int n = n0 + r;
+    const bool row_ok = n < p.N;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    bool ok = true;
+    for (int i = 0; i < KS; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      uint32_t a[32];
+      // metadata of this stage (loaded before the waits)
+      uint32_t s2 = 0, zz = 0;          // INT4: f16x2 scale, f16x2 (1024 + z)
+      uint32_t e2 = 0;                  // MXFP4: two E8M0 bytes
+      const int k0 = i * BK;
+      if constexpr (FMT == kInt4G128) {
+        const int g = k0 / 128;
+        uint16_t sb = 0, zb = 0;
+        if (row_ok) {
+          sb = reinterpret_cast<const uint16_t*>(p.scales)[static_cast<long long>(n) * p.G + g];
+          zb = p.zeros[static_cast<long long>(n) * p.G + g];
+        }
+        s2 = static_cast<uint32_t>(sb) | (static_cast<uint32_t>(sb) << 16);
+        const __half zh = __float2half_rn(1024.f + __half2float(__ushort_as_half(zb)));
+        const uint32_t zu = __half_as_ushort(zh);
+        zz = zu | (zu << 16);
+      } else {
+        const int b = k0 / 32;
+        if (row_ok) {
+          const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(n) * p.KB;
+          const uint32_t lo = (b < p.KB) ? E[b] : 0u;
+          const uint32_t hi = (b + 1 < p.KB) ? E[b + 1] : 0u;
+          e2 = lo | (hi << 8);
+        }
+      }
+      if (!mbar_wait(&sm.full[s], ph, &g_gemm_err, kErrWaitFull)) { ok = false; break; }
+      const uint4* wrow = reinterpret_cast<const uint4*>(&sm.w[s][r * (BK / 2)]);
+      const uint4 v0 = wrow[0], v1 = wrow[1];
+      const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      if constexpr (FMT == kInt4G128) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w = wv[j], w4 = wv[j] >> 4;
+          // natural k order: (n0,n1) (n2,n3) (n4,n5) (n6,n7) as fp16 1024 + q
+          const uint32_t p0 = lop3_and_or(prmt(w, w4, 0x4400), 0x000f000fu, 0x64006400u);
+          const uint32_t p1 = lop3_and_or(prmt(w, w4, 0x5511), 0x000f000fu, 0x64006400u);
+          const uint32_t p2 = lop3_and_or(prmt(w, w4, 0x6622), 0x000f000fu, 0x64006400u);
+          const uint32_t p3 = lop3_and_or(prmt(w, w4, 0x7733), 0x000f000fu, 0x64006400u);
+          a[4 * j + 0] = hmul2_u(hsub2_u(p0, zz), s2);
+          a[4 * j + 1] = hmul2_u(hsub2_u(p1, zz), s2);
+          a[4 * j + 2] = hmul2_u(hsub2_u(p2, zz), s2);
+          a[4 * j + 3] = hmul2_u(hsub2_u(p3, zz), s2);
+        }
+      } else {
+        const float f0 = e8m0_to_f32(e2 & 0xffu), f1 = e8m0_to_f32(e2 >> 8);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float f = j < 4 ? f0 : f1;
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const uint32_t h2 = e2m1x2_to_f16x2((wv[j] >> (8 * bb)) & 0xffu);
+            const float lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu))) * f;
+            const float hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))) * f;
+            __nv_bfloat162 bv = __floats2bfloat162_rn(lo, hi);
+            a[4 * j + bb] = *reinterpret_cast<uint32_t*>(&bv);
+          }
+        }
+      }
+      // The A slot is free once the MMAs of its previous use completed.
+      if (!mbar_wait(&sm.empty[s], ph ^ 1, &g_gemm_err, kErrWaitEmpty)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st32(tmem + lane_base + kACol + 32 * s, a);
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.a_ready[s]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BM; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kAccCol + c, v);
+        tc_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c + j;
+            if (m < p.M) {
+              float y = __uint_as_float(v[j]);
+              if constexpr (FMT == kInt4G128) y *= __ldg(p.xscale + m);
+              p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            }
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// X (bf16) -> fp16 with a per-row power-of-two scale: |x| 2^-k < 2^15, k >= 0; writes
+// xs[m] = 2^k.  One CTA per row; the row is read twice (max, then convert), the second
+// time from L2.
+__global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X, int K, uint16_t* __restrict__ Xh,
+                                                  float* __restrict__ xs) {
+  const int m = blockIdx.x;
+  const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<long long>(m) * K);
+  uint4* out = reinterpret_cast<uint4*>(Xh + static_cast<long long>(m) * K);
+  const int nv = K / 8;
+  uint32_t mx = 0u;
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 r = __ldg(row + v);
+    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  __shared__ uint32_t red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0u;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) mx = max(mx, red[w]);
+  const int ex = static_cast<int>(mx >> 7) - 127;
+  const int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+    const uint4 r = __ldg(row + v);
+    const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      __half2 h = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv, __uint_as_float(w4[q] & 0xffff0000u) * inv);
+      o[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    out[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (threadIdx.x == 0) xs[m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+
+}  // namespace tc
+
+size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
+  (void)N;
+  if (fmt != kInt4G128) return 0;
+  const size_t xh = ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
+  return xh + ((static_cast<size_t>(M) * 4 + 255) / 256) * 256;
+}
+
+cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                           const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream) {
+  using namespace tc;
+  if (ws_bytes < gemm_tc_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
+  Params p{};
+  p.scales = scales;
+  p.zeros = zeros;
+  p.Y = Y;
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.KB = static_cast<int>(K / 32);
+  p.G = static_cast<int>(K / 128);
+  p.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  p.tiles_m = static_cast<int>((M + BM - 1) / BM);
+  p.k_stages = static_cast<int>((K + BK - 1) / BK);
+
+  const void* xsrc = X;
+  if (fmt == kInt4G128) {
+    uint16_t* Xh = reinterpret_cast<uint16_t*>(ws);
+    float* xs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
+                                         ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256);
+    k_x_to_f16<<<static_cast<unsigned>(M), 256, 0, stream>>>(X, static_cast<int>(K), Xh, xs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    xsrc = Xh;
+    p.xscale = xs;
+  }
+  CUtensorMap tx, tw;
+  cudaError_t e = make_tmap_2d(&tx, fmt == kInt4G128 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                               xsrc, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2,
+                               BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N),
+                   static_cast<uint64_t>(K / 2), BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Smem) + 1024;
+  const unsigned grid = static_cast<unsigned>(p.tiles_n) * static_cast<unsigned>(p.tiles_m);
+  if (fmt == kInt4G128) {
+    e = cudaFuncSetAttribute(k_gemm_tc<kInt4G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_gemm_tc<kInt4G128><<<grid, kThreads, smem, stream>>>(tx, tw, p);
+  } else {
+    e = cudaFuncSetAttribute(k_gemm_tc<kMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_gemm_tc<kMxfp4><<<grid, kThreads, smem, stream>>>(tx, tw, p);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace wq

@@ -1,0 +1,115 @@
+"""tcgen05 tensor-core kernel against the float64 oracle on the same dequantized weights."""
+import numpy as np
+import pytest
+
+from bit_weight_quantized_wq_gb300 import inputs
+from oracle import int4_g128, linear, mxfp4
+from tests._util import assert_close, to_dev, x_to_dev, y_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import torch
+    from bit_weight_quantized_wq_gb300 import binding
+    binding.check_device()
+    torch.cuda.init()
+    return binding
+
+
+def _pack(fmt, W):
+    return int4_g128.quantize(W) if fmt == "int4_g128" else mxfp4.quantize(W)
+
+
+def _run(fn, fmt, xbits, pk):
+    X = x_to_dev(xbits)
+    d = [to_dev(a) for a in pk]
+    if fmt == "int4_g128":
+        return fn(fmt, X, d[0], d[1], d[2])
+    return fn(fmt, X, d[0], d[1])
+
+
+# (M, N, K): single tile, ragged M/N, several tiles in both directions, long K.
+CASES = [(1, 128, 128), (256, 128, 128), (17, 200, 256), (300, 384, 512), (513, 1000, 1024),
+         (64, 256, 4096), (1024, 512, 2048)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M,N,K", CASES)
+def test_gemm_tc_small(B, fmt, M, N, K):
+    W = inputs.weights(N * 3 + K, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M + K, M, K)
+    Y = _run(B.gemm_tc_w4a16, fmt, xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16(fmt, xf, *pk), "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+@pytest.mark.parametrize("K", [32, 96, 160])
+def test_gemm_tc_mxfp4_k_tail(B, K):
+    M, N = 100, 300
+    W = inputs.weights(K + 5, N, K, 0.05)
+    pk = mxfp4.quantize(W)
+    xb, xf = inputs.activations(K + 6, M, K)
+    Y = _run(B.gemm_tc_w4a16, "mxfp4", xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16("mxfp4", xf, *pk), "mxfp4 K=%d" % K)
+
+
+def test_gemm_tc_int4_large_activations(B):
+    # Activations beyond the fp16 range: the per-row power-of-two scaling keeps them exact.
+    M, N, K = 64, 256, 512
+    W = inputs.weights(7, N, K, 0.05)
+    pk = int4_g128.quantize(W)
+    xb, xf = inputs.activations(8, M, K, scale=2.0e5)
+    Y = _run(B.gemm_tc_w4a16, "int4_g128", xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16("int4_g128", xf, *pk), "int4 big X")
+
+
+def test_dispatch_routes_by_m(B):
+    M, N, K = 20, 256, 512
+    W = inputs.weights(2, N, K, 0.05)
+    pk = int4_g128.quantize(W)
+    for m in (1, 16, 17, 20):
+        xb, xf = inputs.activations(m, m, K)
+        Y = _run(B.gemm_w4a16, "int4_g128", xb, pk)
+        assert_close(y_to_host(Y), linear.linear_w4a16("int4_g128", xf, *pk), "dispatch M=%d" % m)
+
+
+# Full-size prefill shapes (K, N) at M = 2048 (and one at 8192): 256 sampled output columns.
+PREFILL = [(8192, 10240), (8192, 8192), (8192, 59136), (29568, 8192)]
+
+
+@pytest.mark.parametrize("K,N", PREFILL)
+def test_gemm_tc_full_size_sampled(B, K, N):
+    W = inputs.weights(3000 + K % 97 + N % 89, N, K, 0.015)
+    pk = int4_g128.quantize(W)
+    rows = np.sort(np.random.default_rng(K * 7 + N).choice(N, 256, replace=False))
+    M = 2048
+    xb, xf = inputs.activations(K + N, M, K)
+    Y = y_to_host(_run(B.gemm_tc_w4a16, "int4_g128", xb, pk))
+    ref = linear.linear_rows("int4_g128", xf, pk[0], pk[1], pk[2], rows)
+    assert_close(Y[:, rows], ref, "int4 K=%d N=%d M=%d" % (K, N, M))
+    assert B.read_error_flags() == 0
+
+
+def test_gemm_tc_full_size_m8192_sampled(B):
+    K, N, M = 8192, 8192, 8192
+    W = inputs.weights(3001, N, K, 0.015)
+    pk = int4_g128.quantize(W)
+    rows = np.sort(np.random.default_rng(5).choice(N, 128, replace=False))
+    xb, xf = inputs.activations(3002, M, K)
+    Y = y_to_host(_run(B.gemm_tc_w4a16, "int4_g128", xb, pk))
+    ref = linear.linear_rows("int4_g128", xf, pk[0], pk[1], pk[2], rows)
+    assert_close(Y[:, rows], ref, "int4 M=8192")
+
+
+@pytest.mark.parametrize("M", [64, 512, 2048])
+def test_gemm_tc_mxfp4_crossover_shape(B, M):
+    K = N = 8192
+    W = inputs.weights(4000, N, K, 0.02)
+    pk = mxfp4.quantize(W)
+    rows = np.sort(np.random.default_rng(M).choice(N, 256, replace=False))
+    xb, xf = inputs.activations(4000 + M, M, K)
+    Y = y_to_host(_run(B.gemm_tc_w4a16, "mxfp4", xb, pk))
+    ref = linear.linear_rows("mxfp4", xf, pk[0], pk[1], None, rows)
+    assert_close(Y[:, rows], ref, "mxfp4 M=%d" % M)
