@@ -44,10 +44,14 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void
 }
 
 int device_sm_count() {
+  static int cached[64] = {0};
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  if (n <= 0) return 1;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 }  // namespace wq

@@ -461,15 +461,21 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem) + 1024;
   const unsigned grid = static_cast<unsigned>(p.tiles_n) * static_cast<unsigned>(p.tiles_m);
-  if (fmt == kInt4G128) {
-    e = cudaFuncSetAttribute(k_gemm_tc<kInt4G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static bool attr_set[2][64] = {{false}};  // once per (format, device)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int fi = fmt == kInt4G128 ? 0 : 1;
+  if (dev < 0 || dev >= 64 || !attr_set[fi][dev]) {
+    e = fmt == kInt4G128
+            ? cudaFuncSetAttribute(k_gemm_tc<kInt4G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))
+            : cudaFuncSetAttribute(k_gemm_tc<kMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k_gemm_tc<kInt4G128><<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  } else {
-    e = cudaFuncSetAttribute(k_gemm_tc<kMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    k_gemm_tc<kMxfp4><<<grid, kThreads, smem, stream>>>(tx, tw, p);
+    if (dev >= 0 && dev < 64) attr_set[fi][dev] = true;
   }
+  if (fmt == kInt4G128)
+    k_gemm_tc<kInt4G128><<<grid, kThreads, smem, stream>>>(tx, tw, p);
+  else
+    k_gemm_tc<kMxfp4><<<grid, kThreads, smem, stream>>>(tx, tw, p);
   return cudaGetLastError();
 }
 

@@ -572,8 +572,14 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tmap, const gemv::Params& p,
   using S = gemv::Smem<FMT, MT>;
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};  // once per device
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   kern<<<p.P, gemv::kThreads, smem, stream>>>(tmap, p);
   return cudaGetLastError();
 }
