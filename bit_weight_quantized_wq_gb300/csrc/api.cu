@@ -164,6 +164,7 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
   if (M > 16) return WQ_ERR_SHAPE;
+  if ((N + 255) / 256 > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
   if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;

@@ -418,7 +418,7 @@ size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   (void)N;
   if (fmt != kInt4G128) return 0;
   const size_t xh = ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
-  return xh + ((static_cast<size_t>(M) * 4 + 255) / 256) * 256;
+  return kWsCounterBytes + xh + ((static_cast<size_t>(M) * 4 + 255) / 256) * 256;
 }
 
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -441,9 +441,9 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
 
   const void* xsrc = X;
   if (fmt == kInt4G128) {
-    uint16_t* Xh = reinterpret_cast<uint16_t*>(ws);
-    float* xs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) +
-                                         ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256);
+    uint8_t* base = reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes;  // never touch the counter header
+    uint16_t* Xh = reinterpret_cast<uint16_t*>(base);
+    float* xs = reinterpret_cast<float*>(base + ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256);
     k_x_to_f16<<<static_cast<unsigned>(M), 256, 0, stream>>>(X, static_cast<int>(K), Xh, xs);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

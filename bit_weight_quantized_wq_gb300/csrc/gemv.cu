@@ -562,9 +562,8 @@ size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   const long long G = (K + gemv::kGroupK - 1) / gemv::kGroupK;
   const long long bands = (N + gemv::kBand - 1) / gemv::kBand;
   const int P = gemv::num_ctas(bands * G);
-  const size_t cnt_bytes = ((bands * 4 + 255) / 256) * 256;
   (void)fmt;
-  return cnt_bytes + static_cast<size_t>(P) * 2 * MT * gemv::kBand * sizeof(float);
+  return kWsCounterBytes + static_cast<size_t>(P) * 2 * MT * gemv::kBand * sizeof(float);
 }
 
 template <int FMT, int MT>
@@ -600,10 +599,10 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
   p.bands = static_cast<int>((N + gemv::kBand - 1) / gemv::kBand);
   p.U = static_cast<long long>(p.bands) * p.G;
   p.P = gemv::num_ctas(p.U);
-  const size_t cnt_bytes = ((static_cast<size_t>(p.bands) * 4 + 255) / 256) * 256;
+  if (p.bands > kWsMaxCounters) return cudaErrorInvalidValue;
   if (ws_bytes < gemv_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
-  p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + cnt_bytes);
+  p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
   CUtensorMap tmap;
   cudaError_t e = make_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2),

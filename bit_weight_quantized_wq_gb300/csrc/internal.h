@@ -21,6 +21,12 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void
 
 int device_sm_count();
 
+// Every workspace layout starts with this fixed header of split-K counters.  Only the
+// decode kernel touches it and every call leaves it at zero, so one workspace zeroed once
+// can be shared by calls of any shape and by both kernels.
+constexpr size_t kWsCounterBytes = 64 * 1024;
+constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
+
 // quantize.cu
 cudaError_t launch_quant_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq, uint16_t* scales,
                                    uint16_t* zeros, cudaStream_t stream);

@@ -85,8 +85,9 @@ wq_status wq_quantize_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq,
 
 /*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
- * The workspace must be zero-filled once before its first use (it holds reduction
- * counters); every call that completes leaves those counters at zero again.  One workspace
+ * Every layout starts with the same 64 KiB header of split-K counters.  Zero the
+ * workspace once before its first use; every call that completes leaves the header at zero
+ * again, so one workspace can serve calls of any shape and either kernel.  One workspace
  * must not be used by two calls that can run at the same time.  Returns 0 for invalid
  * arguments.
  */
@@ -115,7 +116,8 @@ wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
                         uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 16).
+ * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 16
+ * and N <= 4194304).
  * Streams the packed weights with TMA, unpacks in registers and applies the group scale in
  * fp32 after exact integer-valued tensor-core products; the zero point enters as (q - z),
  * the cross term of 第 6 课：量化源码走读 §3.

@@ -67,6 +67,20 @@ def test_gemv_mxfp4_large_activations(B):
     assert_close(y_to_host(Y), linear.linear_w4a16("mxfp4", xf, *pk), "mxfp4 big X")
 
 
+def test_gemv_workspace_shared_across_shapes_and_kernels(B):
+    # One workspace, zeroed once, serves calls of different shapes and both kernels.
+    import torch
+    ws = torch.zeros(B.gemm_workspace_bytes("int4_g128", 256, 4096, 28672), dtype=torch.uint8, device="cuda")
+    for (M, K, N) in [(4, 4096, 6144), (256, 4096, 512), (1, 4096, 28672), (16, 14336, 4096), (1, 4096, 28672)]:
+        W = inputs.weights(N + K, N, K, 0.02)
+        pk = int4_g128.quantize(W)
+        xb, xf = inputs.activations(M, M, K)
+        d = [to_dev(a) for a in pk]
+        Y = y_to_host(B.gemm_w4a16("int4_g128", x_to_dev(xb), d[0], d[1], d[2], workspace=ws))
+        rows = np.arange(0, N, max(1, N // 300))
+        assert_close(Y[:, rows], linear.linear_rows("int4_g128", xf, pk[0], pk[1], pk[2], rows), "M=%d N=%d" % (M, N))
+
+
 def test_gemv_deterministic_and_workspace_reusable(B):
     M, N, K = 4, 4096, 4096
     W = inputs.weights(9, N, K, 0.02)
