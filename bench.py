@@ -73,6 +73,24 @@ def profile_traffic(kernel_file, key):
         return None
 
 
+# ----------------------------------------------------------------------------------- ranks
+def max_over_ranks(value, device=None):
+    """The largest of every rank's value (a no-op without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, step_bytes, steps, ms_max):
+    """Whole-job GB/s: every rank streams step_bytes per step; time is the slowest rank's."""
+    return world * step_bytes * steps / (ms_max * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
@@ -284,12 +302,8 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     barrier()
     clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * step_bytes * args.steps / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    value = replica_throughput(world, step_bytes, args.steps, ms)
     ms_step = ms / args.steps
 
     # ---------------- e2e through the public API with host buffers (no graph)
