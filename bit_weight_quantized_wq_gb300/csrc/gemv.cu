@@ -8,10 +8,12 @@
 // Structure (one persistent CTA per SM, warp-specialised):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
 //               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4-stage smem ring.
-//   warp 1      X-prep: stages the activations of the same k-range in the exact order of the
-//               mma.sync B fragments (MXFP4: converted to fp16 with a per-row power-of-two
-//               scale that keeps every value in fp16 range).
-//   warps 2..9  consumers: 32 weight rows each; unpack nibbles in registers, tensor-core
+//   warps 1-2   prep (stage i by prep warp i % 2): the activations of the stage's k-range in
+//               the exact order of the mma.sync B fragments (MXFP4: converted to fp16 with a
+//               per-row power-of-two scale that keeps every value in fp16 range), plus the
+//               scales / zero points (INT4) or E8M0 bytes (MXFP4) of the stage's rows.  The
+//               consumers then touch only shared memory in their main loop.
+//   warps 3-10  consumers: 32 weight rows each; unpack nibbles in registers, tensor-core
 //               mma.sync with fp32 accumulation, group scale applied in fp32 afterwards.
 //
 // Exactness: the tensor-core operands are exact small integers (INT4: q - z in bf16) or
@@ -45,7 +47,9 @@ constexpr int kConsumerWarps = 8;
 constexpr int kBand = 32 * kConsumerWarps;          // weight rows per CTA tile
 constexpr int kStages = 4;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
-constexpr int kThreads = 32 * (2 + kConsumerWarps);  // 320
+constexpr int kPrepWarps = 2;                        // stage i is prepared by prep warp i % 2
+constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
+constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 352
 constexpr int kGroupK = 128;                         // k per unit (one INT4 group)
 
 struct Params {
@@ -104,6 +108,9 @@ struct Smem {
   uint8_t w[kStages][kTileBytes];
   uint4 x[kStages][NT][2][4][32];
   float xf[kStages][MT];          // MXFP4: power-of-two factor per activation row
+  // Per-row metadata of the stage's two groups, staged by the prep warps:
+  //   INT4:  {scale as float, bf16x2 (128 + z) bits}    MXFP4: {four E8M0 bytes, unused}
+  float2 meta[kStages][2][kBand];
   uint64_t full_w[kStages];
   uint64_t full_x[kStages];
   uint64_t empty[kStages];
@@ -211,17 +218,68 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       (void)ok;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ X-prep
+  } else if (warp < kFirstConsumer) {
+    // ------------------------------------------------------------------ prep
+    const int pw = warp - 1;
     StageIter it;
     it.init(u0, u1, p.G);
     const int t = lane & 3;
     for (int i = 0; !it.done(); it.next(), ++i) {
+      if (i % kPrepWarps != pw) continue;
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
       if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
       const int ng = it.ng();
       const int g0 = it.g0();
+      const int band = it.band();
+      // metadata of the stage's rows: lane handles rows lane + 32 q
+      {
+        uint32_t ma[8][2], mb[8][2];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int row = band * kBand + lane + 32 * q;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const bool live = (row < p.N) && (h < ng);
+            if constexpr (FMT == kInt4G128) {
+              const long long idx = static_cast<long long>(row) * p.G + g0 + h;
+              ma[q][h] = live ? __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx) : 0u;
+              mb[q][h] = live ? __ldg(reinterpret_cast<const unsigned short*>(p.zeros) + idx) : 0u;
+            } else {
+              const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
+              const int b0 = (g0 + h) * 4;
+              uint32_t v = 0u;
+              if (live) {
+                if ((p.KB & 3) == 0) {
+                  v = __ldg(reinterpret_cast<const uint32_t*>(E + b0));
+                } else {
+#pragma unroll
+                  for (int q2 = 0; q2 < 4; ++q2)
+                    if (b0 + q2 < p.KB) v |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
+                }
+              }
+              ma[q][h] = v;
+              mb[q][h] = 0u;
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float2 m2;
+            if constexpr (FMT == kInt4G128) {
+              m2.x = __half2float(__ushort_as_half(static_cast<unsigned short>(ma[q][h])));
+              const float z = __half2float(__ushort_as_half(static_cast<unsigned short>(mb[q][h])));
+              const uint32_t zb = __bfloat16_as_ushort(__float2bfloat16_rn(128.f + z));
+              m2.y = __uint_as_float(zb | (zb << 16));
+            } else {
+              m2.x = __uint_as_float(ma[q][h]);
+              m2.y = 0.f;
+            }
+            sm.meta[slot][h][lane + 32 * q] = m2;
+          }
+      }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int m = (lane >> 2) + 8 * nt;
@@ -293,10 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ consumers
-    const int cw = warp - 2;
+    const int cw = warp - kFirstConsumer;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int tid = threadIdx.x - 64;  // 0..255
+    const int tid = threadIdx.x - 32 * kFirstConsumer;  // 0..255
     // Rows (inside the band) of this lane: [row-tile][fragment half]
     int rrow[2][2];
 #pragma unroll
@@ -323,7 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g0 = it.g0();
       const int ng = it.ng();
 
-      // Scales / zero points of this stage (issued before the waits so they overlap them).
+      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
+      if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
+
+      // Scales / zero points (INT4) or E8M0 bytes (MXFP4) of this lane's rows, from smem.
       float sc[2][2][2];          // [h][rt][hf]
       uint32_t zz[2][2][2];       // INT4: bf16x2 (128 + z)
       uint32_t e8[2][2][2];       // MXFP4: four E8M0 bytes of the group
@@ -333,36 +394,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            const int row = band * kBand + rrow[rt][hf];
-            const bool live = (row < p.N) && (h < ng);
-            if constexpr (FMT == kInt4G128) {
-              const long long idx = static_cast<long long>(row) * p.G + g0 + h;
-              const __half* S = reinterpret_cast<const __half*>(p.scales);
-              const __half* Z = reinterpret_cast<const __half*>(p.zeros);
-              const float s = live ? __half2float(S[idx]) : 0.f;
-              const float z = live ? __half2float(Z[idx]) : 0.f;
-              sc[h][rt][hf] = s;
-              const uint32_t zb = __bfloat16_as_ushort(__float2bfloat16_rn(128.f + z));
-              zz[h][rt][hf] = zb | (zb << 16);
-            } else {
-              const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
-              const int b0 = (g0 + h) * 4;
-              uint32_t v = 0u;
-              if (live) {
-                if ((p.KB & 3) == 0) {
-                  v = __ldg(reinterpret_cast<const uint32_t*>(E + b0));
-                } else {
-#pragma unroll
-                  for (int q = 0; q < 4; ++q)
-                    if (b0 + q < p.KB) v |= static_cast<uint32_t>(__ldg(E + b0 + q)) << (8 * q);
-                }
-              }
-              e8[h][rt][hf] = v;
-            }
+            const float2 m2 = sm.meta[slot][h][rrow[rt][hf]];
+            sc[h][rt][hf] = m2.x;
+            zz[h][rt][hf] = __float_as_uint(m2.y);
+            e8[h][rt][hf] = __float_as_uint(m2.x);
           }
-
-      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
-      if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
 
       const uint8_t* wt = &sm.w[slot][0];
 #pragma unroll

@@ -70,8 +70,10 @@ def test_gemv_mxfp4_large_activations(B):
 def test_gemv_workspace_shared_across_shapes_and_kernels(B):
     # One workspace, zeroed once, serves calls of different shapes and both kernels.
     import torch
-    ws = torch.zeros(B.gemm_workspace_bytes("int4_g128", 256, 4096, 28672), dtype=torch.uint8, device="cuda")
-    for (M, K, N) in [(4, 4096, 6144), (256, 4096, 512), (1, 4096, 28672), (16, 14336, 4096), (1, 4096, 28672)]:
+    shapes = [(4, 4096, 6144), (256, 4096, 512), (1, 4096, 28672), (16, 14336, 4096), (1, 4096, 28672)]
+    nbytes = max(B.gemm_workspace_bytes("int4_g128", M, K, N) for M, K, N in shapes)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for (M, K, N) in shapes:
         W = inputs.weights(N + K, N, K, 0.02)
         pk = int4_g128.quantize(W)
         xb, xf = inputs.activations(M, M, K)
