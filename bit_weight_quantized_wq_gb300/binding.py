@@ -29,7 +29,7 @@ _STATUS = {0: "WQ_OK", 1: "WQ_ERR_NULL", 2: "WQ_ERR_SHAPE", 3: "WQ_ERR_ALIGN", 4
 EXPORTED = [
     "wq_quantize_int4_g128", "wq_quantize_mxfp4", "wq_gemm_workspace_bytes", "wq_gemm_w4a16",
     "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
-    "wq_status_str", "wq_read_error_flags", "wq_check_device",
+    "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
 ]
 
 _lib = None
@@ -57,6 +57,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_status_str": (ctypes.c_char_p, [I32]),
         "wq_read_error_flags": (I32, [ctypes.POINTER(U32)]),
         "wq_check_device": (I32, []),
+        "wq_gemv_w4a16_noalloc": (I32, [I32, P, I64, I64, I64, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -203,6 +204,20 @@ def gemv_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=
 def gemm_tc_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
     """The tcgen05 tensor-core kernel alone (any M)."""
     return _linear("wq_gemm_tc_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
+
+
+def gemv_w4a16_noalloc(fmt, X, Wq, scales, zeros=None, out=None, stream=None):
+    """The decode kernel with the library's own fixed scratch: no workspace, no allocation
+    inside the library (``out`` is allocated here with torch when it is not given)."""
+    f = _fmt(fmt)
+    _need(X, torch.bfloat16, "X")
+    M, K = X.shape
+    N = Wq.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _check(load_library().wq_gemv_w4a16_noalloc(f, _ptr(X), M, K, N, _ptr(Wq), _ptr(scales), _ptr(zeros),
+                                                _ptr(out), _stream(stream)), "wq_gemv_w4a16_noalloc")
+    return out
 
 
 def dispatch_threshold(fmt, K: int, N: int) -> int:

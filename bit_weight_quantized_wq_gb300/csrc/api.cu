@@ -174,6 +174,21 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
                                    static_cast<cudaStream_t>(stream)));
 }
 
+wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Y,
+                                void* stream) {
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  if (M > 16) return WQ_ERR_SHAPE;
+  if ((N + 255) / 256 > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  // Shapes whose scratch would not fit the library's fixed array (possible only on a device
+  // with more SMs than it was sized for) are refused before anything is enqueued.
+  if (wq::gemv_workspace_bytes(fmt, M, K, N) > wq::gemv_noalloc_scratch_bytes()) return WQ_ERR_SHAPE;
+  return from_cuda(wq::launch_gemv_noalloc(fmt, X, M, K, N, Wq, scales, zeros, Y, static_cast<cudaStream_t>(stream)));
+}
+
 wq_status wq_gemm_tc_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace,
                            size_t ws_bytes, void* stream) {

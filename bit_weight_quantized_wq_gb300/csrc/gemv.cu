@@ -28,6 +28,8 @@
 // by several CTAs is reduced through the workspace (fp32 partials + one counter per band,
 // deterministic order: the last CTA to finish sums the partials in CTA order, writes bf16
 // and resets the counter).
+#include <mutex>
+
 #include "internal.h"
 
 namespace wq {
@@ -649,6 +651,52 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
   if (fmt == kInt4G128)
     return small ? launch_gemv_t<kInt4G128, 8>(tmap, p, stream) : launch_gemv_t<kInt4G128, 16>(tmap, p, stream);
   return small ? launch_gemv_t<kMxfp4, 8>(tmap, p, stream) : launch_gemv_t<kMxfp4, 16>(tmap, p, stream);
+}
+
+// ---------------------------------------------------------------------------------------
+// The decode kernel for callers that cannot allocate device memory.
+//
+// The split-K scratch of the decode kernel (reduction counters and fp32 partial sums) lives
+// here in one fixed, library-owned device array instead of a caller-provided workspace.  It
+// is sized for every decode shape the kernel accepts (M <= 16, N <= 4194304) on a device with
+// at most kNoAllocMaxCtas SMs: 64 KiB of counters + 8 MiB of partials.  Every GPU that loads
+// the library keeps this array until the process exits.
+// ---------------------------------------------------------------------------------------
+constexpr int kNoAllocMaxCtas = 256;
+constexpr size_t kNoAllocScratchBytes =
+    kWsCounterBytes + static_cast<size_t>(kNoAllocMaxCtas) * 2 * 16 * gemv::kBand * sizeof(float);
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t gemv_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                                const void* scales, const uint16_t* zeros, uint16_t* Y, cudaStream_t stream) {
+  // Set-up, once per device with that device current: the array's name is only a host-side
+  // handle, so the kernel gets the device address from cudaGetSymbolAddress.
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+      void* a = nullptr;
+      e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      addr[dev] = a;
+    }
+    scratch = addr[dev];
+  }
+  if (gemv_workspace_bytes(fmt, M, K, N) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  // The array keeps whatever the previous call left; the counters must start at zero.
+  const size_t bands = static_cast<size_t>((N + gemv::kBand - 1) / gemv::kBand);
+  e = cudaMemsetAsync(scratch, 0, bands * sizeof(uint32_t), stream);
+  if (e != cudaSuccess) return e;
+  return launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, scratch, kNoAllocScratchBytes, stream);
 }
 
 }  // namespace wq

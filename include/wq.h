@@ -127,6 +127,28 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
                         uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The decode kernel without a workspace argument, for callers that cannot allocate device
+ * memory when they run the layer -- for example code running inside a host framework that
+ * owns every device allocation and gives extensions none, or a latency-critical loop where
+ * the synchronisation a cudaMalloc implies is not acceptable.  The pages have no counterpart:
+ * this is a deployment convenience of this library, not part of the method.
+ * Same arguments, results and errors as wq_gemv_w4a16 minus workspace/ws_bytes; allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (split-K
+ * counters + fp32 partials) is one library-owned device array of 64 KiB + 8 MiB, held by
+ * every GPU that loads the library until the process exits; it covers every shape the decode
+ * kernel accepts (M <= 16, N <= 4194304) on devices with up to 256 SMs, and a shape it cannot
+ * hold is refused with WQ_ERR_SHAPE before anything is enqueued.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.  Each call
+ * clears the counters it needs on `stream` before the kernel.  All calls on a device share
+ * the one array: calls that can overlap on the GPU (other streams, other threads) race and
+ * corrupt each other's results -- serialise them.
+ */
+wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                                uint16_t* Y, void* stream);
+
+/*
  * The tensor-core (tcgen05, TMEM accumulator) kernel alone, for any M >= 1 (same arguments
  * and errors as wq_gemm_w4a16).
  */
