@@ -5,26 +5,29 @@
 // design goal is to stream the 0.53125 B/weight of packed weights + metadata once, at full
 // HBM bandwidth, with the arithmetic hidden underneath.
 //
-// Structure (one persistent CTA per SM, warp-specialised):
+// Structure (one persistent CTA per SM, warp-specialised, 19 warps):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
-//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4-stage smem ring.
+//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4-stage smem ring,
+//               plus the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
 //   warps 1-2   prep (stage i by prep warp i % 2): the activations of the stage's k-range in
-//               the exact order of the mma.sync B fragments (MXFP4: converted to fp16 with a
-//               per-row power-of-two scale that keeps every value in fp16 range), plus the
-//               scales / zero points (INT4) or E8M0 bytes (MXFP4) of the stage's rows.  The
-//               consumers then touch only shared memory in their main loop.
-//   warps 3-10  consumers: 32 weight rows each; unpack nibbles in registers, tensor-core
+//               the exact order of the mma.sync B fragments, with their per-group sums (INT4)
+//               or converted to fp16 with a per-row power-of-two scale that keeps every value
+//               in fp16 range (MXFP4); and the per-row metadata of the stage in the form the
+//               consumers use.  The consumers touch only shared memory in their main loop.
+//   warps 3-18  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
 //               mma.sync with fp32 accumulation, group scale applied in fp32 afterwards.
 //
-// Exactness: the tensor-core operands are exact small integers (INT4: q - z in bf16) or
+// Exactness: the tensor-core operands are exact small integers (INT4: 128 + q in bf16) or
 // exact E2M1 values (MXFP4, fp16); every product is exact and the per-group (INT4) or
-// per-32 (MXFP4) power-of-two/fp16 scale is applied to the fp32 partial sum.  No operand
-// is rounded to 16 bits, which keeps the layer within 1e-2 (1 + |y|) of the float64 oracle
-// at every K (a bf16-rounded dequantised weight would not).  The zero point enters through
-// (q - z), the cross term 第 6 课：量化源码走读 §3 warns must not be dropped.
+// per-32 (MXFP4) scale is applied to the fp32 partial sum.  No operand is rounded to 16
+// bits, which keeps the layer within 1e-2 (1 + |y|) of the float64 oracle at every K (a
+// bf16-rounded dequantised weight would not).  INT4 per group and output:
+//   sum_k (q - z) s x = s * sum_k (128 + q) x  -  s (128 + z) * sum_k x,
+// i.e. the zero-point cross term of 第 6 课：量化源码走读 §3 is compensated with the group sum of
+// the activations instead of subtracting z from every weight.
 //
-// Work split: the (256-row band, 128-k group) units are split evenly over the CTAs in
-// band-major order.  A band covered by one CTA is written directly as bf16; a band shared
+// Work split: the (256-row band, 256-k group pair) units -- one per pipeline stage -- are
+// split evenly over the CTAs in band-major order.  A band covered by one CTA is written directly as bf16; a band shared
 // by several CTAs is reduced through the workspace (fp32 partials + one counter per band,
 // deterministic order: the last CTA to finish sums the partials in CTA order, writes bf16
 // and resets the counter).
@@ -45,14 +48,16 @@ uint32_t gemv_read_and_clear_error() {
 
 namespace gemv {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kBand = 32 * kConsumerWarps;          // weight rows per CTA tile
+constexpr int kConsumerWarps = 16;
+constexpr int kRowsPerWarp = 16;                     // one m16 row tile per consumer warp
+constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
 constexpr int kStages = 4;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
 constexpr int kPrepWarps = 2;                        // stage i is prepared by prep warp i % 2
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
-constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 352
-constexpr int kGroupK = 128;                         // k per unit (one INT4 group)
+constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 608
+constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
+constexpr int kMetaRawBytes = kBand * 16 * 2;        // raw metadata tile(s) per stage (8 KB max)
 
 struct Params {
   const uint16_t* X;
@@ -62,11 +67,13 @@ struct Params {
   float* part;        // [P][2][MT][kBand] fp32 partials
   uint32_t* cnt;      // [bands] counters
   int M, K, N;
-  int G;              // units (128-k groups) per row
+  int G;              // 128-k groups per row (ceil(K / 128))
+  int GP;             // group pairs per row (ceil(G / 2)) -- one pair per stage
   int KB;             // MXFP4: scale bytes per row (K / 32)
   int bands;
-  long long U;        // bands * G
+  long long U;        // bands * GP units (one unit = one stage)
   int P;              // CTAs
+  int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: prep warps gather them
 };
 
 // Fragment row f (0..15) of a 16-row tile -> row inside the tile.  Rows g and g+4 of a
@@ -74,49 +81,23 @@ struct Params {
 // are conflict-free.
 __device__ __forceinline__ int frag_row(int f) { return (f & 8) | ((f >> 1) & 3) | ((f & 1) << 2); }
 
-__device__ __forceinline__ long long unit_start(long long U, int P, int c) {
-  return (U * c) / P;
-}
-
-// Iterator over the stages of one CTA's unit range: 1 or 2 units per stage, never crossing
-// a band boundary.
-struct StageIter {
-  long long u, u0, u1;
-  int G;
-  __device__ void init(long long a, long long b, int g) { u = a; u0 = a; u1 = b; G = g; }
-  __device__ bool done() const { return u >= u1; }
-  __device__ int band() const { return static_cast<int>(u / G); }
-  __device__ int g0() const { return static_cast<int>(u % G); }
-  __device__ long long seg_end() const {
-    long long be = (u / G + 1) * static_cast<long long>(G);
-    return be < u1 ? be : u1;
-  }
-  __device__ int ng() const {
-    long long r = seg_end() - u;
-    return r >= 2 ? 2 : 1;
-  }
-  __device__ bool last_in_seg() const { return u + ng() == seg_end(); }
-  __device__ long long seg_start() const {
-    long long bs = (u / G) * static_cast<long long>(G);
-    return bs > u0 ? bs : u0;
-  }
-  __device__ void next() { u += ng(); }
-};
+__device__ __forceinline__ long long unit_start(long long U, int P, int c) { return (U * c) / P; }
 
 template <int FMT, int MT>
 struct Smem {
   static constexpr int NT = MT / 8;
-  static constexpr int kXBytes = NT * 2 * 4 * 32 * 16;  // [nt][group][vec][lane] uint4
-  uint8_t w[kStages][kTileBytes];
-  uint4 x[kStages][NT][2][4][32];
-  float xf[kStages][MT];          // MXFP4: power-of-two factor per activation row
-  // Per-row metadata of the stage's two groups, staged by the prep warps:
-  //   INT4:  {scale as float, bf16x2 (128 + z) bits}    MXFP4: {four E8M0 bytes, unused}
+  uint8_t w[kStages][kTileBytes];            // SWIZZLE_128B weight tiles (1024-aligned)
+  uint8_t mraw[kStages][kMetaRawBytes];      // raw metadata tiles (TMA), 16 B per row per tensor
+  uint4 x[kStages][NT][2][4][32];            // B fragments [nt][group][vec][lane]
+  float xsum[kStages][2][MT];                // INT4: sum of the group's activations per row m
+  float xf[kStages][MT];                     // MXFP4: power-of-two factor per activation row
+  // Per-row metadata of the stage's two groups, prepared by the prep warps:
+  //   INT4:  {s, c = -s (128 + z)}     MXFP4: {four E8M0 bytes, unused}
   float2 meta[kStages][2][kBand];
   uint64_t full_w[kStages];
   uint64_t full_x[kStages];
   uint64_t empty[kStages];
-  uint64_t group_bar;             // consumer-warp barrier (bounded wait) for the split-K path
+  uint64_t group_bar;                        // consumer barrier (bounded wait), split-K path
   int reduce_flag;
 };
 
@@ -129,12 +110,6 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t bsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
@@ -169,9 +144,30 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
 }
 
+// Stage i of a CTA = unit u0 + i = (band, group pair j).  Ranges are split at pair
+// boundaries, so a stage never straddles a band.
+struct Stage {
+  int band, j, ng;      // ng: groups of the pair inside K (2, or 1 for the last pair of odd G)
+  bool seg_last;        // last stage of this CTA inside this band
+  long long seg_start, seg_end;
+};
+
+__device__ __forceinline__ Stage stage_of(long long u, long long u0, long long u1, int GP, int G) {
+  Stage s;
+  s.band = static_cast<int>(u / GP);
+  s.j = static_cast<int>(u % GP);
+  s.ng = (2 * s.j + 1 < G) ? 2 : 1;
+  const long long bs = static_cast<long long>(s.band) * GP, be = bs + GP;
+  s.seg_start = bs > u0 ? bs : u0;
+  s.seg_end = be < u1 ? be : u1;
+  s.seg_last = (u + 1 == s.seg_end);
+  return s;
+}
+
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemv(const __grid_constant__ CUtensorMap tmap_w, const Params p) {
+    k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
+           const __grid_constant__ CUtensorMap tmap_z, const Params p) {
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -182,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cta = blockIdx.x;
   const long long u0 = unit_start(p.U, p.P, cta);
   const long long u1 = unit_start(p.U, p.P, cta + 1);
+  const int nstages = static_cast<int>(u1 - u0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -194,140 +191,107 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
 
+  // Metadata tile geometry (TMA path).
+  //   INT4:  scales and zeros [N, G] fp16, box 8 groups x 256 rows at x = (2j) & ~7.
+  //   MXFP4: E8M0 [N, K/32] bytes, box 16 bytes x 256 rows at x = (8j) & ~15.
+  constexpr int kMetaBytes = (FMT == kInt4G128) ? 2 * kBand * 16 : kBand * 16;
+
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
-      const uint64_t pol = l2_policy_evict_first();
-      StageIter it;
-      it.init(u0, u1, p.G);
+      if (p.meta_tma) {
+        tma_prefetch_desc(&tmap_s);
+        if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
+      }
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_m = l2_policy_evict_last();
       int i = 0;
-      bool ok = true;
-      for (; !it.done(); it.next(), ++i) {
+      for (; i < nstages; ++i) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) { ok = false; break; }
-        mbar_arrive_expect_tx(&sm.full_w[slot], kTileBytes);
-        tma_load_2d(&sm.w[slot][0], &tmap_w, it.g0() * 64, it.band() * kBand, &sm.full_w[slot], pol);
+        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+        const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
+        const uint32_t bytes = kTileBytes + (p.meta_tma ? kMetaBytes : 0);
+        mbar_arrive_expect_tx(&sm.full_w[slot], bytes);
+        tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
+        if (p.meta_tma) {
+          if constexpr (FMT == kInt4G128) {
+            const int gx = (2 * st.j) & ~7;
+            tma_load_2d(&sm.mraw[slot][0], &tmap_s, gx, st.band * kBand, &sm.full_w[slot], pol_m);
+            tma_load_2d(&sm.mraw[slot][kBand * 16], &tmap_z, gx, st.band * kBand, &sm.full_w[slot], pol_m);
+          } else {
+            tma_load_2d(&sm.mraw[slot][0], &tmap_s, (8 * st.j) & ~15, st.band * kBand, &sm.full_w[slot], pol_m);
+          }
+        }
       }
-      // Drain: the last fill of every slot must have landed before the CTA may exit.
-      const int issued = i;
-      for (int j = issued - kStages; j < issued; ++j) {
-        if (j < 0) continue;
-        const int slot = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrDrain);
+      for (int jj = i - kStages; jj < i; ++jj) {  // drain: the last fill of every slot landed
+        if (jj < 0) continue;
+        mbar_wait(&sm.full_w[jj % kStages], (jj / kStages) & 1, &g_gemv_err, kErrDrain);
       }
-      (void)ok;
     }
   } else if (warp < kFirstConsumer) {
     // ------------------------------------------------------------------ prep
     const int pw = warp - 1;
-    StageIter it;
-    it.init(u0, u1, p.G);
     const int t = lane & 3;
-    for (int i = 0; !it.done(); it.next(), ++i) {
-      if (i % kPrepWarps != pw) continue;
+    for (int i = pw; i < nstages; i += kPrepWarps) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
       if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-      const int ng = it.ng();
-      const int g0 = it.g0();
-      const int band = it.band();
-      // metadata of the stage's rows: lane handles rows lane + 32 q
-      {
-        uint32_t ma[8][2], mb[8][2];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int row = band * kBand + lane + 32 * q;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const bool live = (row < p.N) && (h < ng);
-            if constexpr (FMT == kInt4G128) {
-              const long long idx = static_cast<long long>(row) * p.G + g0 + h;
-              ma[q][h] = live ? __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx) : 0u;
-              mb[q][h] = live ? __ldg(reinterpret_cast<const unsigned short*>(p.zeros) + idx) : 0u;
-            } else {
-              const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
-              const int b0 = (g0 + h) * 4;
-              uint32_t v = 0u;
-              if (live) {
-                if ((p.KB & 3) == 0) {
-                  v = __ldg(reinterpret_cast<const uint32_t*>(E + b0));
-                } else {
-#pragma unroll
-                  for (int q2 = 0; q2 < 4; ++q2)
-                    if (b0 + q2 < p.KB) v |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
-                }
-              }
-              ma[q][h] = v;
-              mb[q][h] = 0u;
-            }
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float2 m2;
-            if constexpr (FMT == kInt4G128) {
-              m2.x = __half2float(__ushort_as_half(static_cast<unsigned short>(ma[q][h])));
-              const float z = __half2float(__ushort_as_half(static_cast<unsigned short>(mb[q][h])));
-              const uint32_t zb = __bfloat16_as_ushort(__float2bfloat16_rn(128.f + z));
-              m2.y = __uint_as_float(zb | (zb << 16));
-            } else {
-              m2.x = __uint_as_float(ma[q][h]);
-              m2.y = 0.f;
-            }
-            sm.meta[slot][h][lane + 32 * q] = m2;
-          }
-      }
+      const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
+      // (1) activations: B fragments (+ INT4 group sums / MXFP4 fp16 conversion)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         const int m = (lane >> 2) + 8 * nt;
         if constexpr (FMT == kInt4G128) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int kbase = (g0 + h) * kGroupK + 32 * t;
-            const bool live = (m < p.M) && (h < ng);
+            const int kbase = (2 * st.j + h) * kGroupK + 32 * t;
+            const bool live = (m < p.M) && (h < st.ng);
             const uint4* src = reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase);
+            uint4 r[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+            float sum = 0.f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              uint4 r = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
               // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
               uint4 o;
-              o.x = prmt(r.x, r.z, 0x5410);
-              o.y = prmt(r.x, r.z, 0x7632);
-              o.z = prmt(r.y, r.w, 0x5410);
-              o.w = prmt(r.y, r.w, 0x7632);
+              o.x = prmt(r[v].x, r[v].z, 0x5410);
+              o.y = prmt(r[v].x, r[v].z, 0x7632);
+              o.z = prmt(r[v].y, r[v].w, 0x5410);
+              o.w = prmt(r[v].y, r[v].w, 0x7632);
               sm.x[slot][nt][h][v][lane] = o;
+              const uint32_t w4[4] = {r[v].x, r[v].y, r[v].z, r[v].w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) sum += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
             }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (t == 0) sm.xsum[slot][h][m] = sum;
           }
         } else {
-          // MXFP4: fp16 operands.  Row scale 2^-k so that |x| * 2^-k < 2^15 (k >= 0).
+          // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
           uint4 raw[2][4];
           uint32_t mx = 0u;  // max |x| bit pattern (bf16 magnitudes order like integers)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
-              const int kbase = (g0 + h) * kGroupK + 32 * blk + 8 * t;
-              const bool live = (m < p.M) && (h < ng) && (kbase < p.K);
+              const int kbase = (2 * st.j + h) * kGroupK + 32 * blk + 8 * t;
+              const bool live = (m < p.M) && (h < st.ng) && (kbase < p.K);
               uint4 r = live ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase))
                              : make_uint4(0u, 0u, 0u, 0u);
               raw[h][blk] = r;
               const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                mx = max(mx, w4[q] & 0x7fffu);
-                mx = max(mx, (w4[q] >> 16) & 0x7fffu);
-              }
+              for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
             }
           }
           mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
           mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
           const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
-          int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);         // inf/nan: no scaling
+          const int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);   // inf/nan: no scaling
           const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -338,9 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t o[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
-                const float lo = __uint_as_float(w4[q] << 16) * inv;
-                const float hi = __uint_as_float(w4[q] & 0xffff0000u) * inv;
-                __half2 hh = __floats2half2_rn(lo, hi);
+                __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv,
+                                               __uint_as_float(w4[q] & 0xffff0000u) * inv);
                 o[q] = *reinterpret_cast<uint32_t*>(&hh);
               }
               sm.x[slot][nt][h][blk][lane] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -349,225 +312,232 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
         }
       }
+      // (2) per-row metadata of the stage: lane handles rows lane + 32 q
+      bool ok = true;
+      if (p.meta_tma) {
+        if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) ok = false;
+      }
+      if (ok) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int r = lane + 32 * q;
+          const int row = st.band * kBand + r;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const bool live = (row < p.N) && (h < st.ng);
+            float2 m2 = make_float2(0.f, 0.f);
+            if constexpr (FMT == kInt4G128) {
+              uint32_t sb = 0u, zb = 0u;
+              if (p.meta_tma) {
+                const int col = ((2 * st.j) & 7) + h;
+                sb = reinterpret_cast<const uint16_t*>(&sm.mraw[slot][0])[r * 8 + col];
+                zb = reinterpret_cast<const uint16_t*>(&sm.mraw[slot][kBand * 16])[r * 8 + col];
+              } else if (live) {
+                const long long idx = static_cast<long long>(row) * p.G + 2 * st.j + h;
+                sb = __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx);
+                zb = __ldg(p.zeros + idx);
+              }
+              const float s = live ? __half2float(__ushort_as_half(static_cast<unsigned short>(sb))) : 0.f;
+              const float z = live ? __half2float(__ushort_as_half(static_cast<unsigned short>(zb))) : 0.f;
+              m2.x = s;
+              m2.y = -s * (128.f + z);
+            } else {
+              uint32_t v = 0u;
+              if (p.meta_tma) {
+                v = reinterpret_cast<const uint32_t*>(&sm.mraw[slot][0])[r * 4 + (((8 * st.j) & 15) >> 2) + h];
+              } else if (live) {
+                const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
+                const int b0 = (2 * st.j + h) * 4;
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                  if (b0 + q2 < p.KB) v |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
+              }
+              m2.x = __uint_as_float(live ? v : 0u);
+            }
+            sm.meta[slot][h][r] = m2;
+          }
+        }
+      }
       mbar_arrive(&sm.full_x[slot]);
+      if (!ok) break;
     }
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - kFirstConsumer;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int tid = threadIdx.x - 32 * kFirstConsumer;  // 0..255
-    // Rows (inside the band) of this lane: [row-tile][fragment half]
-    int rrow[2][2];
-#pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) rrow[rt][hf] = cw * 32 + rt * 16 + frag_row(g + 8 * hf);
+    const int tid = threadIdx.x - 32 * kFirstConsumer;  // 0..511
+    const int r0 = cw * kRowsPerWarp + frag_row(g);      // rows (inside the band) of this lane
+    const int r1 = cw * kRowsPerWarp + frag_row(g + 8);
 
-    float acc[2][NT][4];
+    float acc[NT][4];
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 
-    StageIter it;
-    it.init(u0, u1, p.G);
-    bool aborted = false;
     uint32_t gphase = 0;  // phase parity of group_bar
-    for (int i = 0; !it.done(); it.next(), ++i) {
+    for (int i = 0; i < nstages; ++i) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      const int band = it.band();
-      const int g0 = it.g0();
-      const int ng = it.ng();
-
-      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
-      if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) { aborted = true; break; }
-
-      // Scales / zero points (INT4) or E8M0 bytes (MXFP4) of this lane's rows, from smem.
-      float sc[2][2][2];          // [h][rt][hf]
-      uint32_t zz[2][2][2];       // INT4: bf16x2 (128 + z)
-      uint32_t e8[2][2][2];       // MXFP4: four E8M0 bytes of the group
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const float2 m2 = sm.meta[slot][h][rrow[rt][hf]];
-            sc[h][rt][hf] = m2.x;
-            zz[h][rt][hf] = __float_as_uint(m2.y);
-            e8[h][rt][hf] = __float_as_uint(m2.x);
-          }
+      const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
+      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) break;
+      if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) break;
 
       const uint8_t* wt = &sm.w[slot][0];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (h >= ng) break;
+        if (h >= st.ng) break;
+        const float2 m0 = sm.meta[slot][h][r0];
+        const float2 m1 = sm.meta[slot][h][r1];
         uint4 bx[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int v = 0; v < 4; ++v) bx[nt][v] = sm.x[slot][nt][h][v][lane];
 
+        if constexpr (FMT == kInt4G128) {
+          const int c = 4 * h + t;
+          const uint4 wv0 = *reinterpret_cast<const uint4*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4));
+          const uint4 wv1 = *reinterpret_cast<const uint4*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4));
+          const uint32_t w0[4] = {wv0.x, wv0.y, wv0.z, wv0.w};
+          const uint32_t w1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
+          float ga[2][NT][4];  // two independent accumulation chains (even / odd words)
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt) {
-          if constexpr (FMT == kInt4G128) {
-            uint4 wv[2];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int r = rrow[rt][hf];
-              const int c = 4 * h + t;
-              wv[hf] = *reinterpret_cast<const uint4*>(wt + r * 128 + ((c ^ (r & 7)) << 4));
-            }
-            float gacc[NT][4];
+          for (int ch = 0; ch < 2; ++ch)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) gacc[nt][e] = 0.f;
-            const uint32_t w0[4] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w};
-            const uint32_t w1[4] = {wv[1].x, wv[1].y, wv[1].z, wv[1].w};
+              for (int e = 0; e < 4; ++e) ga[ch][nt][e] = 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              // nibble pairs (s, s+4) as bf16 128+q, then minus (128+z): exact (q - z)
-              uint32_t pa[4], pb[4];
+          for (int jw = 0; jw < 4; ++jw) {
+            // nibble pairs (s, s+4) as bf16 128 + q (exact); the zero point is folded below
+            uint32_t pa[4], pb[4];
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                pa[s] = bsub2(lop3_and_or(w0[j] >> (4 * s), 0x000f000fu, 0x43004300u), zz[h][rt][0]);
-                pb[s] = bsub2(lop3_and_or(w1[j] >> (4 * s), 0x000f000fu, 0x43004300u), zz[h][rt][1]);
-              }
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  const uint4 bv = bx[nt][j];
-                  mma_bf16(gacc[nt], pa[2 * hh], pb[2 * hh], pa[2 * hh + 1], pb[2 * hh + 1], hh ? bv.z : bv.x,
-                           hh ? bv.w : bv.y);
-                }
-              }
+            for (int s = 0; s < 4; ++s) {
+              pa[s] = lop3_and_or(w0[jw] >> (4 * s), 0x000f000fu, 0x43004300u);
+              pb[s] = lop3_and_or(w1[jw] >> (4 * s), 0x000f000fu, 0x43004300u);
             }
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              acc[rt][nt][0] = fmaf(sc[h][rt][0], gacc[nt][0], acc[rt][nt][0]);
-              acc[rt][nt][1] = fmaf(sc[h][rt][0], gacc[nt][1], acc[rt][nt][1]);
-              acc[rt][nt][2] = fmaf(sc[h][rt][1], gacc[nt][2], acc[rt][nt][2]);
-              acc[rt][nt][3] = fmaf(sc[h][rt][1], gacc[nt][3], acc[rt][nt][3]);
-            }
-          } else {
-            // MXFP4: lane t holds 8 codes of each 32-block; two k16 steps per block.
-            float sacc[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              uint32_t wr[2];
-#pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const int r = rrow[rt][hf];
-                const int c = 4 * h + blk;
-                wr[hf] = *reinterpret_cast<const uint32_t*>(wt + r * 128 + ((c ^ (r & 7)) << 4) + 4 * t);
-              }
-              float bacc[NT][4];
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) bacc[nt][e] = 0.f;
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t a0 = e2m1x2_to_f16x2((wr[0] >> (16 * hh)) & 0xffu);
-                const uint32_t a2 = e2m1x2_to_f16x2((wr[0] >> (16 * hh + 8)) & 0xffu);
-                const uint32_t a1 = e2m1x2_to_f16x2((wr[1] >> (16 * hh)) & 0xffu);
-                const uint32_t a3 = e2m1x2_to_f16x2((wr[1] >> (16 * hh + 8)) & 0xffu);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                  const uint4 bv = bx[nt][blk];
-                  const uint32_t b0r = hh ? bv.z : bv.x;
-                  const uint32_t b1r = hh ? bv.w : bv.y;
-                  mma_f16(bacc[nt], a0, a1, a2, a3, b0r, b1r);
-                }
-              }
-              const float f0 = e8m0_to_f32((e8[h][rt][0] >> (8 * blk)) & 0xffu);
-              const float f1 = e8m0_to_f32((e8[h][rt][1] >> (8 * blk)) & 0xffu);
+            for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
-                sacc[nt][0] = fmaf(f0, bacc[nt][0], sacc[nt][0]);
-                sacc[nt][1] = fmaf(f0, bacc[nt][1], sacc[nt][1]);
-                sacc[nt][2] = fmaf(f1, bacc[nt][2], sacc[nt][2]);
-                sacc[nt][3] = fmaf(f1, bacc[nt][3], sacc[nt][3]);
+                const uint4 bv = bx[nt][jw];
+                mma_bf16(ga[jw & 1][nt], pa[2 * hh], pb[2 * hh], pa[2 * hh + 1], pb[2 * hh + 1], hh ? bv.z : bv.x,
+                         hh ? bv.w : bv.y);
+              }
+          }
+          // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)   (zero-point cross term)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float2 xs = *reinterpret_cast<const float2*>(&sm.xsum[slot][h][2 * t + 8 * nt]);
+            acc[nt][0] = fmaf(m0.y, xs.x, fmaf(m0.x, ga[0][nt][0] + ga[1][nt][0], acc[nt][0]));
+            acc[nt][1] = fmaf(m0.y, xs.y, fmaf(m0.x, ga[0][nt][1] + ga[1][nt][1], acc[nt][1]));
+            acc[nt][2] = fmaf(m1.y, xs.x, fmaf(m1.x, ga[0][nt][2] + ga[1][nt][2], acc[nt][2]));
+            acc[nt][3] = fmaf(m1.y, xs.y, fmaf(m1.x, ga[0][nt][3] + ga[1][nt][3], acc[nt][3]));
+          }
+        } else {
+          // MXFP4: lane t holds 8 codes of each 32-block; two k16 steps per block.
+          const uint32_t e0 = __float_as_uint(m0.x), e1 = __float_as_uint(m1.x);
+          float sacc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            const int c = 4 * h + blk;
+            const uint32_t wr0 = *reinterpret_cast<const uint32_t*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4) + 4 * t);
+            const uint32_t wr1 = *reinterpret_cast<const uint32_t*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4) + 4 * t);
+            float bacc[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) bacc[nt][e] = 0.f;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t a0 = e2m1x2_to_f16x2((wr0 >> (16 * hh)) & 0xffu);
+              const uint32_t a2 = e2m1x2_to_f16x2((wr0 >> (16 * hh + 8)) & 0xffu);
+              const uint32_t a1 = e2m1x2_to_f16x2((wr1 >> (16 * hh)) & 0xffu);
+              const uint32_t a3 = e2m1x2_to_f16x2((wr1 >> (16 * hh + 8)) & 0xffu);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint4 bv = bx[nt][blk];
+                mma_f16(bacc[nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
               }
             }
+            const float f0 = e8m0_to_f32((e0 >> (8 * blk)) & 0xffu);
+            const float f1 = e8m0_to_f32((e1 >> (8 * blk)) & 0xffu);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const float x0 = sm.xf[slot][2 * t + 8 * nt];
-              const float x1 = sm.xf[slot][2 * t + 1 + 8 * nt];
-              acc[rt][nt][0] = fmaf(x0, sacc[nt][0], acc[rt][nt][0]);
-              acc[rt][nt][1] = fmaf(x1, sacc[nt][1], acc[rt][nt][1]);
-              acc[rt][nt][2] = fmaf(x0, sacc[nt][2], acc[rt][nt][2]);
-              acc[rt][nt][3] = fmaf(x1, sacc[nt][3], acc[rt][nt][3]);
+              sacc[nt][0] = fmaf(f0, bacc[nt][0], sacc[nt][0]);
+              sacc[nt][1] = fmaf(f0, bacc[nt][1], sacc[nt][1]);
+              sacc[nt][2] = fmaf(f1, bacc[nt][2], sacc[nt][2]);
+              sacc[nt][3] = fmaf(f1, bacc[nt][3], sacc[nt][3]);
             }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float2 xf = *reinterpret_cast<const float2*>(&sm.xf[slot][2 * t + 8 * nt]);
+            acc[nt][0] = fmaf(xf.x, sacc[nt][0], acc[nt][0]);
+            acc[nt][1] = fmaf(xf.y, sacc[nt][1], acc[nt][1]);
+            acc[nt][2] = fmaf(xf.x, sacc[nt][2], acc[nt][2]);
+            acc[nt][3] = fmaf(xf.y, sacc[nt][3], acc[nt][3]);
           }
         }
       }
       __syncwarp();
       mbar_arrive(&sm.empty[slot]);
 
-      if (it.last_in_seg()) {
-        const long long ss = it.seg_start();
-        const long long se = it.seg_end();
-        const bool full = (ss == static_cast<long long>(band) * p.G) && (se == static_cast<long long>(band + 1) * p.G);
+      if (st.seg_last) {
+        const int band = st.band;
+        const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
+                          (st.seg_end == static_cast<long long>(band + 1) * p.GP);
         if (full) {
 #pragma unroll
-          for (int rt = 0; rt < 2; ++rt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int m = 2 * t + (e & 1) + 8 * nt;
-                const int n = band * kBand + rrow[rt][e >> 1];
-                if (m < p.M && n < p.N)
-                  p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[rt][nt][e]));
-              }
+            for (int e = 0; e < 4; ++e) {
+              const int m = 2 * t + (e & 1) + 8 * nt;
+              const int n = band * kBand + ((e >> 1) ? r1 : r0);
+              if (m < p.M && n < p.N)
+                p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
+            }
         } else {
-          const int side = (static_cast<int>(u0 / p.G) == band) ? 0 : 1;
+          const int side = (static_cast<int>(u0 / p.GP) == band) ? 0 : 1;
           float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
 #pragma unroll
-          for (int rt = 0; rt < 2; ++rt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int m = 2 * t + (e & 1) + 8 * nt;
-                __stcg(slotp + m * kBand + rrow[rt][e >> 1], acc[rt][nt][e]);
-              }
+            for (int e = 0; e < 4; ++e) {
+              const int m = 2 * t + (e & 1) + 8 * nt;
+              __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
+            }
           __threadfence();
           mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) { aborted = true; break; }
+          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) break;
           gphase ^= 1u;
           if (tid == 0) {
-            const uint32_t mine = static_cast<uint32_t>(se - ss);
+            const uint32_t mine = static_cast<uint32_t>(st.seg_end - st.seg_start);
             const uint32_t old = atomicAdd(p.cnt + band, mine);
-            sm.reduce_flag = (old + mine == static_cast<uint32_t>(p.G)) ? 1 : 0;
+            sm.reduce_flag = (old + mine == static_cast<uint32_t>(p.GP)) ? 1 : 0;
           }
           mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) { aborted = true; break; }
+          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) break;
           gphase ^= 1u;
           if (sm.reduce_flag) {
             __threadfence();
-            // Contributors: CTAs whose unit range meets this band, in CTA order.
-            const long long bs = static_cast<long long>(band) * p.G, be = bs + p.G;
+            // Contributors: CTAs whose unit range meets this band, summed in CTA order.
+            const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
             int c_lo = static_cast<int>((bs * p.P) / p.U);
             while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
             while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
-            const int r = tid;  // one band row per consumer thread
+            const int r = tid & (kBand - 1);
             const int n = band * kBand + r;
-            for (int m = 0; m < p.M; ++m) {
+            for (int m = tid >> 8; m < p.M; m += 2) {
               float sum = 0.f;
               for (int c = c_lo; c < p.P && unit_start(p.U, p.P, c) < be; ++c) {
-                const int cs = (static_cast<int>(unit_start(p.U, p.P, c) / p.G) == band) ? 0 : 1;
+                const int cs = (static_cast<int>(unit_start(p.U, p.P, c) / p.GP) == band) ? 0 : 1;
                 sum += ld_cg_f32(p.part + (static_cast<long long>(c) * 2 + cs) * MT * kBand + m * kBand + r);
               }
               if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
@@ -576,14 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
       }
     }
-    (void)aborted;
   }
 }
 
@@ -599,13 +566,14 @@ size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   const int MT = M <= 8 ? 8 : 16;
   const long long G = (K + gemv::kGroupK - 1) / gemv::kGroupK;
   const long long bands = (N + gemv::kBand - 1) / gemv::kBand;
-  const int P = gemv::num_ctas(bands * G);
+  const int P = gemv::num_ctas(bands * ((G + 1) / 2));
   (void)fmt;
   return kWsCounterBytes + static_cast<size_t>(P) * 2 * MT * gemv::kBand * sizeof(float);
 }
 
 template <int FMT, int MT>
-static cudaError_t launch_gemv_t(const CUtensorMap& tmap, const gemv::Params& p, cudaStream_t stream) {
+static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
+                                 const gemv::Params& p, cudaStream_t stream) {
   using S = gemv::Smem<FMT, MT>;
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT>;
@@ -617,7 +585,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tmap, const gemv::Params& p,
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<p.P, gemv::kThreads, smem, stream>>>(tmap, p);
+  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, p);
   return cudaGetLastError();
 }
 
@@ -633,24 +601,51 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
   p.G = static_cast<int>((K + gemv::kGroupK - 1) / gemv::kGroupK);
+  p.GP = (p.G + 1) / 2;
   p.KB = static_cast<int>(K / 32);
   p.bands = static_cast<int>((N + gemv::kBand - 1) / gemv::kBand);
-  p.U = static_cast<long long>(p.bands) * p.G;
+  p.U = static_cast<long long>(p.bands) * p.GP;
   p.P = gemv::num_ctas(p.U);
   if (p.bands > kWsMaxCounters) return cudaErrorInvalidValue;
   if (ws_bytes < gemv_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
-  CUtensorMap tmap;
-  cudaError_t e = make_tmap_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2),
+  CUtensorMap tw, ts, tz;
+  cudaError_t e = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2),
                                static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, gemv::kBand,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
+  // Metadata tiles travel with the weights by TMA when the metadata row pitch is a multiple
+  // of 16 bytes (INT4: K % 1024 == 0; MXFP4: K % 512 == 0); otherwise the prep warps gather
+  // them.  Unused descriptors are copies of the weight descriptor (never dereferenced).
+  ts = tw;
+  tz = tw;
+  if (fmt == kInt4G128) {
+    p.meta_tma = (p.G % 8 == 0) ? 1 : 0;
+    if (p.meta_tma) {
+      e = make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, static_cast<uint64_t>(p.G),
+                       static_cast<uint64_t>(N), static_cast<uint64_t>(p.G) * 2, 8, gemv::kBand,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+      if (e != cudaSuccess) return e;
+      e = make_tmap_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_UINT16, zeros, static_cast<uint64_t>(p.G),
+                       static_cast<uint64_t>(N), static_cast<uint64_t>(p.G) * 2, 8, gemv::kBand,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+      if (e != cudaSuccess) return e;
+    }
+  } else {
+    p.meta_tma = (p.KB % 16 == 0) ? 1 : 0;
+    if (p.meta_tma) {
+      e = make_tmap_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, static_cast<uint64_t>(p.KB),
+                       static_cast<uint64_t>(N), static_cast<uint64_t>(p.KB), 16, gemv::kBand,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+      if (e != cudaSuccess) return e;
+    }
+  }
   const bool small = M <= 8;
   if (fmt == kInt4G128)
-    return small ? launch_gemv_t<kInt4G128, 8>(tmap, p, stream) : launch_gemv_t<kInt4G128, 16>(tmap, p, stream);
-  return small ? launch_gemv_t<kMxfp4, 8>(tmap, p, stream) : launch_gemv_t<kMxfp4, 16>(tmap, p, stream);
+    return small ? launch_gemv_t<kInt4G128, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kInt4G128, 16>(tw, ts, tz, p, stream);
+  return small ? launch_gemv_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kMxfp4, 16>(tw, ts, tz, p, stream);
 }
 
 // ---------------------------------------------------------------------------------------
