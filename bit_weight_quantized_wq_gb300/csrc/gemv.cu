@@ -145,24 +145,29 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
 }
 
 // Stage i of a CTA = unit u0 + i = (band, group pair j).  Ranges are split at pair
-// boundaries, so a stage never straddles a band.
-struct Stage {
-  int band, j, ng;      // ng: groups of the pair inside K (2, or 1 for the last pair of odd G)
-  bool seg_last;        // last stage of this CTA inside this band
-  long long seg_start, seg_end;
+// boundaries, so a stage never straddles a band.  The cursor divides once at start-up and
+// then steps incrementally (64-bit division is a long software sequence on the GPU).
+struct Cursor {
+  long long u, u0, u1, seg_start, seg_end;
+  int band, j, GP, G;
+  __device__ void set_seg() {
+    const long long bs = static_cast<long long>(band) * GP;
+    seg_start = bs > u0 ? bs : u0;
+    seg_end = bs + GP < u1 ? bs + GP : u1;
+  }
+  __device__ void init(long long a, long long b, int gp, int g) {
+    u = a; u0 = a; u1 = b; GP = gp; G = g;
+    band = static_cast<int>(a / gp);
+    j = static_cast<int>(a - static_cast<long long>(band) * gp);
+    set_seg();
+  }
+  __device__ int ng() const { return (2 * j + 1 < G) ? 2 : 1; }   // groups of the pair inside K
+  __device__ bool seg_last() const { return u + 1 == seg_end; }    // last stage of this band here
+  __device__ void next() {
+    ++u;
+    if (++j == GP) { j = 0; ++band; set_seg(); }
+  }
 };
-
-__device__ __forceinline__ Stage stage_of(long long u, long long u0, long long u1, int GP, int G) {
-  Stage s;
-  s.band = static_cast<int>(u / GP);
-  s.j = static_cast<int>(u % GP);
-  s.ng = (2 * s.j + 1 < G) ? 2 : 1;
-  const long long bs = static_cast<long long>(s.band) * GP, be = bs + GP;
-  s.seg_start = bs > u0 ? bs : u0;
-  s.seg_end = be < u1 ? be : u1;
-  s.seg_last = (u + 1 == s.seg_end);
-  return s;
-}
 
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -206,12 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_m = l2_policy_evict_last();
+      Cursor st;
+      st.init(u0, u1, p.GP, p.G);
       int i = 0;
-      for (; i < nstages; ++i) {
+      for (; i < nstages; ++i, st.next()) {
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-        const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
         const uint32_t bytes = kTileBytes + (p.meta_tma ? kMetaBytes : 0);
         mbar_arrive_expect_tx(&sm.full_w[slot], bytes);
         tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
@@ -234,11 +240,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ prep
     const int pw = warp - 1;
     const int t = lane & 3;
-    for (int i = pw; i < nstages; i += kPrepWarps) {
+    Cursor st;
+    st.init(u0, u1, p.GP, p.G);
+    for (int q = 0; q < pw; ++q) st.next();
+    for (int i = pw; i < nstages; i += kPrepWarps, st.next(), st.next()) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
       if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-      const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
       // (1) activations: B fragments (+ INT4 group sums / MXFP4 fp16 conversion)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int kbase = (2 * st.j + h) * kGroupK + 32 * t;
-            const bool live = (m < p.M) && (h < st.ng);
+            const bool live = (m < p.M) && (h < st.ng());
             const uint4* src = reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase);
             uint4 r[4];
 #pragma unroll
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
               const int kbase = (2 * st.j + h) * kGroupK + 32 * blk + 8 * t;
-              const bool live = (m < p.M) && (h < st.ng) && (kbase < p.K);
+              const bool live = (m < p.M) && (h < st.ng()) && (kbase < p.K);
               uint4 r = live ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase))
                              : make_uint4(0u, 0u, 0u, 0u);
               raw[h][blk] = r;
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int row = st.band * kBand + r;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const bool live = (row < p.N) && (h < st.ng);
+            const bool live = (row < p.N) && (h < st.ng());
             float2 m2 = make_float2(0.f, 0.f);
             if constexpr (FMT == kInt4G128) {
               uint32_t sb = 0u, zb = 0u;
@@ -377,17 +385,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 
     uint32_t gphase = 0;  // phase parity of group_bar
-    for (int i = 0; i < nstages; ++i) {
+    Cursor st;
+    st.init(u0, u1, p.GP, p.G);
+    for (int i = 0; i < nstages; ++i, st.next()) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      const Stage st = stage_of(u0 + i, u0, u1, p.GP, p.G);
       if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) break;
       if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) break;
 
       const uint8_t* wt = &sm.w[slot][0];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (h >= st.ng) break;
+        if (h >= st.ng()) break;
         const float2 m0 = sm.meta[slot][h][r0];
         const float2 m1 = sm.meta[slot][h][r1];
         uint4 bx[NT][4];
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       mbar_arrive(&sm.empty[slot]);
 
-      if (st.seg_last) {
+      if (st.seg_last()) {
         const int band = st.band;
         const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
                           (st.seg_end == static_cast<long long>(band + 1) * p.GP);
