@@ -33,6 +33,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Bytes to add to the dynamic shared-memory base to reach a 1024-byte boundary (the
+// SWIZZLE_128B atom).  Applied as pointer arithmetic on the __shared__ array itself, so the
+// compiler keeps the shared address space and emits shared-memory loads/stores (a round trip
+// through an integer type would turn every access into a generic one).
+__device__ __forceinline__ uint32_t smem_align_pad(const void* base) {
+  return (1024u - (smem_u32(base) & 1023u)) & 1023u;
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  S& sm = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  S& sm = *reinterpret_cast<S*>(smem_raw + smem_align_pad(smem_raw));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
