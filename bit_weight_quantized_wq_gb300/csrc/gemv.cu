@@ -5,16 +5,16 @@
 // design goal is to stream the 0.53125 B/weight of packed weights + metadata once, at full
 // HBM bandwidth, with the arithmetic hidden underneath.
 //
-// Structure (one persistent CTA per SM, warp-specialised, 19 warps):
+// Structure (one persistent CTA per SM, warp-specialised, 21 warps):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
 //               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4-stage smem ring,
 //               plus the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
-//   warps 1-2   prep (stage i by prep warp i % 2): the activations of the stage's k-range in
+//   warps 1-4   prep (stage i by prep warp i % 4): the activations of the stage's k-range in
 //               the exact order of the mma.sync B fragments, with their per-group sums (INT4)
 //               or converted to fp16 with a per-row power-of-two scale that keeps every value
 //               in fp16 range (MXFP4); and the per-row metadata of the stage in the form the
 //               consumers use.  The consumers touch only shared memory in their main loop.
-//   warps 3-18  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
+//   warps 5-20  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
 //               mma.sync with fp32 accumulation, group scale applied in fp32 afterwards.
 //
 // Exactness: the tensor-core operands are exact small integers (INT4: 128 + q in bf16) or
@@ -53,7 +53,7 @@ constexpr int kRowsPerWarp = 16;                     // one m16 row tile per con
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
 constexpr int kStages = 4;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
-constexpr int kPrepWarps = 2;                        // stage i is prepared by prep warp i % 2
+constexpr int kPrepWarps = 4;                        // stage i is prepared by prep warp i % 4
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
 constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 608
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
@@ -243,34 +243,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int q = 0; q < pw; ++q) st.next();
-    for (int i = pw; i < nstages; i += kPrepWarps, st.next(), st.next()) {
+    for (int i = pw; i < nstages; i += kPrepWarps) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-      // (1) activations: B fragments (+ INT4 group sums / MXFP4 fp16 conversion)
+      // (1) activations of the stage.  The global loads go out before the wait for the slot,
+      //     so their latency overlaps it; only the shared-memory writes need the slot.
+      if constexpr (FMT == kInt4G128) {
+        uint4 r[NT][2][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = (lane >> 2) + 8 * nt;
-        if constexpr (FMT == kInt4G128) {
+        for (int nt = 0; nt < NT; ++nt) {
+          const int m = (lane >> 2) + 8 * nt;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int kbase = (2 * st.j + h) * kGroupK + 32 * t;
             const bool live = (m < p.M) && (h < st.ng());
             const uint4* src = reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase);
-            uint4 r[4];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) r[v] = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+            for (int v = 0; v < 4; ++v) r[nt][h][v] = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int m = (lane >> 2) + 8 * nt;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
             float sum = 0.f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
+              const uint4 x = r[nt][h][v];
               // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
               uint4 o;
-              o.x = prmt(r[v].x, r[v].z, 0x5410);
-              o.y = prmt(r[v].x, r[v].z, 0x7632);
-              o.z = prmt(r[v].y, r[v].w, 0x5410);
-              o.w = prmt(r[v].y, r[v].w, 0x7632);
+              o.x = prmt(x.x, x.z, 0x5410);
+              o.y = prmt(x.x, x.z, 0x7632);
+              o.z = prmt(x.y, x.w, 0x5410);
+              o.w = prmt(x.y, x.w, 0x7632);
               sm.x[slot][nt][h][v][lane] = o;
-              const uint32_t w4[4] = {r[v].x, r[v].y, r[v].z, r[v].w};
+              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int q = 0; q < 4; ++q) sum += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
             }
@@ -278,35 +287,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if (t == 0) sm.xsum[slot][h][m] = sum;
           }
-        } else {
-          // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
-          uint4 raw[2][4];
-          uint32_t mx = 0u;  // max |x| bit pattern (bf16 magnitudes order like integers)
+        }
+      } else {
+        uint4 raw[NT][2][4];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+        for (int nt = 0; nt < NT; ++nt) {
+          const int m = (lane >> 2) + 8 * nt;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
               const int kbase = (2 * st.j + h) * kGroupK + 32 * blk + 8 * t;
               const bool live = (m < p.M) && (h < st.ng()) && (kbase < p.K);
-              uint4 r = live ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase))
-                             : make_uint4(0u, 0u, 0u, 0u);
-              raw[h][blk] = r;
-              const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+              raw[nt][h][blk] = live ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int m = (lane >> 2) + 8 * nt;
+          // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
+          uint32_t mx = 0u;  // max |x| bit pattern (bf16 magnitudes order like integers)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+              const uint4 x = raw[nt][h][blk];
+              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
             }
-          }
           mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
           mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
           const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
           const int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);   // inf/nan: no scaling
           const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
-              const uint4 r = raw[h][blk];
-              const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+              const uint4 x = raw[nt][h][blk];
+              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
               uint32_t o[4];
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
@@ -316,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               sm.x[slot][nt][h][blk][lane] = make_uint4(o[0], o[1], o[2], o[3]);
             }
-          }
           if (t == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
         }
       }
@@ -368,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&sm.full_x[slot]);
       if (!ok) break;
+      for (int q = 0; q < kPrepWarps; ++q) st.next();
     }
   } else {
     // ------------------------------------------------------------------ consumers
@@ -513,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
             }
         } else {
-          const int side = (static_cast<int>(u0 / p.GP) == band) ? 0 : 1;
+          const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
           float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -536,19 +558,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           gphase ^= 1u;
           if (sm.reduce_flag) {
             __threadfence();
-            // Contributors: CTAs whose unit range meets this band, summed in CTA order.
+            // Contributors: CTAs whose unit range meets this band, summed in CTA order.  CTA
+            // c_lo holds the band's first unit; every later contributor starts inside the band
+            // (partial slot 0), c_lo uses slot 1 when its range started in an earlier band.
             const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
             int c_lo = static_cast<int>((bs * p.P) / p.U);
             while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
             while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
+            int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
+            while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
+            while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
+            const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
             const int r = tid & (kBand - 1);
             const int n = band * kBand + r;
             for (int m = tid >> 8; m < p.M; m += 2) {
-              float sum = 0.f;
-              for (int c = c_lo; c < p.P && unit_start(p.U, p.P, c) < be; ++c) {
-                const int cs = (static_cast<int>(unit_start(p.U, p.P, c) / p.GP) == band) ? 0 : 1;
-                sum += ld_cg_f32(p.part + (static_cast<long long>(c) * 2 + cs) * MT * kBand + m * kBand + r);
-              }
+              float sum = ld_cg_f32(p.part + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand + m * kBand + r);
+              for (int c = c_lo + 1; c <= c_hi; ++c)
+                sum += ld_cg_f32(p.part + static_cast<long long>(c) * 2 * MT * kBand + m * kBand + r);
               if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
             }
             if (tid == 0) atomicExch(p.cnt + band, 0u);
