@@ -164,7 +164,7 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
   if (M > 16) return WQ_ERR_SHAPE;
-  if ((N + 255) / 256 > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
+  if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
   if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
   if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
@@ -180,7 +180,7 @@ wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
   if (M > 16) return WQ_ERR_SHAPE;
-  if ((N + 255) / 256 > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
+  if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   st = check_device_cached();
   if (st != WQ_OK) return st;
   // Shapes whose scratch would not fit the library's fixed array (possible only on a device
@@ -230,7 +230,7 @@ const char* wq_status_str(wq_status s) {
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
-  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error();
+  *out = wq::gemv_read_and_clear_error() | wq::gemv_tc_read_and_clear_error() | wq::gemm_tc_read_and_clear_error();
   return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 

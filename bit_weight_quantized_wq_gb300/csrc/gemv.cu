@@ -596,7 +596,7 @@ int num_ctas(long long U) {
 
 }  // namespace gemv
 
-size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
+size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   if (M < 1 || M > 16 || N < 1 || K < 1) return 0;
   const int MT = M <= 8 ? 8 : 16;
   const long long G = (K + gemv::kGroupK - 1) / gemv::kGroupK;
@@ -624,9 +624,9 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
-                        const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
   gemv::Params p{};
   p.X = X;
   p.scales = scales;
@@ -642,7 +642,7 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
   p.U = static_cast<long long>(p.bands) * p.GP;
   p.P = gemv::num_ctas(p.U);
   if (p.bands > kWsMaxCounters) return cudaErrorInvalidValue;
-  if (ws_bytes < gemv_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
+  if (ws_bytes < gemv_mma_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
@@ -683,12 +683,22 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
   return small ? launch_gemv_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kMxfp4, 16>(tw, ts, tz, p, stream);
 }
 
+// The decode entry points run the tcgen05 decode kernel (gemv_tc.cu); the CUDA-core
+// mma.sync kernel above stays available to the library internally.
+size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return gemv_tc_workspace_bytes(fmt, M, K, N); }
+
+cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                        const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
+  return launch_gemv_tc(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream);
+}
+
 // ---------------------------------------------------------------------------------------
 // The decode kernel for callers that cannot allocate device memory.
 //
 // The split-K scratch of the decode kernel (reduction counters and fp32 partial sums) lives
 // here in one fixed, library-owned device array instead of a caller-provided workspace.  It
-// is sized for every decode shape the kernel accepts (M <= 16, N <= 4194304) on a device with
+// is sized for every decode shape the kernel accepts (M <= 16, N <= 2097152) on a device with
 // at most kNoAllocMaxCtas SMs: 64 KiB of counters + 8 MiB of partials.  Every GPU that loads
 // the library keeps this array until the process exits.
 // ---------------------------------------------------------------------------------------
@@ -723,7 +733,7 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
   }
   if (gemv_workspace_bytes(fmt, M, K, N) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
   // The array keeps whatever the previous call left; the counters must start at zero.
-  const size_t bands = static_cast<size_t>((N + gemv::kBand - 1) / gemv::kBand);
+  const size_t bands = static_cast<size_t>((N + kDecodeBand - 1) / kDecodeBand);
   e = cudaMemsetAsync(scratch, 0, bands * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   return launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, scratch, kNoAllocScratchBytes, stream);

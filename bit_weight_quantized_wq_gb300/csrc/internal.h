@@ -26,6 +26,8 @@ int device_sm_count();
 // can be shared by calls of any shape and by both kernels.
 constexpr size_t kWsCounterBytes = 64 * 1024;
 constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
+// Weight rows per split-K band of the decode kernel: N <= kWsMaxCounters * kDecodeBand.
+constexpr int64_t kDecodeBand = 128;
 
 // quantize.cu
 cudaError_t launch_quant_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq, uint16_t* scales,
@@ -42,6 +44,13 @@ uint32_t gemv_read_and_clear_error();
 size_t gemv_noalloc_scratch_bytes();
 cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                                 const void* scales, const uint16_t* zeros, uint16_t* Y, cudaStream_t stream);
+
+// gemv_tc.cu -- decode kernel on tcgen05, M <= 16
+size_t gemv_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
+cudaError_t launch_gemv_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
+                           const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
+                           cudaStream_t stream);
+uint32_t gemv_tc_read_and_clear_error();
 
 // gemm_tc.cu -- tcgen05 kernel, any M
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);

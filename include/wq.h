@@ -117,7 +117,7 @@ wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
 
 /*
  * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 16
- * and N <= 4194304).
+ * and N <= 2097152).
  * Streams the packed weights with TMA, unpacks in registers and applies the group scale in
  * fp32 after exact integer-valued tensor-core products; the zero point enters as (q - z),
  * the cross term of 第 6 课：量化源码走读 §3.
@@ -136,7 +136,7 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (split-K
  * counters + fp32 partials) is one library-owned device array of 64 KiB + 8 MiB, held by
  * every GPU that loads the library until the process exits; it covers every shape the decode
- * kernel accepts (M <= 16, N <= 4194304) on devices with up to 256 SMs, and a shape it cannot
+ * kernel accepts (M <= 16, N <= 2097152) on devices with up to 256 SMs, and a shape it cannot
  * hold is refused with WQ_ERR_SHAPE before anything is enqueued.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.  Each call

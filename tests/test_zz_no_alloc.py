@@ -72,6 +72,6 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row(lib):
 
 def test_noalloc_rejects_sizes_beyond_its_array(lib):
     fake = ctypes.c_void_p(0x10000)       # never dereferenced: refused before any launch
-    assert lib.wq_gemv_w4a16_noalloc(0, fake, 1, 128, 4194304 + 256, fake, fake, fake, fake, None) == 2
+    assert lib.wq_gemv_w4a16_noalloc(0, fake, 1, 128, 2097152 + 128, fake, fake, fake, fake, None) == 2
     assert lib.wq_gemv_w4a16_noalloc(0, fake, 17, 128, 256, fake, fake, fake, fake, None) == 2
     assert lib.wq_gemv_w4a16_noalloc(0, None, 1, 128, 256, fake, fake, fake, fake, None) == 1
