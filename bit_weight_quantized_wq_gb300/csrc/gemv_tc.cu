@@ -14,10 +14,12 @@
 //   B  -- prep warps write the activations of the stage into shared memory in the 128-byte
 //         swizzled K-major layout the MMA reads (k order matching the unpacked A, see below).
 //   D  -- one fp32 accumulator per group in tensor memory; after the group's 8 MMAs the
-//         dequant thread of the row folds it into registers with the group's scale.
+//         fold thread of the row folds it into registers with the group's scale.
 // Warps: 0 TMA (weights + metadata tiles), 1 TMEM allocator + MMA issuer, 2-5 prep,
-// 6-13 dequant + fold (warp w may touch TMEM lanes 32 (w % 4) .. +31; warps 6-9 take the
-// stage's first group, 10-13 its second).
+// 6-13 unpack (warp w may touch TMEM lanes 32 (w % 4) .. +31; warps 6-9 take the stage's
+// first group, 10-13 its second), 14-17 fold + output (one thread per row, both groups).
+// Tensor memory holds 3 A buffers and 4 D buffers (512 columns), so the MMAs of a stage
+// overlap the unpacking of the next three and the fold never stalls the unpack.
 //
 // Exactness, INT4: A holds 128 + q (bf16, exact; one lop3 for two weights), so per group
 //     sum_k (q - z) s x = s * D  -  s (128 + z) * sum_k x,
@@ -59,10 +61,14 @@ constexpr int kPrepWarps = 4;
 constexpr int kFirstPrep = 2;
 constexpr int kFirstDeq = kFirstPrep + kPrepWarps;  // 6
 constexpr int kDeqWarps = 8;
-constexpr int kThreads = 32 * (kFirstDeq + kDeqWarps);  // 448
+constexpr int kFirstFold = kFirstDeq + kDeqWarps;   // 14
+constexpr int kFoldWarps = 4;
+constexpr int kThreads = 32 * (kFirstFold + kFoldWarps);  // 576
 constexpr int kTmemCols = 512;
-constexpr int kACol = 0;      // A: buffer b at 128 b, group h at + 64 h (64 cols = 128 k of 16-bit)
-constexpr int kDCol = 256;    // D: buffer b at 256 + 32 b, group h at + 16 h
+constexpr int kABufs = 3;     // A: buffer b at 128 b, group h at + 64 h (64 cols = 128 k of 16-bit)
+constexpr int kDBufs = 4;     // D: buffer b at 384 + 32 b, group h at + 16 h
+constexpr int kACol = 0;
+constexpr int kDCol = kABufs * 128;
 
 struct Params {
   const uint16_t* X;
@@ -84,10 +90,9 @@ struct Smem {
   uint8_t x[kXStages][kXBytes];          // 1024-aligned
   uint8_t mraw[kWStages][kMetaBytes];
   float xs[8][2][kN];                    // INT4: group sums of X; MXFP4: row factor 2^k (h = 0)
-  float red[kN][kBand];                  // second group's accumulators at a segment end
   uint64_t w_full[kWStages], w_empty[kWStages];
   uint64_t x_full[kXStages], x_empty[kXStages];
-  uint64_t a_full[2], d_full[2];
+  uint64_t a_full[kABufs], d_full[kDBufs], d_empty[kDBufs];
   uint64_t group_bar;
   uint32_t tmem_base;
   int reduce_flag;
@@ -213,17 +218,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&sm.w_full[s], 1);
-      mbar_init(&sm.w_empty[s], 32 * kDeqWarps);
+      mbar_init(&sm.w_empty[s], 32 * kFoldWarps);
     }
     for (int s = 0; s < kXStages; ++s) {
       mbar_init(&sm.x_full[s], 32);
       mbar_init(&sm.x_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.a_full[b], 32 * kDeqWarps);
+    for (int b = 0; b < kABufs; ++b) mbar_init(&sm.a_full[b], 32 * kDeqWarps);
+    for (int b = 0; b < kDBufs; ++b) {
       mbar_init(&sm.d_full[b], 1);
+      mbar_init(&sm.d_empty[b], 32 * kFoldWarps);
     }
-    mbar_init(&sm.group_bar, 32 * kDeqWarps);
+    mbar_init(&sm.group_bar, 32 * kFoldWarps);
     fence_barrier_init();
   }
   // Activation tiles: rows >= M stay zero for the whole kernel (the prep warps write rows < M).
@@ -256,8 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int i = 0;
       for (; i < nstages; ++i, st.next()) {
         const int s = i % kWStages;
-        const uint32_t ph = (i / kWStages) & 1;
-        if (!mbar_wait(&sm.w_empty[s], ph ^ 1, &g_gemv_tc_err, kErrWaitEmpty)) break;
+        if (!mbar_wait(&sm.w_empty[s], ((i / kWStages) & 1) ^ 1, &g_gemv_tc_err, kErrWaitEmpty)) break;
         mbar_arrive_expect_tx(&sm.w_full[s], kWBytes + (p.meta_tma ? kMetaTx : 0));
         tma_load_2d(&sm.w[s][0], &tmap_w, st.j * 128, st.band * kBand, &sm.w_full[s], pol_w);
         if (p.meta_tma) {
@@ -283,9 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.init(u0, u1, p.GP, p.G);
       int issued = 0;
       for (int i = 0; i < nstages; ++i, st.next()) {
-        const int b = i & 1, sx = i % kXStages;
-        if (!mbar_wait(&sm.a_full[b], (i >> 1) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
+        const int ab = i % kABufs, db = i % kDBufs, sx = i % kXStages;
+        if (!mbar_wait(&sm.a_full[ab], (i / kABufs) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
         if (!mbar_wait(&sm.x_full[sx], (i / kXStages) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
+        if (i >= kDBufs && !mbar_wait(&sm.d_empty[db], ((i - kDBufs) / kDBufs) & 1, &g_gemv_tc_err, kErrWaitEmpty))
+          break;
         tc_fence_after();
         const uint32_t xbase = smem_u32(&sm.x[sx][0]);
         for (int h = 0; h < st.ng(); ++h) {
@@ -293,18 +300,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < 8; ++kk) {
             const int kb = 2 * h + (kk >> 2);                       // 64-k block of the stage
             const uint64_t bd = smem_desc_sw128(xbase + kb * 2048 + (kk & 3) * 32);
-            tc_mma_ts(tmem + kDCol + 32 * b + 16 * h, tmem + kACol + 128 * b + 64 * h + 8 * kk, bd, id,
+            tc_mma_ts(tmem + kDCol + 32 * db + 16 * h, tmem + kACol + 128 * ab + 64 * h + 8 * kk, bd, id,
                       kk > 0 ? 1u : 0u);
           }
         }
-        tc_commit(&sm.d_full[b]);
+        tc_commit(&sm.d_full[db]);
         tc_commit(&sm.x_empty[sx]);
         issued = i + 1;
       }
       // Every issued MMA must finish before the tensor memory is released below.
       if (issued > 0) {
-        uint64_t* last = &sm.d_full[(issued - 1) & 1];
-        mbar_wait(last, ((issued - 1) >> 1) & 1, &g_gemv_tc_err, kErrWaitAccum);
+        const int last = issued - 1;
+        mbar_wait(&sm.d_full[last % kDBufs], (last / kDBufs) & 1, &g_gemv_tc_err, kErrWaitAccum);
       }
     }
   } else if (warp < kFirstDeq) {
@@ -375,222 +382,205 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.x_full[sx]);
       for (int q2 = 0; q2 < kPrepWarps; ++q2) st.next();
     }
-  } else {
-    // -------------------------------------------------------------- dequant + fold
+  } else if (warp < kFirstFold) {
+    // -------------------------------------------------------------- unpack into tensor memory
     const int dw = warp - kFirstDeq;              // 0..7
     const int h = dw >> 2;                        // group of the stage this thread unpacks
     const int quarter = warp & 3;                 // TMEM lane quarter
     const int r = quarter * 32 + lane;            // weight row inside the band == TMEM lane
-    const int tid = threadIdx.x - 32 * kFirstDeq; // 0..255
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    Cursor st;
+    st.init(u0, u1, p.GP, p.G);
+    for (int i = 0; i < nstages; ++i, st.next()) {
+      const int s = i % kWStages;
+      const int ab = i % kABufs;
+      if (!mbar_wait(&sm.w_full[s], (i / kWStages) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
+      const uint8_t* wrow = &sm.w[s][r * 128];
+      uint4 wv[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wrow + (((4 * h + c) ^ (r & 7)) << 4));
+      uint32_t a[2][32];
+      if constexpr (FMT == kInt4G128) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t wd[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) {
+            const int col = 16 * c + 4 * jw;  // 4 columns = 8 k per word, order (0,4)(1,5)(2,6)(3,7)
+#pragma unroll
+            for (int s2 = 0; s2 < 4; ++s2)
+              a[col >> 5][(col & 31) + s2] = lop3_and_or(wd[jw] >> (4 * s2), 0x000f000fu, 0x43004300u);
+          }
+        }
+      } else {
+        // per-block offsets from the group's largest E8M0 scale, folded into the fp16 operand
+        const int row = st.band * kBand + r;
+        uint32_t e4 = 0u;
+        if ((h < st.ng()) && (row < p.N)) {
+          if (p.meta_tma) {
+            e4 = reinterpret_cast<const uint32_t*>(&sm.mraw[s][0])[r * 4 + (((8 * st.j) & 15) >> 2) + h];
+          } else {
+            const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
+            const int b0 = (2 * st.j + h) * 4;
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2)
+              if (b0 + q2 < p.KB) e4 |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
+          }
+        }
+        int eb[4], emax = 0;
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+          eb[q2] = static_cast<int>((e4 >> (8 * q2)) & 0xffu);
+          emax = max(emax, eb[q2]);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {           // chunk c == 32-block c of the group
+          const int d = emax - eb[c];
+          // 2^-d as fp16 (exact down to 2^-24; below that the block's weights vanish)
+          const uint32_t f = d <= 14 ? (static_cast<uint32_t>(15 - d) << 10) : (d <= 24 ? (1u << (24 - d)) : 0u);
+          const uint32_t f2 = f | (f << 16);
+          const uint32_t wd[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) {
+            const int col = 16 * c + 4 * jw;
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb) {
+              uint32_t v = e2m1x2_to_f16x2((wd[jw] >> (8 * bb)) & 0xffu);
+              if (d != 0) v = hmul2_u(v, f2);
+              a[col >> 5][(col & 31) + bb] = v;
+            }
+          }
+        }
+      }
+      // A buffer ab was last read by the MMAs of stage i - kABufs.
+      if (i >= kABufs) {
+        const int ip = i - kABufs;
+        if (!mbar_wait(&sm.d_full[ip % kDBufs], (ip / kDBufs) & 1, &g_gemv_tc_err, kErrWaitAccum)) break;
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_base + kACol + 128 * ab + 64 * h, a[0]);
+      tmem_st32(tmem + lane_base + kACol + 128 * ab + 64 * h + 32, a[1]);
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(&sm.a_full[ab]);
+    }
+  } else {
+    // -------------------------------------------------------------- fold + output
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;            // weight row inside the band == TMEM lane
+    const int tid = threadIdx.x - 32 * kFirstFold;  // 0..127
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    // metadata of the previous stage (folded one iteration late)
-    float pv_s = 0.f, pv_c = 0.f;
-    bool pv_live = false;
-    int pv_band = 0;
-    long long pv_seg_start = 0, pv_seg_end = 0;
-    bool pv_seg_last = false;
     uint32_t gphase = 0;
-    bool ok = true;
-
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
-    for (int i = 0; i <= nstages && ok; ++i) {
-      // ---- (1) unpack stage i into A buffer i & 1
-      float cur_s = 0.f, cur_c = 0.f;
-      bool cur_live = false;
-      if (i < nstages) {
-        const int s = i % kWStages;
-        const int b = i & 1;
-        if (!mbar_wait(&sm.w_full[s], (i / kWStages) & 1, &g_gemv_tc_err, kErrWaitFull)) { ok = false; break; }
-        const int row = st.band * kBand + r;
-        cur_live = (h < st.ng()) && (row < p.N);
-        // metadata (raw tile from TMA, or gathered from global)
+    for (int i = 0; i < nstages; ++i, st.next()) {
+      const int s = i % kWStages, db = i % kDBufs;
+      if (!mbar_wait(&sm.d_full[db], (i / kDBufs) & 1, &g_gemv_tc_err, kErrWaitAccum)) break;
+      tc_fence_after();
+      uint32_t dv[2][16];
+      tmem_ld16(tmem + lane_base + kDCol + 32 * db, dv[0]);
+      tmem_ld16(tmem + lane_base + kDCol + 32 * db + 16, dv[1]);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sm.d_empty[db]);
+      // metadata of the stage (the weight slot is still held: this thread releases it below)
+      if (!mbar_wait(&sm.w_full[s], (i / kWStages) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
+      const int row = st.band * kBand + r;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool live = (h < st.ng()) && (row < p.N);
+        if (!live) continue;
         if constexpr (FMT == kInt4G128) {
-          uint32_t sb = 0u, zb = 0u;
-          if (cur_live) {
-            if (p.meta_tma) {
-              const int col = ((2 * st.j) & 7) + h;
-              sb = reinterpret_cast<const uint16_t*>(&sm.mraw[s][0])[r * 8 + col];
-              zb = reinterpret_cast<const uint16_t*>(&sm.mraw[s][kBand * 16])[r * 8 + col];
-            } else {
-              const long long idx = static_cast<long long>(row) * p.G + 2 * st.j + h;
-              sb = __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx);
-              zb = __ldg(p.zeros + idx);
-            }
+          uint32_t sb, zb;
+          if (p.meta_tma) {
+            const int col = ((2 * st.j) & 7) + h;
+            sb = reinterpret_cast<const uint16_t*>(&sm.mraw[s][0])[r * 8 + col];
+            zb = reinterpret_cast<const uint16_t*>(&sm.mraw[s][kBand * 16])[r * 8 + col];
+          } else {
+            const long long idx = static_cast<long long>(row) * p.G + 2 * st.j + h;
+            sb = __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx);
+            zb = __ldg(p.zeros + idx);
           }
           const float sf = __half2float(__ushort_as_half(static_cast<unsigned short>(sb)));
-          const float zf = __half2float(__ushort_as_half(static_cast<unsigned short>(zb)));
-          cur_s = cur_live ? sf : 0.f;
-          cur_c = cur_live ? -sf * (128.f + zf) : 0.f;
-        }
-        uint32_t e4 = 0u;  // MXFP4: four E8M0 bytes of the group
-        if constexpr (FMT == kMxfp4) {
-          if (cur_live) {
-            if (p.meta_tma) {
-              e4 = reinterpret_cast<const uint32_t*>(&sm.mraw[s][0])[r * 4 + (((8 * st.j) & 15) >> 2) + h];
-            } else {
-              const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
-              const int b0 = (2 * st.j + h) * 4;
+          const float cf = -sf * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zb))));
 #pragma unroll
-              for (int q2 = 0; q2 < 4; ++q2)
-                if (b0 + q2 < p.KB) e4 |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
-            }
-          }
-        }
-        // the row's 64 bytes of this group: chunks 4h .. 4h+3 of the SW128 row
-        const uint8_t* wrow = &sm.w[s][r * 128];
-        uint4 wv[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wrow + (((4 * h + c) ^ (r & 7)) << 4));
-        mbar_arrive(&sm.w_empty[s]);  // the codes are in registers now
-        uint32_t a[2][32];
-        if constexpr (FMT == kInt4G128) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t wd[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
-#pragma unroll
-            for (int jw = 0; jw < 4; ++jw) {
-              const int col = 16 * c + 4 * jw;  // 4 columns = 8 k per word, order (0,4)(1,5)(2,6)(3,7)
-#pragma unroll
-              for (int s2 = 0; s2 < 4; ++s2)
-                a[col >> 5][(col & 31) + s2] = lop3_and_or(wd[jw] >> (4 * s2), 0x000f000fu, 0x43004300u);
-            }
-          }
+          for (int m = 0; m < MT; ++m)
+            acc[m] = fmaf(cf, sm.xs[i & 7][h][m], fmaf(sf, __uint_as_float(dv[h][m]), acc[m]));
         } else {
-          int eb[4], emax = 0;
-#pragma unroll
-          for (int q2 = 0; q2 < 4; ++q2) {
-            eb[q2] = static_cast<int>((e4 >> (8 * q2)) & 0xffu);
-            emax = max(emax, eb[q2]);
-          }
-          cur_s = cur_live ? ((emax ? __uint_as_float(static_cast<uint32_t>(emax) << 23) : __uint_as_float(0x00400000u)))
-                           : 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {           // chunk c == 32-block c of the group
-            const int d = emax - eb[c];
-            // 2^-d as fp16 (exact down to 2^-24; below that the block's weights vanish)
-            const uint32_t f = d <= 14 ? (static_cast<uint32_t>(15 - d) << 10)
-                                       : (d <= 24 ? (1u << (24 - d)) : 0u);
-            const uint32_t f2 = f | (f << 16);
-            const uint32_t wd[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
-#pragma unroll
-            for (int jw = 0; jw < 4; ++jw) {
-              const int col = 16 * c + 4 * jw;
-#pragma unroll
-              for (int bb = 0; bb < 4; ++bb) {
-                uint32_t v = e2m1x2_to_f16x2((wd[jw] >> (8 * bb)) & 0xffu);
-                if (d != 0) v = hmul2_u(v, f2);
-                a[col >> 5][(col & 31) + bb] = v;
-              }
-            }
-          }
-        }
-        tmem_st32(tmem + lane_base + kACol + 128 * b + 64 * h, a[0]);
-        tmem_st32(tmem + lane_base + kACol + 128 * b + 64 * h + 32, a[1]);
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(&sm.a_full[b]);
-      }
-      // ---- (2) fold stage i - 1 (its MMAs ran while stage i was unpacked)
-      if (i >= 1) {
-        const int ip = i - 1, b = ip & 1;
-        if (!mbar_wait(&sm.d_full[b], (ip >> 1) & 1, &g_gemv_tc_err, kErrWaitAccum)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t dv[16];
-        tmem_ld16(tmem + lane_base + kDCol + 32 * b + 16 * h, dv);
-        tc_wait_ld();
-        if (pv_live) {
-          if constexpr (FMT == kInt4G128) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-              acc[m] = fmaf(pv_c, sm.xs[ip & 7][h][m], fmaf(pv_s, __uint_as_float(dv[m]), acc[m]));
+          uint32_t e4 = 0u;
+          if (p.meta_tma) {
+            e4 = reinterpret_cast<const uint32_t*>(&sm.mraw[s][0])[r * 4 + (((8 * st.j) & 15) >> 2) + h];
           } else {
+            const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
+            const int b0 = (2 * st.j + h) * 4;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] = fmaf(pv_s * sm.xs[ip & 7][0][m], __uint_as_float(dv[m]), acc[m]);
+            for (int q2 = 0; q2 < 4; ++q2)
+              if (b0 + q2 < p.KB) e4 |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
           }
-        }
-        tc_fence_before();
-        // ---- (3) output at the end of a band segment
-        if (pv_seg_last) {
-          const int band = pv_band;
-          if (h == 1) {
+          uint32_t emax = 0u;
 #pragma unroll
-            for (int m = 0; m < MT; ++m) sm.red[m][r] = acc[m];
-          }
-          mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_tc_err, kErrWaitReduce)) { ok = false; break; }
-          gphase ^= 1u;
-          const bool full = (pv_seg_start == static_cast<long long>(band) * p.GP) &&
-                            (pv_seg_end == static_cast<long long>(band + 1) * p.GP);
-          const int n = band * kBand + r;
-          if (h == 0) {
+          for (int q2 = 0; q2 < 4; ++q2) emax = max(emax, (e4 >> (8 * q2)) & 0xffu);
+          const float F = emax ? __uint_as_float(emax << 23) : __uint_as_float(0x00400000u);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m] += sm.red[m][r];
-            if (full) {
-              if (n < p.N)
-                for (int m = 0; m < p.M; ++m)
-                  p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
-            } else {
-              const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
-              float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
-#pragma unroll
-              for (int m = 0; m < MT; ++m) __stcg(slotp + m * kBand + r, acc[m]);
-              __threadfence();
-            }
-          }
-          // red[] consumed (and partials published) before anyone moves on
-          mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_tc_err, kErrWaitReduce)) { ok = false; break; }
-          gphase ^= 1u;
-          if (!full) {
-            if (tid == 0) {
-              const uint32_t mine = static_cast<uint32_t>(pv_seg_end - pv_seg_start);
-              const uint32_t old = atomicAdd(p.cnt + band, mine);
-              sm.reduce_flag = (old + mine == static_cast<uint32_t>(p.GP)) ? 1 : 0;
-            }
-            mbar_arrive(&sm.group_bar);
-            if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_tc_err, kErrWaitReduce)) { ok = false; break; }
-            gphase ^= 1u;
-            if (sm.reduce_flag && h == 0) {
-              __threadfence();
-              const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
-              int c_lo = static_cast<int>((bs * p.P) / p.U);
-              while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
-              while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
-              int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
-              while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
-              while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
-              const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
-              for (int m = 0; m < p.M; ++m) {
-                float sum = ld_cg_f32(p.part + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand + m * kBand + r);
-                for (int c = c_lo + 1; c <= c_hi; ++c)
-                  sum += ld_cg_f32(p.part + static_cast<long long>(c) * 2 * MT * kBand + m * kBand + r);
-                if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-              }
-              if (r == 0) atomicExch(p.cnt + band, 0u);
-            }
-          }
-#pragma unroll
-          for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+          for (int m = 0; m < MT; ++m) acc[m] = fmaf(F * sm.xs[i & 7][0][m], __uint_as_float(dv[h][m]), acc[m]);
         }
       }
-      // the stage just unpacked becomes "previous"
-      if (i < nstages) {
-        pv_s = cur_s;
-        pv_c = cur_c;
-        pv_live = cur_live;
-        pv_band = st.band;
-        pv_seg_start = st.seg_start;
-        pv_seg_end = st.seg_end;
-        pv_seg_last = st.seg_last();
-        st.next();
+      mbar_arrive(&sm.w_empty[s]);
+      // ---- output at the end of a band segment
+      if (st.seg_last()) {
+        const int band = st.band;
+        const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
+                          (st.seg_end == static_cast<long long>(band + 1) * p.GP);
+        const int n = band * kBand + r;
+        if (full) {
+          if (n < p.N)
+            for (int m = 0; m < p.M; ++m)
+              p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[m]));
+        } else {
+          const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
+          float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
+#pragma unroll
+          for (int m = 0; m < MT; ++m) __stcg(slotp + m * kBand + r, acc[m]);
+          __threadfence();
+          mbar_arrive(&sm.group_bar);
+          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_tc_err, kErrWaitReduce)) break;
+          gphase ^= 1u;
+          if (tid == 0) {
+            const uint32_t mine = static_cast<uint32_t>(st.seg_end - st.seg_start);
+            const uint32_t old = atomicAdd(p.cnt + band, mine);
+            sm.reduce_flag = (old + mine == static_cast<uint32_t>(p.GP)) ? 1 : 0;
+          }
+          mbar_arrive(&sm.group_bar);
+          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_tc_err, kErrWaitReduce)) break;
+          gphase ^= 1u;
+          if (sm.reduce_flag) {
+            __threadfence();
+            const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
+            int c_lo = static_cast<int>((bs * p.P) / p.U);
+            while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
+            while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
+            int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
+            while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
+            while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
+            const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
+            for (int m = 0; m < p.M; ++m) {
+              float sum = ld_cg_f32(p.part + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand + m * kBand + r);
+              for (int c = c_lo + 1; c <= c_hi; ++c)
+                sum += ld_cg_f32(p.part + static_cast<long long>(c) * 2 * MT * kBand + m * kBand + r);
+              if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+            }
+            if (tid == 0) atomicExch(p.cnt + band, 0u);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
       }
     }
-    tc_fence_before();
   }
+  tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
