@@ -11,8 +11,9 @@
 //   A  -- dequant threads (one per weight row and group) unpack the stage's nibbles and write
 //         them straight into tensor memory (tcgen05.st): no shared-memory round trip and no
 //         register fragments.
-//   B  -- prep warps write the activations of the stage into shared memory in the 128-byte
-//         swizzled K-major layout the MMA reads (k order matching the unpacked A, see below).
+//   B  -- the stage's raw activations arrive by TMA with its weights; prep warps rewrite them
+//         into the 128-byte swizzled K-major layout the MMA reads (k order matching the
+//         unpacked A, see below), shared memory to shared memory.
 //   D  -- one fp32 accumulator per group in tensor memory; after the group's 8 MMAs the
 //         fold thread of the row folds it into registers with the group's scale.
 // Warps: 0 TMA (weights + metadata tiles), 1 TMEM allocator + MMA issuer, 2-5 prep,
@@ -52,11 +53,12 @@ namespace dec {
 
 constexpr int kBand = 128;                 // weight rows per band (MMA M)
 constexpr int kN = 16;                     // MMA N: activations, padded
-constexpr int kWStages = 8;                // weight ring
+constexpr int kWStages = 6;                // weight ring (weights + metadata + raw activations)
 constexpr int kXStages = 4;                // activation ring
 constexpr int kWBytes = kBand * 128;       // 16 KB: 128 rows x 256 k of 4-bit codes, SW128
 constexpr int kXBytes = kN * 256 * 2;      // 8 KB: 16 rows x 256 k, 16-bit, SW128 (4 k-blocks)
 constexpr int kMetaBytes = kBand * 16 * 2; // raw metadata tiles: 16 B per row per tensor
+constexpr int kXRawBytes = kN * 256 * 2;   // raw activation tile: 16 rows x 256 k bf16 (TMA, rows >= M zero)
 constexpr int kPrepWarps = 4;
 constexpr int kFirstPrep = 2;
 constexpr int kFirstDeq = kFirstPrep + kPrepWarps;  // 6
@@ -89,6 +91,7 @@ struct Smem {
   uint8_t w[kWStages][kWBytes];          // 1024-aligned
   uint8_t x[kXStages][kXBytes];          // 1024-aligned
   uint8_t mraw[kWStages][kMetaBytes];
+  uint8_t xraw[kWStages][kXRawBytes];
   float xs[8][2][kN];                    // INT4: group sums of X; MXFP4: row factor 2^k (h = 0)
   uint64_t w_full[kWStages], w_empty[kWStages];
   uint64_t x_full[kXStages], x_empty[kXStages];
@@ -204,7 +207,8 @@ __device__ __forceinline__ int x_chunk_off(int m, int q) {
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv_tc(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-              const __grid_constant__ CUtensorMap tmap_z, const Params p) {
+              const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
+              const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + smem_align_pad(smem_raw));
   const int warp = threadIdx.x >> 5;
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kWStages; ++s) {
       mbar_init(&sm.w_full[s], 1);
-      mbar_init(&sm.w_empty[s], 32 * kFoldWarps);
+      mbar_init(&sm.w_empty[s], 32 * (kFoldWarps + 1));  // fold warps + the stage's prep warp
     }
     for (int s = 0; s < kXStages; ++s) {
       mbar_init(&sm.x_full[s], 32);
@@ -251,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
+      tma_prefetch_desc(&tmap_x);
       if (p.meta_tma) {
         tma_prefetch_desc(&tmap_s);
         if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
@@ -263,8 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; i < nstages; ++i, st.next()) {
         const int s = i % kWStages;
         if (!mbar_wait(&sm.w_empty[s], ((i / kWStages) & 1) ^ 1, &g_gemv_tc_err, kErrWaitEmpty)) break;
-        mbar_arrive_expect_tx(&sm.w_full[s], kWBytes + (p.meta_tma ? kMetaTx : 0));
+        mbar_arrive_expect_tx(&sm.w_full[s], kWBytes + kXRawBytes + (p.meta_tma ? kMetaTx : 0));
         tma_load_2d(&sm.w[s][0], &tmap_w, st.j * 128, st.band * kBand, &sm.w_full[s], pol_w);
+        tma_load_2d(&sm.xraw[s][0], &tmap_x, st.j * 256, 0, &sm.w_full[s], pol_m);
         if (p.meta_tma) {
           if constexpr (FMT == kInt4G128) {
             const int gx = (2 * st.j) & ~7;
@@ -322,17 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < pw; ++q) st.next();
     for (int i = pw; i < nstages; i += kPrepWarps) {
       const int sx = i % kXStages;
-      const int ng = st.ng();
-      // lane = 16-byte chunk q of the stage (8 k); group h = q / 16; rows m < M.
+      const int s = i % kWStages;
+      // lane = 16-byte chunk q of the stage (8 k); group h = q / 16; rows m < M.  The raw tile
+      // came with the stage's weights (TMA; rows >= M and k >= K are zero-filled).
       const int q = lane;
       const int h = q >> 4;
-      const int k0 = (2 * st.j) * 128 + 8 * q;
-      const bool kin = (h < ng) && (k0 < p.K);
+      if (!mbar_wait(&sm.w_full[s], (i / kWStages) & 1, &g_gemv_tc_err, kErrWaitFull)) break;
       uint4 r[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m)
-        r[m] = (m < p.M && kin) ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + k0))
-                                : make_uint4(0u, 0u, 0u, 0u);
+        r[m] = (m < p.M) ? *reinterpret_cast<const uint4*>(&sm.xraw[s][m * 512 + 16 * q]) : make_uint4(0u, 0u, 0u, 0u);
+      mbar_arrive(&sm.w_empty[s]);  // the raw activations are in registers now
       if (!mbar_wait(&sm.x_empty[sx], ((i / kXStages) & 1) ^ 1, &g_gemv_tc_err, kErrWaitEmpty)) break;
       uint8_t* xt = &sm.x[sx][0];
       if constexpr (FMT == kInt4G128) {
@@ -606,8 +612,8 @@ size_t gemv_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 }
 
 template <int FMT, int MT>
-static cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz, const dec::Params& p,
-                            cudaStream_t stream) {
+static cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz, const CUtensorMap& tx,
+                            const dec::Params& p, cudaStream_t stream) {
   const size_t smem = sizeof(dec::Smem) + 1024;
   auto kern = dec::k_gemv_tc<FMT, MT>;
   static bool attr_set[64] = {false};
@@ -618,7 +624,7 @@ static cudaError_t launch_t(const CUtensorMap& tw, const CUtensorMap& ts, const 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<p.P, dec::kThreads, smem, stream>>>(tw, ts, tz, p);
+  kern<<<p.P, dec::kThreads, smem, stream>>>(tw, ts, tz, tx, p);
   return cudaGetLastError();
 }
 
@@ -644,10 +650,15 @@ cudaError_t launch_gemv_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
-  CUtensorMap tw, ts, tz;
+  CUtensorMap tw, ts, tz, tx;
   cudaError_t e = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2),
                                static_cast<uint64_t>(N), static_cast<uint64_t>(K / 2), 128, dec::kBand,
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e != cudaSuccess) return e;
+  // activations: 16 rows x 256 k per stage; rows >= M and columns >= K come back as zeros
+  e = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(K) * 2, 256, dec::kN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
   ts = tw;
   tz = tw;
@@ -674,8 +685,8 @@ cudaError_t launch_gemv_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   }
   const bool small = M <= 8;
   if (fmt == kInt4G128)
-    return small ? launch_t<kInt4G128, 8>(tw, ts, tz, p, stream) : launch_t<kInt4G128, 16>(tw, ts, tz, p, stream);
-  return small ? launch_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_t<kMxfp4, 16>(tw, ts, tz, p, stream);
+    return small ? launch_t<kInt4G128, 8>(tw, ts, tz, tx, p, stream) : launch_t<kInt4G128, 16>(tw, ts, tz, tx, p, stream);
+  return small ? launch_t<kMxfp4, 8>(tw, ts, tz, tx, p, stream) : launch_t<kMxfp4, 16>(tw, ts, tz, tx, p, stream);
 }
 
 }  // namespace wq
