@@ -51,7 +51,7 @@ namespace gemv {
 constexpr int kConsumerWarps = 16;
 constexpr int kRowsPerWarp = 16;                     // one m16 row tile per consumer warp
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
 constexpr int kPrepWarps = 4;                        // stage i is prepared by prep warp i % 4
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
@@ -88,6 +88,7 @@ struct Smem {
   static constexpr int NT = MT / 8;
   uint8_t w[kStages][kTileBytes];            // SWIZZLE_128B weight tiles (1024-aligned)
   uint8_t mraw[kStages][kMetaRawBytes];      // raw metadata tiles (TMA), 16 B per row per tensor
+  uint8_t xraw[kStages][MT * 512];           // raw activations of the stage (TMA): MT rows x 256 k bf16
   uint4 x[kStages][NT][2][4][32];            // B fragments [nt][group][vec][lane]
   float xsum[kStages][2][MT];                // INT4: sum of the group's activations per row m
   float xf[kStages][MT];                     // MXFP4: power-of-two factor per activation row
@@ -172,7 +173,8 @@ struct Cursor {
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-           const __grid_constant__ CUtensorMap tmap_z, const Params p) {
+           const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
+           const Params p) {
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full_w[s], 1);
       mbar_init(&sm.full_x[s], 32);
-      mbar_init(&sm.empty[s], 32 * kConsumerWarps);
+      mbar_init(&sm.empty[s], 32 * (kConsumerWarps + 1));  // consumers + the stage's prep warp
     }
     mbar_init(&sm.group_bar, 32 * kConsumerWarps);
     fence_barrier_init();
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
+      tma_prefetch_desc(&tmap_x);
       if (p.meta_tma) {
         tma_prefetch_desc(&tmap_s);
         if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
@@ -218,9 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-        const uint32_t bytes = kTileBytes + (p.meta_tma ? kMetaBytes : 0);
+        const uint32_t bytes = kTileBytes + MT * 512 + (p.meta_tma ? kMetaBytes : 0);
         mbar_arrive_expect_tx(&sm.full_w[slot], bytes);
         tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
+        tma_load_2d(&sm.xraw[slot][0], &tmap_x, st.j * 256, 0, &sm.full_w[slot], pol_m);
         if (p.meta_tma) {
           if constexpr (FMT == kInt4G128) {
             const int gx = (2 * st.j) & ~7;
@@ -246,23 +250,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = pw; i < nstages; i += kPrepWarps) {
       const int slot = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
-      // (1) activations of the stage.  The global loads go out before the wait for the slot,
-      //     so their latency overlaps it; only the shared-memory writes need the slot.
+      // (1) activations of the stage: the raw tile came by TMA with the stage's weights (rows
+      //     >= M and columns >= K zero-filled), so this is shared memory to shared memory.
+      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) break;
+      const uint8_t* xr = &sm.xraw[slot][0];
       if constexpr (FMT == kInt4G128) {
         uint4 r[NT][2][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int m = (lane >> 2) + 8 * nt;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int kbase = (2 * st.j + h) * kGroupK + 32 * t;
-            const bool live = (m < p.M) && (h < st.ng());
-            const uint4* src = reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase);
+          for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int v = 0; v < 4; ++v) r[nt][h][v] = live ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-          }
+            for (int v = 0; v < 4; ++v)
+              r[nt][h][v] = (m < p.M) ? *reinterpret_cast<const uint4*>(xr + m * 512 + 256 * h + 64 * t + 16 * v)
+                                      : make_uint4(0u, 0u, 0u, 0u);
         }
-        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int m = (lane >> 2) + 8 * nt;
@@ -296,14 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              const int kbase = (2 * st.j + h) * kGroupK + 32 * blk + 8 * t;
-              const bool live = (m < p.M) && (h < st.ng()) && (kbase < p.K);
-              raw[nt][h][blk] = live ? __ldg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(m) * p.K + kbase))
-                                     : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int blk = 0; blk < 4; ++blk)
+              raw[nt][h][blk] = (m < p.M) ? *reinterpret_cast<const uint4*>(xr + m * 512 + 256 * h + 64 * blk + 16 * t)
+                                          : make_uint4(0u, 0u, 0u, 0u);
         }
-        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const int m = (lane >> 2) + 8 * nt;
@@ -343,10 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // (2) per-row metadata of the stage: lane handles rows lane + 32 q
       bool ok = true;
-      if (p.meta_tma) {
-        if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) ok = false;
-      }
-      if (ok) {
+      {
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int r = lane + 32 * q;
@@ -388,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mbar_arrive(&sm.full_x[slot]);
+      mbar_arrive(&sm.empty[slot]);   // this warp is done reading the slot's raw tiles
       if (!ok) break;
       for (int q = 0; q < kPrepWarps; ++q) st.next();
     }
@@ -609,6 +606,12 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 template <int FMT, int MT>
 static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
                                  const gemv::Params& p, cudaStream_t stream) {
+  // activations: MT rows x 256 k per stage; rows >= M and columns >= K come back as zeros
+  CUtensorMap tx;
+  cudaError_t ex = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.X, static_cast<uint64_t>(p.K),
+                                static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K) * 2, 256, MT,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (ex != cudaSuccess) return ex;
   using S = gemv::Smem<FMT, MT>;
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT>;
@@ -620,7 +623,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, p);
+  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, tx, p);
   return cudaGetLastError();
 }
 
@@ -683,14 +686,15 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
   return small ? launch_gemv_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kMxfp4, 16>(tw, ts, tz, p, stream);
 }
 
-// The decode entry points run the tcgen05 decode kernel (gemv_tc.cu); the CUDA-core
-// mma.sync kernel above stays available to the library internally.
-size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return gemv_tc_workspace_bytes(fmt, M, K, N); }
+// The decode entry points run the mma.sync kernel above.  The tcgen05 decode kernel
+// (gemv_tc.cu) is kept for comparison: at N = 16 a tcgen05.mma costs ~56 cycles per
+// 128 x 16 x 16 instruction, which caps it below HBM speed on this shape.
+size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return gemv_mma_workspace_bytes(fmt, M, K, N); }
 
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                         const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
-  return launch_gemv_tc(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream);
+  return launch_gemv_mma(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -733,7 +737,7 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
   }
   if (gemv_workspace_bytes(fmt, M, K, N) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
   // The array keeps whatever the previous call left; the counters must start at zero.
-  const size_t bands = static_cast<size_t>((N + kDecodeBand - 1) / kDecodeBand);
+  const size_t bands = static_cast<size_t>((N + gemv::kBand - 1) / gemv::kBand);
   e = cudaMemsetAsync(scratch, 0, bands * sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   return launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, scratch, kNoAllocScratchBytes, stream);
