@@ -5,16 +5,16 @@
 // design goal is to stream the 0.53125 B/weight of packed weights + metadata once, at full
 // HBM bandwidth, with the arithmetic hidden underneath.
 //
-// Structure (one persistent CTA per SM, warp-specialised, 21 warps):
+// Structure (one persistent CTA per SM, warp-specialised, 20 warps):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
-//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4-stage smem ring,
+//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 3-stage smem ring,
 //               plus the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
-//   warps 1-4   prep (stage i by prep warp i % 4): the activations of the stage's k-range in
+//   warps 1-3   prep (stage i by prep warp i % 3): the activations of the stage's k-range in
 //               the exact order of the mma.sync B fragments, with their per-group sums (INT4)
 //               or converted to fp16 with a per-row power-of-two scale that keeps every value
 //               in fp16 range (MXFP4); and the per-row metadata of the stage in the form the
 //               consumers use.  The consumers touch only shared memory in their main loop.
-//   warps 5-20  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
+//   warps 4-19  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
 //               mma.sync with fp32 accumulation, group scale applied in fp32 afterwards.
 //
 // Exactness: the tensor-core operands are exact small integers (INT4: 128 + q in bf16) or
@@ -53,7 +53,10 @@ constexpr int kRowsPerWarp = 16;                     // one m16 row tile per con
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
 constexpr int kStages = 3;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
-constexpr int kPrepWarps = 4;                        // stage i is prepared by prep warp i % 4
+constexpr int kPrepWarps = kStages;                  // stage i is prepared by prep warp i % 3
+// Each prep warp owns whole ring slots (kStages % kPrepWarps == 0), so it waits on every phase
+// of its slots' barriers in order; a parity wait two phases ahead would pass at once.
+static_assert(kStages % kPrepWarps == 0, "prep warps must own whole ring slots");
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
 constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 608
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)

@@ -53,13 +53,16 @@ namespace dec {
 
 constexpr int kBand = 128;                 // weight rows per band (MMA M)
 constexpr int kN = 16;                     // MMA N: activations, padded
-constexpr int kWStages = 6;                // weight ring (weights + metadata + raw activations)
+constexpr int kWStages = 4;                // weight ring (weights + metadata + raw activations)
 constexpr int kXStages = 4;                // activation ring
 constexpr int kWBytes = kBand * 128;       // 16 KB: 128 rows x 256 k of 4-bit codes, SW128
 constexpr int kXBytes = kN * 256 * 2;      // 8 KB: 16 rows x 256 k, 16-bit, SW128 (4 k-blocks)
 constexpr int kMetaBytes = kBand * 16 * 2; // raw metadata tiles: 16 B per row per tensor
 constexpr int kXRawBytes = kN * 256 * 2;   // raw activation tile: 16 rows x 256 k bf16 (TMA, rows >= M zero)
 constexpr int kPrepWarps = 4;
+// Each prep warp owns whole slots of both rings, so it waits on every phase of their barriers
+// in order (a parity wait two phases ahead would pass at once).
+static_assert(kWStages % kPrepWarps == 0 && kXStages % kPrepWarps == 0, "prep warps must own whole slots");
 constexpr int kFirstPrep = 2;
 constexpr int kFirstDeq = kFirstPrep + kPrepWarps;  // 6
 constexpr int kDeqWarps = 8;
