@@ -5,17 +5,19 @@
 // design goal is to stream the 0.53125 B/weight of packed weights + metadata once, at full
 // HBM bandwidth, with the arithmetic hidden underneath.
 //
-// Structure (one persistent CTA per SM, warp-specialised, 20 warps):
+// Structure (one persistent CTA per SM, warp-specialised, 19 warps):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
-//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 3-stage smem ring,
-//               plus the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
-//   warps 1-3   prep (stage i by prep warp i % 3): the activations of the stage's k-range in
-//               the exact order of the mma.sync B fragments, with their per-group sums (INT4)
-//               or converted to fp16 with a per-row power-of-two scale that keeps every value
-//               in fp16 range (MXFP4); and the per-row metadata of the stage in the form the
-//               consumers use.  The consumers touch only shared memory in their main loop.
-//   warps 4-19  consumers: 16 weight rows each; unpack nibbles in registers, tensor-core
-//               mma.sync with fp32 accumulation, group scale applied in fp32 afterwards.
+//               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4- or 5-stage smem
+//               ring, with the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
+//   warps 1-2   prep (stage i by prep warp i % 2), on a separate 4-stage ring: the
+//               activations of the stage's k-range (from L2; they are small and shared by
+//               every CTA) in the exact order of the mma.sync B fragments, with their
+//               per-group sums (INT4) or converted to fp16 with a per-row power-of-two scale
+//               that keeps every value in fp16 range (MXFP4).  The activations do not depend
+//               on the weights, so this runs ahead of the weight stream.
+//   warps 3-18  consumers: 16 weight rows each; per-row metadata straight from its tile,
+//               nibbles unpacked in registers, tensor-core mma.sync with fp32 accumulation,
+//               group scale applied in fp32 afterwards.
 //
 // Exactness: the tensor-core operands are exact small integers (INT4: 128 + q in bf16) or
 // exact E2M1 values (MXFP4, fp16); every product is exact and the per-group (INT4) or
@@ -51,16 +53,29 @@ namespace gemv {
 constexpr int kConsumerWarps = 16;
 constexpr int kRowsPerWarp = 16;                     // one m16 row tile per consumer warp
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
-constexpr int kStages = 3;
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
-constexpr int kPrepWarps = kStages;                  // stage i is prepared by prep warp i % 3
-// Each prep warp owns whole ring slots (kStages % kPrepWarps == 0), so it waits on every phase
+constexpr int kXStages = 4;                          // activation-fragment ring depth
+constexpr int kPrepWarps = 2;                        // stage i is prepared by prep warp i % 2
+// Each prep warp owns whole ring slots (kXStages % kPrepWarps == 0), so it waits on every phase
 // of its slots' barriers in order; a parity wait two phases ahead would pass at once.
-static_assert(kStages % kPrepWarps == 0, "prep warps must own whole ring slots");
+static_assert(kXStages % kPrepWarps == 0, "prep warps must own whole ring slots");
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
 constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 608
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
-constexpr int kMetaRawBytes = kBand * 16 * 2;        // raw metadata tile(s) per stage (8 KB max)
+constexpr int kSmemLimit = 227 * 1024;               // dynamic shared memory per CTA
+constexpr int kSmemReserve = 1024 + 512;             // alignment pad + barriers and flags
+
+// Raw metadata tile(s) per weight stage: INT4 scales + zeros boxes of 8 groups x 256 rows
+// (fp16); MXFP4 one box of 16 E8M0 bytes x 256 rows.
+__host__ __device__ constexpr int meta_raw_bytes(int fmt) { return fmt == kInt4G128 ? 2 * kBand * 16 : kBand * 16; }
+// One activation stage: B fragments + per-row group sums + per-row power-of-two factors.
+__host__ __device__ constexpr int x_stage_bytes(int mt) { return (mt / 8) * 2 * 4 * 32 * 16 + 2 * mt * 4 + mt * 4; }
+// Weight stages: as many as fit beside the activation ring (4 or 5).
+__host__ __device__ constexpr int w_stages(int fmt, int mt) {
+  return (kSmemLimit - kSmemReserve - kXStages * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt)) > 6
+             ? 6
+             : (kSmemLimit - kSmemReserve - kXStages * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt));
+}
 
 struct Params {
   const uint16_t* X;
@@ -76,7 +91,7 @@ struct Params {
   int bands;
   long long U;        // bands * GP units (one unit = one stage)
   int P;              // CTAs
-  int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: prep warps gather them
+  int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: consumers gather them
 };
 
 // Fragment row f (0..15) of a 16-row tile -> row inside the tile.  Rows g and g+4 of a
@@ -89,18 +104,16 @@ __device__ __forceinline__ long long unit_start(long long U, int P, int c) { ret
 template <int FMT, int MT>
 struct Smem {
   static constexpr int NT = MT / 8;
-  uint8_t w[kStages][kTileBytes];            // SWIZZLE_128B weight tiles (1024-aligned)
-  uint8_t mraw[kStages][kMetaRawBytes];      // raw metadata tiles (TMA), 16 B per row per tensor
-  uint8_t xraw[kStages][MT * 512];           // raw activations of the stage (TMA): MT rows x 256 k bf16
-  uint4 x[kStages][NT][2][4][32];            // B fragments [nt][group][vec][lane]
-  float xsum[kStages][2][MT];                // INT4: sum of the group's activations per row m
-  float xf[kStages][MT];                     // MXFP4: power-of-two factor per activation row
-  // Per-row metadata of the stage's two groups, prepared by the prep warps:
-  //   INT4:  {s, c = -s (128 + z)}     MXFP4: {four E8M0 bytes, unused}
-  float2 meta[kStages][2][kBand];
-  uint64_t full_w[kStages];
-  uint64_t full_x[kStages];
-  uint64_t empty[kStages];
+  static constexpr int WS = w_stages(FMT, MT);
+  uint8_t w[WS][kTileBytes];                 // SWIZZLE_128B weight tiles (1024-aligned)
+  uint8_t mraw[WS][meta_raw_bytes(FMT)];     // raw metadata tiles (TMA), 16 B per row per tensor
+  uint4 x[kXStages][NT][2][4][32];           // B fragments [nt][group][vec][lane]
+  float xsum[kXStages][2][MT];               // INT4: sum of the group's activations per row m
+  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row
+  uint64_t full_w[WS];
+  uint64_t empty_w[WS];
+  uint64_t full_x[kXStages];
+  uint64_t empty_x[kXStages];
   uint64_t group_bar;                        // consumer barrier (bounded wait), split-K path
   int reduce_flag;
 };
@@ -125,10 +138,11 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   return d;
 }
 
+// Tensor-core MACs.  Not volatile: they are pure functions of their operands, so the
+// compiler may interleave independent accumulation chains.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -136,8 +150,7 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -146,6 +159,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 // 2^(byte - 127) as a float for an E8M0 byte (byte 0 -> 2^-127, subnormal).
 __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
 }
 
 // Stage i of a CTA = unit u0 + i = (band, group pair j).  Ranges are split at pair
@@ -165,7 +184,6 @@ struct Cursor {
     j = static_cast<int>(a - static_cast<long long>(band) * gp);
     set_seg();
   }
-  __device__ int ng() const { return (2 * j + 1 < G) ? 2 : 1; }   // groups of the pair inside K
   __device__ bool seg_last() const { return u + 1 == seg_end; }    // last stage of this band here
   __device__ void next() {
     ++u;
@@ -176,10 +194,10 @@ struct Cursor {
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-           const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
-           const Params p) {
+           const __grid_constant__ CUtensorMap tmap_z, const Params p) {
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
+  constexpr int WS = S::WS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>(smem_raw + smem_align_pad(smem_raw));
 
@@ -191,10 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nstages = static_cast<int>(u1 - u0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < WS; ++s) {
       mbar_init(&sm.full_w[s], 1);
+      mbar_init(&sm.empty_w[s], 32 * kConsumerWarps);
+    }
+    for (int s = 0; s < kXStages; ++s) {
       mbar_init(&sm.full_x[s], 32);
-      mbar_init(&sm.empty[s], 32 * (kConsumerWarps + 1));  // consumers + the stage's prep warp
+      mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
     mbar_init(&sm.group_bar, 32 * kConsumerWarps);
     fence_barrier_init();
@@ -204,13 +225,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Metadata tile geometry (TMA path).
   //   INT4:  scales and zeros [N, G] fp16, box 8 groups x 256 rows at x = (2j) & ~7.
   //   MXFP4: E8M0 [N, K/32] bytes, box 16 bytes x 256 rows at x = (8j) & ~15.
-  constexpr int kMetaBytes = (FMT == kInt4G128) ? 2 * kBand * 16 : kBand * 16;
+  constexpr int kMetaBytes = meta_raw_bytes(FMT);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
-      tma_prefetch_desc(&tmap_x);
       if (p.meta_tma) {
         tma_prefetch_desc(&tmap_s);
         if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
@@ -221,13 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       st.init(u0, u1, p.GP, p.G);
       int i = 0;
       for (; i < nstages; ++i, st.next()) {
-        const int slot = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        if (!mbar_wait(&sm.empty[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-        const uint32_t bytes = kTileBytes + MT * 512 + (p.meta_tma ? kMetaBytes : 0);
-        mbar_arrive_expect_tx(&sm.full_w[slot], bytes);
+        const int slot = i % WS;
+        const uint32_t ph = (i / WS) & 1;
+        if (!mbar_wait(&sm.empty_w[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+        mbar_arrive_expect_tx(&sm.full_w[slot], kTileBytes + (p.meta_tma ? kMetaBytes : 0));
         tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
-        tma_load_2d(&sm.xraw[slot][0], &tmap_x, st.j * 256, 0, &sm.full_w[slot], pol_m);
         if (p.meta_tma) {
           if constexpr (FMT == kInt4G128) {
             const int gx = (2 * st.j) & ~7;
@@ -238,46 +256,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      for (int jj = i - kStages; jj < i; ++jj) {  // drain: the last fill of every slot landed
+      for (int jj = i - WS; jj < i; ++jj) {  // drain: the last fill of every slot landed
         if (jj < 0) continue;
-        mbar_wait(&sm.full_w[jj % kStages], (jj / kStages) & 1, &g_gemv_err, kErrDrain);
+        mbar_wait(&sm.full_w[jj % WS], (jj / WS) & 1, &g_gemv_err, kErrDrain);
       }
     }
   } else if (warp < kFirstConsumer) {
     // ------------------------------------------------------------------ prep
+    // Activations only: they do not depend on the weight tiles, so the prep warps run up to
+    // kXStages stages ahead of the consumers and stay off the weight ring's critical path.
     const int pw = warp - 1;
     const int t = lane & 3;
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int q = 0; q < pw; ++q) st.next();
     for (int i = pw; i < nstages; i += kPrepWarps) {
-      const int slot = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      // (1) activations of the stage: the raw tile came by TMA with the stage's weights (rows
-      //     >= M and columns >= K zero-filled), so this is shared memory to shared memory.
-      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) break;
-      const uint8_t* xr = &sm.xraw[slot][0];
-      if constexpr (FMT == kInt4G128) {
-        uint4 r[NT][2][4];
+      const int slot = i % kXStages;
+      const uint32_t ph = (i / kXStages) & 1;
+      if (!mbar_wait(&sm.empty_x[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+      const int k0 = 256 * st.j;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int m = (lane >> 2) + 8 * nt;
+      for (int nt = 0; nt < NT; ++nt) {
+        const int m = (lane >> 2) + 8 * nt;
+        const uint16_t* xrow = p.X + static_cast<long long>(m) * p.K;
+        if constexpr (FMT == kInt4G128) {
+          // lane t: elements 32t .. 32t+31 of each group (K % 128 == 0: a group is all in or out)
+          uint4 r[2][4];
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              r[nt][h][v] = (m < p.M) ? *reinterpret_cast<const uint4*>(xr + m * 512 + 256 * h + 64 * t + 16 * v)
-                                      : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int m = (lane >> 2) + 8 * nt;
+            for (int v = 0; v < 4; ++v) {
+              const int k = k0 + 128 * h + 32 * t + 8 * v;
+              r[h][v] = (m < p.M && k < p.K) ? ldg_nc_v4(xrow + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float sum = 0.f;
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const uint4 x = r[nt][h][v];
+              const uint4 x = r[h][v];
               // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
               uint4 o;
               o.x = prmt(x.x, x.z, 0x5410);
@@ -293,29 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             if (t == 0) sm.xsum[slot][h][m] = sum;
           }
-        }
-      } else {
-        uint4 raw[NT][2][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int m = (lane >> 2) + 8 * nt;
+        } else {
+          // lane t: elements 8t .. 8t+7 of each 32-block (K % 32 == 0: a block is all in or out)
+          uint4 raw[2][4];
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk)
-              raw[nt][h][blk] = (m < p.M) ? *reinterpret_cast<const uint4*>(xr + m * 512 + 256 * h + 64 * blk + 16 * t)
-                                          : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const int m = (lane >> 2) + 8 * nt;
+            for (int blk = 0; blk < 4; ++blk) {
+              const int k = k0 + 128 * h + 32 * blk + 8 * t;
+              raw[h][blk] = (m < p.M && k < p.K) ? ldg_nc_v4(xrow + k) : make_uint4(0u, 0u, 0u, 0u);
+            }
           // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
           uint32_t mx = 0u;  // max |x| bit pattern (bf16 magnitudes order like integers)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
-              const uint4 x = raw[nt][h][blk];
+              const uint4 x = raw[h][blk];
               const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
               for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
@@ -329,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 2; ++h)
 #pragma unroll
             for (int blk = 0; blk < 4; ++blk) {
-              const uint4 x = raw[nt][h][blk];
+              const uint4 x = raw[h][blk];
               const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
               uint32_t o[4];
 #pragma unroll
@@ -343,52 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
         }
       }
-      // (2) per-row metadata of the stage: lane handles rows lane + 32 q
-      bool ok = true;
-      {
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int r = lane + 32 * q;
-          const int row = st.band * kBand + r;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const bool live = (row < p.N) && (h < st.ng());
-            float2 m2 = make_float2(0.f, 0.f);
-            if constexpr (FMT == kInt4G128) {
-              uint32_t sb = 0u, zb = 0u;
-              if (p.meta_tma) {
-                const int col = ((2 * st.j) & 7) + h;
-                sb = reinterpret_cast<const uint16_t*>(&sm.mraw[slot][0])[r * 8 + col];
-                zb = reinterpret_cast<const uint16_t*>(&sm.mraw[slot][kBand * 16])[r * 8 + col];
-              } else if (live) {
-                const long long idx = static_cast<long long>(row) * p.G + 2 * st.j + h;
-                sb = __ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx);
-                zb = __ldg(p.zeros + idx);
-              }
-              const float s = live ? __half2float(__ushort_as_half(static_cast<unsigned short>(sb))) : 0.f;
-              const float z = live ? __half2float(__ushort_as_half(static_cast<unsigned short>(zb))) : 0.f;
-              m2.x = s;
-              m2.y = -s * (128.f + z);
-            } else {
-              uint32_t v = 0u;
-              if (p.meta_tma) {
-                v = reinterpret_cast<const uint32_t*>(&sm.mraw[slot][0])[r * 4 + (((8 * st.j) & 15) >> 2) + h];
-              } else if (live) {
-                const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
-                const int b0 = (2 * st.j + h) * 4;
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2)
-                  if (b0 + q2 < p.KB) v |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
-              }
-              m2.x = __uint_as_float(live ? v : 0u);
-            }
-            sm.meta[slot][h][r] = m2;
-          }
-        }
-      }
       mbar_arrive(&sm.full_x[slot]);
-      mbar_arrive(&sm.empty[slot]);   // this warp is done reading the slot's raw tiles
-      if (!ok) break;
       for (int q = 0; q < kPrepWarps; ++q) st.next();
     }
   } else {
@@ -410,115 +376,198 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int i = 0; i < nstages; ++i, st.next()) {
-      const int slot = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      if (!mbar_wait(&sm.full_w[slot], ph, &g_gemv_err, kErrWaitFull)) break;
-      if (!mbar_wait(&sm.full_x[slot], ph, &g_gemv_err, kErrWaitFull)) break;
+      const int ws = i % WS;
+      const uint32_t wph = (i / WS) & 1;
+      const int xs = i % kXStages;
+      const uint32_t xph = (i / kXStages) & 1;
 
-      const uint8_t* wt = &sm.w[slot][0];
+      // Per-row metadata of the stage's two groups, rows r0 / r1 of this lane:
+      //   INT4: sc[h][rr] = {s, c = -s (128 + z)}     MXFP4: eb[rr] = E8M0 bytes of the 8 blocks
+      // Without metadata tiles they are gathered from global memory before the waits.
+      uint32_t sraw[2] = {0u, 0u}, zraw[2] = {0u, 0u};   // INT4: fp16 pairs (group 2j, 2j+1)
+      uint32_t eb[2][2] = {{0u, 0u}, {0u, 0u}};          // MXFP4: [row][group] 4 E8M0 bytes
+      if (!p.meta_tma) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (h >= st.ng()) break;
-        const float2 m0 = sm.meta[slot][h][r0];
-        const float2 m1 = sm.meta[slot][h][r1];
-        uint4 bx[NT][4];
+        for (int rr = 0; rr < 2; ++rr) {
+          const int row = st.band * kBand + (rr ? r1 : r0);
+          if (row >= p.N) continue;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) bx[nt][v] = sm.x[slot][nt][h][v][lane];
-
-        if constexpr (FMT == kInt4G128) {
-          const int c = 4 * h + t;
-          const uint4 wv0 = *reinterpret_cast<const uint4*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4));
-          const uint4 wv1 = *reinterpret_cast<const uint4*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4));
-          const uint32_t w0[4] = {wv0.x, wv0.y, wv0.z, wv0.w};
-          const uint32_t w1[4] = {wv1.x, wv1.y, wv1.z, wv1.w};
-          float ga[2][NT][4];  // two independent accumulation chains (even / odd words)
-#pragma unroll
-          for (int ch = 0; ch < 2; ++ch)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) ga[ch][nt][e] = 0.f;
-#pragma unroll
-          for (int jw = 0; jw < 4; ++jw) {
-            // nibble pairs (s, s+4) as bf16 128 + q (exact); the zero point is folded below
-            uint32_t pa[4], pb[4];
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              pa[s] = lop3_and_or(w0[jw] >> (4 * s), 0x000f000fu, 0x43004300u);
-              pb[s] = lop3_and_or(w1[jw] >> (4 * s), 0x000f000fu, 0x43004300u);
-            }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const uint4 bv = bx[nt][jw];
-                mma_bf16(ga[jw & 1][nt], pa[2 * hh], pb[2 * hh], pa[2 * hh + 1], pb[2 * hh + 1], hh ? bv.z : bv.x,
-                         hh ? bv.w : bv.y);
+          for (int h = 0; h < 2; ++h) {
+            if constexpr (FMT == kInt4G128) {
+              if (2 * st.j + h < p.G) {
+                const long long idx = static_cast<long long>(row) * p.G + 2 * st.j + h;
+                sraw[rr] |= static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p.scales) + idx)) << (16 * h);
+                zraw[rr] |= static_cast<uint32_t>(__ldg(p.zeros + idx)) << (16 * h);
               }
-          }
-          // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)   (zero-point cross term)
+            } else {
+              const uint8_t* E = reinterpret_cast<const uint8_t*>(p.scales) + static_cast<long long>(row) * p.KB;
+              const int b0 = (2 * st.j + h) * 4;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float2 xs = *reinterpret_cast<const float2*>(&sm.xsum[slot][h][2 * t + 8 * nt]);
-            acc[nt][0] = fmaf(m0.y, xs.x, fmaf(m0.x, ga[0][nt][0] + ga[1][nt][0], acc[nt][0]));
-            acc[nt][1] = fmaf(m0.y, xs.y, fmaf(m0.x, ga[0][nt][1] + ga[1][nt][1], acc[nt][1]));
-            acc[nt][2] = fmaf(m1.y, xs.x, fmaf(m1.x, ga[0][nt][2] + ga[1][nt][2], acc[nt][2]));
-            acc[nt][3] = fmaf(m1.y, xs.y, fmaf(m1.x, ga[0][nt][3] + ga[1][nt][3], acc[nt][3]));
-          }
-        } else {
-          // MXFP4: lane t holds 8 codes of each 32-block; two k16 steps per block.
-          const uint32_t e0 = __float_as_uint(m0.x), e1 = __float_as_uint(m1.x);
-          float sacc[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-#pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            const int c = 4 * h + blk;
-            const uint32_t wr0 = *reinterpret_cast<const uint32_t*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4) + 4 * t);
-            const uint32_t wr1 = *reinterpret_cast<const uint32_t*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4) + 4 * t);
-            float bacc[NT][4];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) bacc[nt][e] = 0.f;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t a0 = e2m1x2_to_f16x2((wr0 >> (16 * hh)) & 0xffu);
-              const uint32_t a2 = e2m1x2_to_f16x2((wr0 >> (16 * hh + 8)) & 0xffu);
-              const uint32_t a1 = e2m1x2_to_f16x2((wr1 >> (16 * hh)) & 0xffu);
-              const uint32_t a3 = e2m1x2_to_f16x2((wr1 >> (16 * hh + 8)) & 0xffu);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const uint4 bv = bx[nt][blk];
-                mma_f16(bacc[nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
-              }
+              for (int q2 = 0; q2 < 4; ++q2)
+                if (b0 + q2 < p.KB) eb[rr][h] |= static_cast<uint32_t>(__ldg(E + b0 + q2)) << (8 * q2);
             }
-            const float f0 = e8m0_to_f32((e0 >> (8 * blk)) & 0xffu);
-            const float f1 = e8m0_to_f32((e1 >> (8 * blk)) & 0xffu);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              sacc[nt][0] = fmaf(f0, bacc[nt][0], sacc[nt][0]);
-              sacc[nt][1] = fmaf(f0, bacc[nt][1], sacc[nt][1]);
-              sacc[nt][2] = fmaf(f1, bacc[nt][2], sacc[nt][2]);
-              sacc[nt][3] = fmaf(f1, bacc[nt][3], sacc[nt][3]);
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const float2 xf = *reinterpret_cast<const float2*>(&sm.xf[slot][2 * t + 8 * nt]);
-            acc[nt][0] = fmaf(xf.x, sacc[nt][0], acc[nt][0]);
-            acc[nt][1] = fmaf(xf.y, sacc[nt][1], acc[nt][1]);
-            acc[nt][2] = fmaf(xf.x, sacc[nt][2], acc[nt][2]);
-            acc[nt][3] = fmaf(xf.y, sacc[nt][3], acc[nt][3]);
           }
         }
       }
-      __syncwarp();
-      mbar_arrive(&sm.empty[slot]);
+
+      if (!mbar_wait(&sm.full_x[xs], xph, &g_gemv_err, kErrWaitFull)) break;
+      if (!mbar_wait(&sm.full_w[ws], wph, &g_gemv_err, kErrWaitFull)) break;
+
+      if (p.meta_tma) {
+        if constexpr (FMT == kInt4G128) {
+          const int cb = 2 * ((2 * st.j) & 7);   // byte offset of group 2j inside the 16-byte row
+          sraw[0] = *reinterpret_cast<const uint32_t*>(&sm.mraw[ws][r0 * 16 + cb]);
+          sraw[1] = *reinterpret_cast<const uint32_t*>(&sm.mraw[ws][r1 * 16 + cb]);
+          zraw[0] = *reinterpret_cast<const uint32_t*>(&sm.mraw[ws][kBand * 16 + r0 * 16 + cb]);
+          zraw[1] = *reinterpret_cast<const uint32_t*>(&sm.mraw[ws][kBand * 16 + r1 * 16 + cb]);
+        } else {
+          const int cw4 = ((8 * st.j) & 15) >> 2;  // word of group 2j inside the 16-byte row
+          const uint2 e0 = *reinterpret_cast<const uint2*>(&sm.mraw[ws][r0 * 16 + 4 * cw4]);
+          const uint2 e1 = *reinterpret_cast<const uint2*>(&sm.mraw[ws][r1 * 16 + 4 * cw4]);
+          eb[0][0] = e0.x; eb[0][1] = e0.y;
+          eb[1][0] = e1.x; eb[1][1] = e1.y;
+        }
+      }
+
+      const uint8_t* wt = &sm.w[ws][0];
+      if constexpr (FMT == kInt4G128) {
+        // Both groups at once.  PAR words per step with their own accumulators keep four
+        // independent MMA chains in flight per warp (groups x word parity x n-tiles).
+        constexpr int PAR = (NT == 1) ? 2 : 1;
+        uint32_t w0[2][4], w1[2][4];   // [group][word] rows r0 / r1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 4 * h + t;
+          const uint4 a = *reinterpret_cast<const uint4*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4));
+          const uint4 b = *reinterpret_cast<const uint4*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4));
+          w0[h][0] = a.x; w0[h][1] = a.y; w0[h][2] = a.z; w0[h][3] = a.w;
+          w1[h][0] = b.x; w1[h][1] = b.y; w1[h][2] = b.z; w1[h][3] = b.w;
+        }
+        float ga[2][PAR][NT][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < PAR; ++q)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ga[h][q][nt][e] = 0.f;
+#pragma unroll
+        for (int jh = 0; jh < 4 / PAR; ++jh) {
+          uint4 bx[2][PAR][NT];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int q = 0; q < PAR; ++q)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) bx[h][q][nt] = sm.x[xs][nt][h][jh * PAR + q][lane];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int q = 0; q < PAR; ++q)
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int jw = jh * PAR + q;
+                // nibble pairs (s, s+4) as bf16 128 + q (exact); the zero point is folded below
+                const uint32_t a0 = lop3_and_or(w0[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                const uint32_t a1 = lop3_and_or(w1[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                const uint32_t a2 = lop3_and_or(w0[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                const uint32_t a3 = lop3_and_or(w1[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                  const uint4 bv = bx[h][q][nt];
+                  mma_bf16(ga[h][q][nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
+                }
+              }
+        }
+        // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)   (zero-point cross term)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[0] >> (16 * h))));
+          const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[1] >> (16 * h))));
+          const float c0 = -s0 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[0] >> (16 * h)))));
+          const float c1 = -s1 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[1] >> (16 * h)))));
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float2 xs2 = *reinterpret_cast<const float2*>(&sm.xsum[xs][h][2 * t + 8 * nt]);
+            float gs[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              gs[e] = ga[h][0][nt][e];
+#pragma unroll
+              for (int q = 1; q < PAR; ++q) gs[e] += ga[h][q][nt][e];
+            }
+            acc[nt][0] = fmaf(c0, xs2.x, fmaf(s0, gs[0], acc[nt][0]));
+            acc[nt][1] = fmaf(c0, xs2.y, fmaf(s0, gs[1], acc[nt][1]));
+            acc[nt][2] = fmaf(c1, xs2.x, fmaf(s1, gs[2], acc[nt][2]));
+            acc[nt][3] = fmaf(c1, xs2.y, fmaf(s1, gs[3], acc[nt][3]));
+          }
+        }
+      } else {
+        // MXFP4: lane t holds 8 codes of each 32-block; two k16 steps per block.  The two
+        // groups' blocks run side by side (independent accumulators).
+        float sacc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t wr0[2], wr1[2];
+          uint4 bx[2][NT];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = 4 * h + blk;
+            wr0[h] = *reinterpret_cast<const uint32_t*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4) + 4 * t);
+            wr1[h] = *reinterpret_cast<const uint32_t*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4) + 4 * t);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) bx[h][nt] = sm.x[xs][nt][h][blk][lane];
+          }
+          float bacc[2][NT][4];
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) bacc[h][nt][e] = 0.f;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t a0 = e2m1x2_to_f16x2((wr0[h] >> (16 * hh)) & 0xffu);
+              const uint32_t a2 = e2m1x2_to_f16x2((wr0[h] >> (16 * hh + 8)) & 0xffu);
+              const uint32_t a1 = e2m1x2_to_f16x2((wr1[h] >> (16 * hh)) & 0xffu);
+              const uint32_t a3 = e2m1x2_to_f16x2((wr1[h] >> (16 * hh + 8)) & 0xffu);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const uint4 bv = bx[h][nt];
+                mma_f16(bacc[h][nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
+              }
+            }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float f0 = e8m0_to_f32((eb[0][h] >> (8 * blk)) & 0xffu);
+            const float f1 = e8m0_to_f32((eb[1][h] >> (8 * blk)) & 0xffu);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              sacc[nt][0] = fmaf(f0, bacc[h][nt][0], sacc[nt][0]);
+              sacc[nt][1] = fmaf(f0, bacc[h][nt][1], sacc[nt][1]);
+              sacc[nt][2] = fmaf(f1, bacc[h][nt][2], sacc[nt][2]);
+              sacc[nt][3] = fmaf(f1, bacc[h][nt][3], sacc[nt][3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float2 xf = *reinterpret_cast<const float2*>(&sm.xf[xs][2 * t + 8 * nt]);
+          acc[nt][0] = fmaf(xf.x, sacc[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(xf.y, sacc[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(xf.x, sacc[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(xf.y, sacc[nt][3], acc[nt][3]);
+        }
+      }
+      mbar_arrive(&sm.empty_w[ws]);
+      mbar_arrive(&sm.empty_x[xs]);
 
       if (st.seg_last()) {
         const int band = st.band;
@@ -609,13 +658,8 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 template <int FMT, int MT>
 static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
                                  const gemv::Params& p, cudaStream_t stream) {
-  // activations: MT rows x 256 k per stage; rows >= M and columns >= K come back as zeros
-  CUtensorMap tx;
-  cudaError_t ex = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.X, static_cast<uint64_t>(p.K),
-                                static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K) * 2, 256, MT,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (ex != cudaSuccess) return ex;
   using S = gemv::Smem<FMT, MT>;
+  static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT>;
   static bool attr_set[64] = {false};  // once per device
@@ -626,7 +670,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, tx, p);
+  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, p);
   return cudaGetLastError();
 }
 
@@ -658,7 +702,7 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
   // Metadata tiles travel with the weights by TMA when the metadata row pitch is a multiple
-  // of 16 bytes (INT4: K % 1024 == 0; MXFP4: K % 512 == 0); otherwise the prep warps gather
+  // of 16 bytes (INT4: K % 1024 == 0; MXFP4: K % 512 == 0); otherwise the consumers gather
   // them.  Unused descriptors are copies of the weight descriptor (never dereferenced).
   ts = tw;
   tz = tw;
