@@ -110,6 +110,21 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, in
       : "memory");
 }
 
+// Warm L2 with a 2-D tile (no shared-memory destination, no completion tracking).  L2 is the
+// point of coherence, so a later write to the same lines by another kernel is never hidden.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(desc)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the stream start
+// its CTAs as SMs free up; wait blocks until every prerequisite grid has completed and its
+// memory operations are visible (it returns at once for a kernel launched without the
+// programmatic-serialization attribute).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // L2 eviction-priority policies for the cache_hint operand.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;

@@ -5,17 +5,17 @@
 // design goal is to stream the 0.53125 B/weight of packed weights + metadata once, at full
 // HBM bandwidth, with the arithmetic hidden underneath.
 //
-// Structure (one persistent CTA per SM, warp-specialised, 19 warps):
+// Structure (one persistent CTA per SM, warp-specialised, 20 warps):
 //   warp 0      TMA producer: 256-row x 128-byte tiles of the packed weights (two 128-k
 //               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4- or 5-stage smem
 //               ring, with the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
-//   warps 1-2   prep (stage i by prep warp i % 2), on a separate 4-stage ring: the
+//   warps 1-3   prep (stage i by prep warp i % 3), on a separate 6-stage ring: the
 //               activations of the stage's k-range (from L2; they are small and shared by
 //               every CTA) in the exact order of the mma.sync B fragments, with their
 //               per-group sums (INT4) or converted to fp16 with a per-row power-of-two scale
 //               that keeps every value in fp16 range (MXFP4).  The activations do not depend
 //               on the weights, so this runs ahead of the weight stream.
-//   warps 3-18  consumers: 16 weight rows each; per-row metadata straight from its tile,
+//   warps 4-19  consumers: 16 weight rows each; per-row metadata straight from its tile,
 //               nibbles unpacked in registers, tensor-core mma.sync with fp32 accumulation,
 //               group scale applied in fp32 afterwards.
 //
@@ -54,13 +54,13 @@ constexpr int kConsumerWarps = 16;
 constexpr int kRowsPerWarp = 16;                     // one m16 row tile per consumer warp
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
-constexpr int kXStages = 4;                          // activation-fragment ring depth
-constexpr int kPrepWarps = 2;                        // stage i is prepared by prep warp i % 2
+constexpr int kPrepWarps = 3;                        // stage i is prepared by prep warp i % 3
+constexpr int kXStages = 2 * kPrepWarps;             // activation-fragment ring depth
 // Each prep warp owns whole ring slots (kXStages % kPrepWarps == 0), so it waits on every phase
 // of its slots' barriers in order; a parity wait two phases ahead would pass at once.
 static_assert(kXStages % kPrepWarps == 0, "prep warps must own whole ring slots");
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
-constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 608
+constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 640
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
 constexpr int kSmemLimit = 227 * 1024;               // dynamic shared memory per CTA
 constexpr int kSmemReserve = 1024 + 512;             // alignment pad + barriers and flags
@@ -114,8 +114,11 @@ struct Smem {
   uint64_t empty_w[WS];
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
-  uint64_t group_bar;                        // consumer barrier (bounded wait), split-K path
-  int reduce_flag;
+  uint64_t prep_done;                        // every prep thread arrives once it has no tail left
+  // Split-K reductions this CTA must perform (a CTA has at most two partial bands): slot k
+  // holds band + 1 once posted (release), 0 before; slots are claimed in order via req_alloc.
+  int req_band[2];
+  int req_alloc;
 };
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
@@ -165,6 +168,68 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
+}
+
+// Counter update that publishes (release) this CTA's partial sums and, for the last
+// contributor, makes every other contributor's partial sums visible (acquire), at GPU scope.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ void st_release_cta(int* p, int v) {
+  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_cta(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// One share of the deterministic split-K reduction of a band: the partial sums of every
+// contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
+// of the M x kBand outputs; bf16 results to Y.
+template <int MT>
+__device__ __forceinline__ void reduce_band_share(const Params& p, int band, int first, int step) {
+  const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
+  // Contributors: CTAs whose unit range meets this band.  CTA c_lo holds the band's first
+  // unit; every later contributor starts inside the band (partial slot 0); c_lo uses slot 1
+  // when its range started in an earlier band.
+  int c_lo = static_cast<int>((bs * p.P) / p.U);
+  while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
+  while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
+  int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
+  while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
+  while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
+  const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
+  const long long cstride = 2LL * MT * kBand;   // floats between two CTAs' partial slots
+  for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
+    const int m = idx / (kBand / 4);
+    const int r4 = 4 * (idx % (kBand / 4));
+    const float* base = p.part + static_cast<long long>(m) * kBand + r4;
+    float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand);
+    for (int c = c_lo + 1; c <= c_hi; c += 8) {
+      float4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[q] = (c + q <= c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c + q <= c_hi) {
+          acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
+        }
+    }
+    const float o4[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int n = band * kBand + r4 + q;
+      if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o4[q]));
+    }
+  }
 }
 
 // Stage i of a CTA = unit u0 + i = (band, group pair j).  Ranges are split at pair
@@ -217,7 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.full_x[s], 32);
       mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
-    mbar_init(&sm.group_bar, 32 * kConsumerWarps);
+    mbar_init(&sm.prep_done, 32 * kPrepWarps);
+    sm.req_band[0] = 0;
+    sm.req_band[1] = 0;
+    sm.req_alloc = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -226,6 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   //   INT4:  scales and zeros [N, G] fp16, box 8 groups x 256 rows at x = (2j) & ~7.
   //   MXFP4: E8M0 [N, K/32] bytes, box 16 bytes x 256 rows at x = (8j) & ~15.
   constexpr int kMetaBytes = meta_raw_bytes(FMT);
+
+  // The next kernel of the stream may start its CTAs as this grid's CTAs exit.
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -239,6 +310,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_m = l2_policy_evict_last();
       Cursor st;
       st.init(u0, u1, p.GP, p.G);
+      {
+        // While the previous kernel of the stream finishes: pull the first stages' weights
+        // into L2.  Every read that lands in shared memory comes after the wait below.
+        Cursor pf = st;
+        for (int q = 0; q < WS && q < nstages; ++q, pf.next()) {
+          tma_prefetch_l2_2d(&tmap_w, pf.j * 128, pf.band * kBand);
+          if (p.meta_tma && (q == 0 || (FMT == kInt4G128 ? (pf.j & 3) == 0 : (pf.j & 1) == 0))) {
+            if constexpr (FMT == kInt4G128) {
+              tma_prefetch_l2_2d(&tmap_s, (2 * pf.j) & ~7, pf.band * kBand);
+              tma_prefetch_l2_2d(&tmap_z, (2 * pf.j) & ~7, pf.band * kBand);
+            } else {
+              tma_prefetch_l2_2d(&tmap_s, (8 * pf.j) & ~15, pf.band * kBand);
+            }
+          }
+        }
+      }
+      pdl_wait();
       int i = 0;
       for (; i < nstages; ++i, st.next()) {
         const int slot = i % WS;
@@ -265,104 +353,142 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ prep
     // Activations only: they do not depend on the weight tiles, so the prep warps run up to
     // kXStages stages ahead of the consumers and stay off the weight ring's critical path.
+    // Lane L owns the 8 activations at k = 256 j + 8 L of every row m < M (one coalesced 512-byte
+    // row per warp load), so the work scales with M, not with the padded fragment height.
+    //   INT4:  L = 16 h + 4 t + v  (group h, fragment lane t, vector v: k = 128 h + 32 t + 8 v)
+    //   MXFP4: L = 16 h + 4 blk + t (group h, block blk, fragment lane t: k = 128 h + 32 blk + 8 t)
     const int pw = warp - 1;
-    const int t = lane & 3;
+    const int h = lane >> 4;
+    const int ft = (FMT == kInt4G128) ? ((lane >> 2) & 3) : (lane & 3);   // fragment lane t
+    const int fv = (FMT == kInt4G128) ? (lane & 3) : ((lane >> 2) & 3);   // vector / block
+    constexpr int kRowBatch = 8;   // rows loaded per round trip
+    // Fragment rows M..MT-1 are never written by the stages; zero them once in the slots this
+    // warp owns so the unused MMA columns see finite values.
+    for (int slot = pw; slot < kXStages; slot += kPrepWarps) {
+      for (int m = p.M; m < MT; ++m) {
+        sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = make_uint4(0u, 0u, 0u, 0u);
+        if (lane < 2) sm.xsum[slot][lane][m] = 0.f;
+        if (lane == 0) sm.xf[slot][m] = 1.f;
+      }
+    }
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int q = 0; q < pw; ++q) st.next();
-    for (int i = pw; i < nstages; i += kPrepWarps) {
+    // Loads of row batch 0 of the next stage are issued before the current stage is processed.
+    uint4 xb[kRowBatch];
+    auto load_batch = [&](int j, int m0, uint4 (&dst)[kRowBatch]) {
+      const int k = 256 * j + 8 * lane;
+#pragma unroll
+      for (int r = 0; r < kRowBatch; ++r) {
+        const int m = m0 + r;
+        dst[r] = (m < p.M && k < p.K) ? ldg_nc_v4(p.X + static_cast<long long>(m) * p.K + k)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // Split-K tails.  A band shared by several CTAs ends, in each of them, with fp32 partial
+    // sums that the consumers store before releasing the stage's activation slot.  The prep
+    // warp that next acquires that slot (the same warp: kXStages % kPrepWarps == 0) publishes
+    // the contribution with one GPU-scope acq_rel counter update.  The last contributor posts
+    // a reduction request; the 16 consumer warps sum every contributor's partials in CTA
+    // order (deterministic) and write the bf16 outputs.  Nobody waits on another CTA.
+    // Pending tails of this warp's last two stages (i - 3 and i - 6): band (-1: none), units.
+    int tb0 = -1, tu0 = 0, tb1 = -1, tu1 = 0;
+    auto split_tail = [&](int band, int units) {
+      if (lane == 0) {
+        const uint32_t old = atom_add_acq_rel_gpu(p.cnt + band, static_cast<uint32_t>(units));
+        if (old + static_cast<uint32_t>(units) == static_cast<uint32_t>(p.GP)) {
+          // last contributor: the consumers sum the band (acquire above, release below)
+          atomicExch(p.cnt + band, 0u);   // ready for the next launch
+          const int k = atomicAdd(&sm.req_alloc, 1);
+          st_release_cta(&sm.req_band[k], band + 1);
+        }
+      }
+      __syncwarp();
+    };
+    pdl_wait();   // the activations (and the split-K counters) may come from the previous kernel
+    if (pw < nstages) load_batch(st.j, 0, xb);
+    // Stages i >= nstages are not prepared; their slot waits only deliver the last tails.
+    for (int i = pw; i < nstages + kXStages; i += kPrepWarps) {
       const int slot = i % kXStages;
       const uint32_t ph = (i / kXStages) & 1;
+      const bool hs = ((i / kPrepWarps) & 1) != 0;
+      const int pend_band = hs ? tb1 : tb0;          // tail of stage i - kXStages, -1 if none
+      const int pend_units = hs ? tu1 : tu0;
+      if (i >= nstages && pend_band < 0) continue;  // nothing left to publish
       if (!mbar_wait(&sm.empty_x[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-      const int k0 = 256 * st.j;
+      // the consumers are done with stage i - kXStages (same slot) and stored its partials
+      if (pend_band >= 0) split_tail(pend_band, pend_units);
+      int nb = -1, nu = 0;
+      if (i < nstages && st.seg_last()) {
+        const int band = st.band;
+        const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
+                          (st.seg_end == static_cast<long long>(band + 1) * p.GP);
+        if (!full) { nb = band; nu = static_cast<int>(st.seg_end - st.seg_start); }
+      }
+      if (hs) { tb1 = nb; tu1 = nu; } else { tb0 = nb; tu0 = nu; }
+      if (i >= nstages) continue;
+      const int j = st.j;
+      for (int q = 0; q < kPrepWarps; ++q) st.next();
+      const bool more = i + kPrepWarps < nstages;
+      for (int m0 = 0; m0 < p.M; m0 += kRowBatch) {
+        uint4 cur[kRowBatch];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int m = (lane >> 2) + 8 * nt;
-        const uint16_t* xrow = p.X + static_cast<long long>(m) * p.K;
-        if constexpr (FMT == kInt4G128) {
-          // lane t: elements 32t .. 32t+31 of each group (K % 128 == 0: a group is all in or out)
-          uint4 r[2][4];
+        for (int r = 0; r < kRowBatch; ++r) cur[r] = xb[r];
+        if (m0 + kRowBatch < p.M) load_batch(j, m0 + kRowBatch, xb);   // next batch of this stage
+        else if (more) load_batch(st.j, 0, xb);                        // first batch of the next stage
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int k = k0 + 128 * h + 32 * t + 8 * v;
-              r[h][v] = (m < p.M && k < p.K) ? ldg_nc_v4(xrow + k) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
+        for (int r = 0; r < kRowBatch; ++r) {
+          const int m = m0 + r;
+          if (m >= p.M) break;
+          const uint4 x = cur[r];
+          const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+          if constexpr (FMT == kInt4G128) {
+            // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
+            uint4 o;
+            o.x = prmt(x.x, x.z, 0x5410);
+            o.y = prmt(x.x, x.z, 0x7632);
+            o.z = prmt(x.y, x.w, 0x5410);
+            o.w = prmt(x.y, x.w, 0x7632);
+            sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = o;
             float sum = 0.f;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint4 x = r[h][v];
-              // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
-              uint4 o;
-              o.x = prmt(x.x, x.z, 0x5410);
-              o.y = prmt(x.x, x.z, 0x7632);
-              o.z = prmt(x.y, x.w, 0x5410);
-              o.w = prmt(x.y, x.w, 0x7632);
-              sm.x[slot][nt][h][v][lane] = o;
-              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) sum += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
-            }
+            for (int q = 0; q < 4; ++q) sum += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
+            // the 16 lanes of group h
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (t == 0) sm.xsum[slot][h][m] = sum;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+            if ((lane & 15) == 0) sm.xsum[slot][h][m] = sum;
+          } else {
+            // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
+            uint32_t mx = 0u;  // max |x| bit pattern over the stage's 256 k (bf16 magnitudes order like integers)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
+#pragma unroll
+            for (int sh = 1; sh < 32; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+            const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
+            const int kk = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);  // inf/nan: no scaling
+            const float inv = __uint_as_float(static_cast<uint32_t>(127 - kk) << 23);
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv,
+                                             __uint_as_float(w4[q] & 0xffff0000u) * inv);
+              o[q] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+            sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = make_uint4(o[0], o[1], o[2], o[3]);
+            if (lane == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + kk) << 23);
           }
-        } else {
-          // lane t: elements 8t .. 8t+7 of each 32-block (K % 32 == 0: a block is all in or out)
-          uint4 raw[2][4];
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              const int k = k0 + 128 * h + 32 * blk + 8 * t;
-              raw[h][blk] = (m < p.M && k < p.K) ? ldg_nc_v4(xrow + k) : make_uint4(0u, 0u, 0u, 0u);
-            }
-          // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
-          uint32_t mx = 0u;  // max |x| bit pattern (bf16 magnitudes order like integers)
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              const uint4 x = raw[h][blk];
-              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
-            }
-          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-          mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-          const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
-          const int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);   // inf/nan: no scaling
-          const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-              const uint4 x = raw[h][blk];
-              const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-              uint32_t o[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv,
-                                               __uint_as_float(w4[q] & 0xffff0000u) * inv);
-                o[q] = *reinterpret_cast<uint32_t*>(&hh);
-              }
-              sm.x[slot][nt][h][blk][lane] = make_uint4(o[0], o[1], o[2], o[3]);
-            }
-          if (t == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
         }
       }
       mbar_arrive(&sm.full_x[slot]);
-      for (int q = 0; q < kPrepWarps; ++q) st.next();
     }
+    mbar_arrive(&sm.prep_done);
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - kFirstConsumer;
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int tid = threadIdx.x - 32 * kFirstConsumer;  // 0..511
     const int r0 = cw * kRowsPerWarp + frag_row(g);      // rows (inside the band) of this lane
     const int r1 = cw * kRowsPerWarp + frag_row(g + 8);
 
@@ -372,7 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 
-    uint32_t gphase = 0;  // phase parity of group_bar
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int i = 0; i < nstages; ++i, st.next()) {
@@ -566,8 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[nt][3] = fmaf(xf.y, sacc[nt][3], acc[nt][3]);
         }
       }
-      mbar_arrive(&sm.empty_w[ws]);
-      mbar_arrive(&sm.empty_x[xs]);
+      mbar_arrive(&sm.empty_w[ws]);   // weights consumed: the producer may refill the slot
 
       if (st.seg_last()) {
         const int band = st.band;
@@ -584,6 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
             }
         } else {
+          // partial sums; the prep warp owning this activation slot publishes them
           const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
           float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
 #pragma unroll
@@ -593,46 +718,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int m = 2 * t + (e & 1) + 8 * nt;
               __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
             }
-          __threadfence();
-          mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) break;
-          gphase ^= 1u;
-          if (tid == 0) {
-            const uint32_t mine = static_cast<uint32_t>(st.seg_end - st.seg_start);
-            const uint32_t old = atomicAdd(p.cnt + band, mine);
-            sm.reduce_flag = (old + mine == static_cast<uint32_t>(p.GP)) ? 1 : 0;
-          }
-          mbar_arrive(&sm.group_bar);
-          if (!mbar_wait(&sm.group_bar, gphase, &g_gemv_err, kErrWaitReduce)) break;
-          gphase ^= 1u;
-          if (sm.reduce_flag) {
-            __threadfence();
-            // Contributors: CTAs whose unit range meets this band, summed in CTA order.  CTA
-            // c_lo holds the band's first unit; every later contributor starts inside the band
-            // (partial slot 0), c_lo uses slot 1 when its range started in an earlier band.
-            const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
-            int c_lo = static_cast<int>((bs * p.P) / p.U);
-            while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
-            while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
-            int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
-            while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
-            while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
-            const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
-            const int r = tid & (kBand - 1);
-            const int n = band * kBand + r;
-            for (int m = tid >> 8; m < p.M; m += 2) {
-              float sum = ld_cg_f32(p.part + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand + m * kBand + r);
-              for (int c = c_lo + 1; c <= c_hi; ++c)
-                sum += ld_cg_f32(p.part + static_cast<long long>(c) * 2 * MT * kBand + m * kBand + r);
-              if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-            }
-            if (tid == 0) atomicExch(p.cnt + band, 0u);
-          }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+      }
+      mbar_arrive(&sm.empty_x[xs]);   // release: orders the partial-sum stores before the tail
+    }
+    // Reductions posted by the prep warps (the last tails are published after the final
+    // stage): wait until the prep warps are done, then take this warp's share, 1/16 of the
+    // float4 slots of each band.
+    if (mbar_wait(&sm.prep_done, 0, &g_gemv_err, kErrWaitReduce)) {
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {
+        const int b1 = ld_acquire_cta(&sm.req_band[k]);
+        if (b1 == 0) break;
+        reduce_band_share<MT>(p, b1 - 1, cw * 32 + lane, 32 * kConsumerWarps);
       }
     }
   }
@@ -670,8 +772,20 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  kern<<<p.P, gemv::kThreads, smem, stream>>>(tw, ts, tz, p);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the CTAs may launch while the previous kernel of the
+  // stream is still running; the kernel itself waits (griddepcontrol.wait) before it reads
+  // anything that kernel may have written.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.P));
+  cfg.blockDim = dim3(gemv::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, p);
 }
 
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
