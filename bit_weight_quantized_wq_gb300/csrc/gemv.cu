@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = lane >> 4;
     const int ft = (FMT == kInt4G128) ? ((lane >> 2) & 3) : (lane & 3);   // fragment lane t
     const int fv = (FMT == kInt4G128) ? (lane & 3) : ((lane >> 2) & 3);   // vector / block
-    constexpr int kRowBatch = 8;   // rows loaded per round trip
+    constexpr int kRowBatch = 4;   // rows loaded per round trip (8 spills registers)
     // Fragment rows M..MT-1 are never written by the stages; zero them once in the slots this
     // warp owns so the unused MMA columns see finite values.
     for (int slot = pw; slot < kXStages; slot += kPrepWarps) {
