@@ -107,11 +107,14 @@ struct Smem {
   static constexpr int WS = w_stages(FMT, MT);
   uint8_t w[WS][kTileBytes];                 // SWIZZLE_128B weight tiles (1024-aligned)
   uint8_t mraw[WS][meta_raw_bytes(FMT)];     // raw metadata tiles (TMA), 16 B per row per tensor
-  uint4 x[kXStages][NT][2][4][32];           // B fragments [nt][group][vec][lane]
+  // B fragments [nt][group][vec][lane].  A stage's raw activations (MT rows x 256 k bf16, row m
+  // at byte 512 m -- the same size) land here by TMA and are converted in place.
+  uint4 x[kXStages][NT][2][4][32];
   float xsum[kXStages][2][MT];               // INT4: sum of the group's activations per row m
   float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row
   uint64_t full_w[WS];
   uint64_t empty_w[WS];
+  uint64_t raw_x[kXStages];                  // the stage's raw activation rows landed (TMA)
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
   uint64_t prep_done;                        // every prep thread arrives once it has no tail left
@@ -259,7 +262,8 @@ struct Cursor {
 template <int FMT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-           const __grid_constant__ CUtensorMap tmap_z, const Params p) {
+           const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
+           const Params p) {
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
   constexpr int WS = S::WS;
@@ -279,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.empty_w[s], 32 * kConsumerWarps);
     }
     for (int s = 0; s < kXStages; ++s) {
+      mbar_init(&sm.raw_x[s], 1);
       mbar_init(&sm.full_x[s], 32);
       mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
@@ -302,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
+      tma_prefetch_desc(&tmap_x);
       if (p.meta_tma) {
         tma_prefetch_desc(&tmap_s);
         if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
@@ -334,6 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sm.empty_w[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
         mbar_arrive_expect_tx(&sm.full_w[slot], kTileBytes + (p.meta_tma ? kMetaBytes : 0));
         tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
+        // the stage's activations into its fragment slot (free once stage i - kXStages is
+        // consumed; never the binding wait: that ring is deeper than the weight ring)
+        const int xs = i % kXStages;
+        if (!mbar_wait(&sm.empty_x[xs], ((i / kXStages) & 1) ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+        mbar_arrive_expect_tx(&sm.raw_x[xs], MT * 512);
+        tma_load_2d(&sm.x[xs][0][0][0][0], &tmap_x, st.j * 256, 0, &sm.raw_x[xs], pol_m);
         if (p.meta_tma) {
           if constexpr (FMT == kInt4G128) {
             const int gx = (2 * st.j) & ~7;
@@ -348,43 +360,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj < 0) continue;
         mbar_wait(&sm.full_w[jj % WS], (jj / WS) & 1, &g_gemv_err, kErrDrain);
       }
+      for (int jj = i - kXStages; jj < i; ++jj) {
+        if (jj < 0) continue;
+        mbar_wait(&sm.raw_x[jj % kXStages], (jj / kXStages) & 1, &g_gemv_err, kErrDrain);
+      }
     }
   } else if (warp < kFirstConsumer) {
     // ------------------------------------------------------------------ prep
-    // Activations only: they do not depend on the weight tiles, so the prep warps run up to
-    // kXStages stages ahead of the consumers and stay off the weight ring's critical path.
-    // Lane L owns the 8 activations at k = 256 j + 8 L of every row m < M (one coalesced 512-byte
-    // row per warp load), so the work scales with M, not with the padded fragment height.
+    // Activations only.  The producer drops each stage's raw rows into the stage's fragment
+    // slot by TMA (rows >= M and columns >= K zero-filled); prep warp i % 3 converts them in
+    // place, off the weight ring's critical path and without global-memory latency.
+    // Lane L owns the 16-byte chunk L (8 activations at k = 256 j + 8 L) of each row:
     //   INT4:  L = 16 h + 4 t + v  (group h, fragment lane t, vector v: k = 128 h + 32 t + 8 v)
     //   MXFP4: L = 16 h + 4 blk + t (group h, block blk, fragment lane t: k = 128 h + 32 blk + 8 t)
     const int pw = warp - 1;
     const int h = lane >> 4;
     const int ft = (FMT == kInt4G128) ? ((lane >> 2) & 3) : (lane & 3);   // fragment lane t
     const int fv = (FMT == kInt4G128) ? (lane & 3) : ((lane >> 2) & 3);   // vector / block
-    constexpr int kRowBatch = 4;   // rows loaded per round trip (8 spills registers)
-    // Fragment rows M..MT-1 are never written by the stages; zero them once in the slots this
-    // warp owns so the unused MMA columns see finite values.
-    for (int slot = pw; slot < kXStages; slot += kPrepWarps) {
-      for (int m = p.M; m < MT; ++m) {
-        sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = make_uint4(0u, 0u, 0u, 0u);
-        if (lane < 2) sm.xsum[slot][lane][m] = 0.f;
-        if (lane == 0) sm.xf[slot][m] = 1.f;
-      }
-    }
     Cursor st;
     st.init(u0, u1, p.GP, p.G);
     for (int q = 0; q < pw; ++q) st.next();
-    // Loads of row batch 0 of the next stage are issued before the current stage is processed.
-    uint4 xb[kRowBatch];
-    auto load_batch = [&](int j, int m0, uint4 (&dst)[kRowBatch]) {
-      const int k = 256 * j + 8 * lane;
-#pragma unroll
-      for (int r = 0; r < kRowBatch; ++r) {
-        const int m = m0 + r;
-        dst[r] = (m < p.M && k < p.K) ? ldg_nc_v4(p.X + static_cast<long long>(m) * p.K + k)
-                                       : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
     // Split-K tails.  A band shared by several CTAs ends, in each of them, with fp32 partial
     // sums that the consumers store before releasing the stage's activation slot.  The prep
     // warp that next acquires that slot (the same warp: kXStages % kPrepWarps == 0) publishes
@@ -405,8 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    pdl_wait();   // the activations (and the split-K counters) may come from the previous kernel
-    if (pw < nstages) load_batch(st.j, 0, xb);
+    pdl_wait();   // the split-K counters may come from the previous kernel
     // Stages i >= nstages are not prepared; their slot waits only deliver the last tails.
     for (int i = pw; i < nstages + kXStages; i += kPrepWarps) {
       const int slot = i % kXStages;
@@ -427,19 +421,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (hs) { tb1 = nb; tu1 = nu; } else { tb0 = nb; tu0 = nu; }
       if (i >= nstages) continue;
-      const int j = st.j;
       for (int q = 0; q < kPrepWarps; ++q) st.next();
-      const bool more = i + kPrepWarps < nstages;
-      for (int m0 = 0; m0 < p.M; m0 += kRowBatch) {
-        uint4 cur[kRowBatch];
+      if (!mbar_wait(&sm.raw_x[slot], ph, &g_gemv_err, kErrWaitFull)) break;
+      uint4* xs4 = &sm.x[slot][0][0][0][0];
 #pragma unroll
-        for (int r = 0; r < kRowBatch; ++r) cur[r] = xb[r];
-        if (m0 + kRowBatch < p.M) load_batch(j, m0 + kRowBatch, xb);   // next batch of this stage
-        else if (more) load_batch(st.j, 0, xb);                        // first batch of the next stage
+      for (int nt = 0; nt < NT; ++nt) {
+        // 8 rows (one n-tile) in registers, then written back permuted: a row's fragment
+        // positions hold other rows' raw chunks, so every read of the tile precedes every write.
+        const int mlive = p.M - 8 * nt;   // rows of this tile below M
+        uint4 cur[8];
 #pragma unroll
-        for (int r = 0; r < kRowBatch; ++r) {
-          const int m = m0 + r;
-          if (m >= p.M) break;
+        for (int r = 0; r < 8; ++r)
+          cur[r] = (r < mlive) ? xs4[(8 * nt + r) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int m = 8 * nt + r;
+          uint4* dst = &sm.x[slot][nt][h][fv][4 * r + ft];
+          if (r >= mlive) {   // zero-filled row: zero fragments (INT4: zero sums below), unit factor
+            *dst = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (FMT != kInt4G128) {
+              if (lane == 0) sm.xf[slot][m] = 1.f;
+            }
+            continue;
+          }
           const uint4 x = cur[r];
           const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
           if constexpr (FMT == kInt4G128) {
@@ -449,16 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.y = prmt(x.x, x.z, 0x7632);
             o.z = prmt(x.y, x.w, 0x5410);
             o.w = prmt(x.y, x.w, 0x7632);
-            sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = o;
-            float sum = 0.f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) sum += __uint_as_float(w4[q] << 16) + __uint_as_float(w4[q] & 0xffff0000u);
-            // the 16 lanes of group h
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-            if ((lane & 15) == 0) sm.xsum[slot][h][m] = sum;
+            *dst = o;
           } else {
             // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
             uint32_t mx = 0u;  // max |x| bit pattern over the stage's 256 k (bf16 magnitudes order like integers)
@@ -476,11 +472,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              __uint_as_float(w4[q] & 0xffff0000u) * inv);
               o[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
-            sm.x[slot][m >> 3][h][fv][4 * (m & 7) + ft] = make_uint4(o[0], o[1], o[2], o[3]);
+            *dst = make_uint4(o[0], o[1], o[2], o[3]);
             if (lane == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + kk) << 23);
           }
         }
+        if constexpr (FMT == kInt4G128) {
+          // Per-group activation sums of the tile's 8 rows on the tensor core: an all-ones A
+          // times the just-written B fragments gives every column sum (exact products, fp32
+          // accumulation).  Lane (g = 0, t) receives rows 2t, 2t + 1 of the tile.
+          __syncwarp();
+          constexpr uint32_t kOnes = 0x3f803f80u;   // bf16 (1, 1)
+#pragma unroll
+          for (int hg = 0; hg < 2; ++hg) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 b = sm.x[slot][nt][hg][v][lane];
+              mma_bf16(d, kOnes, kOnes, kOnes, kOnes, b.x, b.y);
+              mma_bf16(d, kOnes, kOnes, kOnes, kOnes, b.z, b.w);
+            }
+            if (lane < 4) *reinterpret_cast<float2*>(&sm.xsum[slot][hg][8 * nt + 2 * lane]) = make_float2(d[0], d[1]);
+          }
+        }
       }
+      // the slot is refilled by TMA (async proxy) once consumed: order these generic writes first
+      fence_proxy_async_smem();
       mbar_arrive(&sm.full_x[slot]);
     }
     mbar_arrive(&sm.prep_done);
@@ -760,6 +776,12 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 template <int FMT, int MT>
 static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
                                  const gemv::Params& p, cudaStream_t stream) {
+  // activations: MT rows x 256 k per stage; rows >= M and columns >= K come back as zeros
+  CUtensorMap tx;
+  cudaError_t ex = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.X, static_cast<uint64_t>(p.K),
+                                static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K) * 2, 256, MT,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (ex != cudaSuccess) return ex;
   using S = gemv::Smem<FMT, MT>;
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(S) + 1024;
@@ -785,7 +807,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, p);
+  return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, tx, p);
 }
 
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
