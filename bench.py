@@ -525,6 +525,8 @@ def run_ncu_case(args):
     """A few plain launches of one kernel on one layer, for ncu captures (not a bench line).
 
     decode:  the (K, N) = (4096, 28672) layer at M = 1, INT4, 3 weight copies (189 MB > L2).
+    decode_step: the headline step -- the 12 decode calls (4 shapes x M in {1, 4, 16}), INT4,
+             3 weight copies; one step = 12 launches, run warmup + steps times without a graph.
     prefill: the (K, N) = (8192, 8192) layer at M = 2048, INT4 (37 MB weights, 32 MB X).
     mxfp4:   the decode layer in MXFP4.
     quant:   INT4 quantize of the (4096, 28672) weights (470 MB fp32).
@@ -537,6 +539,28 @@ def run_ncu_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     case = args.ncu_case
+    if case == "decode_step":
+        layers = []
+        for i, (K, N) in enumerate(DECODE_SHAPES):
+            W = torch.from_numpy(inputs.weights(1000 + i, N, K, 0.02)).to(dev)
+            pk = binding.quantize_int4_g128(W)
+            layers.append([pk] + [tuple(t.clone() for t in pk) for _ in range(COPIES - 1)])
+            del W
+        X = {(M, K): torch.from_numpy(inputs.activations(M * 100 + K, M, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+             for M in DECODE_M for K, _ in DECODE_SHAPES}
+        Y = {(M, N): torch.empty((M, N), dtype=torch.bfloat16, device=dev) for M in DECODE_M for _, N in DECODE_SHAPES}
+        ws = binding.Workspace(dev).get(max(binding.gemm_workspace_bytes("int4_g128", M, K, N)
+                                            for M in DECODE_M for K, N in DECODE_SHAPES))
+        n = 0
+        for _ in range(args.warmup + args.steps):
+            for ci, M in enumerate(DECODE_M):
+                for li, (K, N) in enumerate(DECODE_SHAPES):
+                    Wq, s, z = layers[li][ci % COPIES]
+                    binding.gemm_w4a16("int4_g128", X[(M, K)], Wq, s, z, out=Y[(M, N)], workspace=ws)
+                    n += 1
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": case, "launches": n, "launches_per_step": len(DECODE_M) * len(DECODE_SHAPES)}))
+        return 0
     if case in ("decode", "mxfp4"):
         K, N, M, fmt = 4096, 28672, 1, ("int4_g128" if case == "decode" else "mxfp4")
     elif case == "prefill":
@@ -575,7 +599,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-sample", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--ncu-case", default=None, choices=["decode", "prefill", "mxfp4", "quant"],
+    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "quant"],
                     help="run a few plain launches of one kernel (for ncu captures) instead of the bench")
     args = ap.parse_args()
     if args.cpu_sample is not None:

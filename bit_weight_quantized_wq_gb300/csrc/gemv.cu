@@ -869,9 +869,9 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
   return small ? launch_gemv_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kMxfp4, 16>(tw, ts, tz, p, stream);
 }
 
-// The decode entry points run the mma.sync kernel above.  The tcgen05 decode kernel
-// (gemv_tc.cu) is kept for comparison: at N = 16 a tcgen05.mma costs ~56 cycles per
-// 128 x 16 x 16 instruction, which caps it below HBM speed on this shape.
+// The decode entry points run the mma.sync kernel above.  (A tcgen05 variant was measured
+// slower: at N = 16 one 128 x 16 x 16 tcgen05.mma costs ~56 cycles, which caps a 256-row
+// stage below the per-SM share of HBM bandwidth.)
 size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return gemv_mma_workspace_bytes(fmt, M, K, N); }
 
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,

@@ -45,12 +45,6 @@ size_t gemv_noalloc_scratch_bytes();
 cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                                 const void* scales, const uint16_t* zeros, uint16_t* Y, cudaStream_t stream);
 
-// gemv_tc.cu -- decode kernel on tcgen05, M <= 16
-size_t gemv_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
-cudaError_t launch_gemv_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
-                           const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                           cudaStream_t stream);
-uint32_t gemv_tc_read_and_clear_error();
 
 // gemm_tc.cu -- tcgen05 kernel, any M
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
