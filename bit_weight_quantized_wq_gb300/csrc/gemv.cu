@@ -94,6 +94,11 @@ struct Params {
   int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: consumers gather them
 };
 
+// The CTAs that share a band: [c_lo, c_hi].  CTA c_lo holds the band's first unit; every
+// later contributor starts inside the band (partial slot 0); c_lo uses slot 1 when its range
+// started in an earlier band (lo_side).
+struct BandContrib { int c_lo, c_hi, lo_side; };
+
 // Fragment row f (0..15) of a 16-row tile -> row inside the tile.  Rows g and g+4 of a
 // smem swizzle atom then land in disjoint bank groups, so the consumer's 128-bit loads
 // are conflict-free.
@@ -122,6 +127,10 @@ struct Smem {
   // holds band + 1 once posted (release), 0 before; slots are claimed in order via req_alloc.
   int req_band[2];
   int req_alloc;
+  // contributors of the CTA's first and last band (the only ones it can share), computed at
+  // start-up off the critical path
+  int ci_band[2];
+  BandContrib ci[2];
 };
 
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
@@ -192,37 +201,39 @@ __device__ __forceinline__ int ld_acquire_cta(const int* p) {
   return v;
 }
 
-// One share of the deterministic split-K reduction of a band: the partial sums of every
-// contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
-// of the M x kBand outputs; bf16 results to Y.
-template <int MT>
-__device__ __forceinline__ void reduce_band_share(const Params& p, int band, int first, int step) {
+// Contributors to a band: the CTAs whose unit range meets it, [c_lo, c_hi] (see BandContrib).
+
+__device__ BandContrib band_contributors(const Params& p, int band) {
   const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
-  // Contributors: CTAs whose unit range meets this band.  CTA c_lo holds the band's first
-  // unit; every later contributor starts inside the band (partial slot 0); c_lo uses slot 1
-  // when its range started in an earlier band.
   int c_lo = static_cast<int>((bs * p.P) / p.U);
   while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
   while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
   int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
   while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
   while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
-  const int lo_side = unit_start(p.U, p.P, c_lo) < bs ? 1 : 0;
+  return BandContrib{c_lo, c_hi, unit_start(p.U, p.P, c_lo) < bs ? 1 : 0};
+}
+
+// One share of the deterministic split-K reduction of a band: the partial sums of every
+// contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
+// of the M x kBand outputs; bf16 results to Y.
+template <int MT>
+__device__ __forceinline__ void reduce_band_share(const Params& p, int band, BandContrib bc, int first, int step) {
   const long long cstride = 2LL * MT * kBand;   // floats between two CTAs' partial slots
   for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
     const int m = idx / (kBand / 4);
     const int r4 = 4 * (idx % (kBand / 4));
     const float* base = p.part + static_cast<long long>(m) * kBand + r4;
-    float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(c_lo) * 2 + lo_side) * MT * kBand);
-    for (int c = c_lo + 1; c <= c_hi; c += 8) {
+    float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(bc.c_lo) * 2 + bc.lo_side) * MT * kBand);
+    for (int c = bc.c_lo + 1; c <= bc.c_hi; c += 8) {
       float4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        v[q] = (c + q <= c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = (c + q <= bc.c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (c + q <= c_hi) {
+        if (c + q <= bc.c_hi) {
           acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
         }
     }
@@ -400,6 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
+    // (on the last prep warp: its first stage is the CTA's third, so short layers never wait for it)
+    if (pw == kPrepWarps - 1 && lane == 0 && nstages > 0) {
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        const int band = static_cast<int>((q == 0 ? u0 : u1 - 1) / p.GP);
+        sm.ci_band[q] = band;
+        sm.ci[q] = band_contributors(p, band);
+      }
+    }
     pdl_wait();   // the split-K counters may come from the previous kernel
     // Stages i >= nstages are not prepared; their slot waits only deliver the last tails.
     for (int i = pw; i < nstages + kXStages; i += kPrepWarps) {
@@ -750,7 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 2; ++k) {
         const int b1 = ld_acquire_cta(&sm.req_band[k]);
         if (b1 == 0) break;
-        reduce_band_share<MT>(p, b1 - 1, cw * 32 + lane, 32 * kConsumerWarps);
+        const BandContrib bc = sm.ci[sm.ci_band[0] == b1 - 1 ? 0 : 1];
+        reduce_band_share<MT>(p, b1 - 1, bc, cw * 32 + lane, 32 * kConsumerWarps);
       }
     }
   }
