@@ -145,12 +145,16 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Two E2M1 codes (low nibble = first element) -> f16x2 (low half = first element), exact.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t d;
-  const unsigned short h = static_cast<unsigned short>(byte);
-  asm("{\n\t.reg .b8 t, u;\n\tmov.b16 {t, u}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(d) : "h"(h));
-  return d;
+// Four E2M1 code pairs (one 32-bit word, byte b = elements 2b, 2b + 1) -> four f16x2, exact.
+// The word is split into bytes by register moves, with no shifts or masks.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
 }
 
 // Tensor-core MACs.  Not volatile: they are pure functions of their operands, so the
@@ -691,14 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) bacc[h][nt][e] = 0.f;
+          uint32_t f0[2][4], f1[2][4];   // [group][byte] rows r0 / r1 as f16x2
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            e2m1x8_to_f16x2x4(wr0[h], f0[h]);
+            e2m1x8_to_f16x2x4(wr1[h], f1[h]);
+          }
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const uint32_t a0 = e2m1x2_to_f16x2((wr0[h] >> (16 * hh)) & 0xffu);
-              const uint32_t a2 = e2m1x2_to_f16x2((wr0[h] >> (16 * hh + 8)) & 0xffu);
-              const uint32_t a1 = e2m1x2_to_f16x2((wr1[h] >> (16 * hh)) & 0xffu);
-              const uint32_t a3 = e2m1x2_to_f16x2((wr1[h] >> (16 * hh + 8)) & 0xffu);
+              const uint32_t a0 = f0[h][2 * hh], a2 = f0[h][2 * hh + 1];
+              const uint32_t a1 = f1[h][2 * hh], a3 = f1[h][2 * hh + 1];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 const uint4 bv = bx[h][nt];
