@@ -116,7 +116,7 @@ struct Smem {
   // at byte 512 m -- the same size) land here by TMA and are converted in place.
   uint4 x[kXStages][NT][2][4][32];
   float xsum[kXStages][2][MT];               // INT4: sum of the group's activations per row m
-  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row
+  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row (one per 8-row tile)
   uint64_t full_w[WS];
   uint64_t empty_w[WS];
   uint64_t raw_x[kXStages];                  // the stage's raw activation rows landed (TMA)
@@ -458,15 +458,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r)
           cur[r] = (r < mlive) ? xs4[(8 * nt + r) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
+        // MXFP4: one power-of-two scale 2^-k per stage and 8-row tile keeps every operand inside
+        // fp16 (|x| 2^-k < 2^15, k >= 0); values below 2^-29 of the tile's largest lose bits only
+        // as fp16 subnormals.  max |x| over the tile: bf16 magnitudes order like integers.
+        float inv = 1.f, xf = 1.f;
+        if constexpr (FMT != kInt4G128) {
+          uint32_t mx2 = 0u;   // per 16-bit half
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const uint4 x = cur[r];
+            mx2 = __vmaxu2(mx2, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                          __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+          }
+          uint32_t mx = max(mx2 & 0xffffu, mx2 >> 16);
+#pragma unroll
+          for (int sh = 1; sh < 32; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+          const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
+          const int kk = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);  // inf/nan: no scaling
+          inv = __uint_as_float(static_cast<uint32_t>(127 - kk) << 23);
+          xf = __uint_as_float(static_cast<uint32_t>(127 + kk) << 23);
+          if (lane < 8) sm.xf[slot][8 * nt + lane] = xf;
+        }
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          const int m = 8 * nt + r;
           uint4* dst = &sm.x[slot][nt][h][fv][4 * r + ft];
-          if (r >= mlive) {   // zero-filled row: zero fragments (INT4: zero sums below), unit factor
+          if (r >= mlive) {   // zero-filled row: zero fragments (INT4: zero sums below)
             *dst = make_uint4(0u, 0u, 0u, 0u);
-            if constexpr (FMT != kInt4G128) {
-              if (lane == 0) sm.xf[slot][m] = 1.f;
-            }
             continue;
           }
           const uint4 x = cur[r];
@@ -480,15 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.w = prmt(x.y, x.w, 0x7632);
             *dst = o;
           } else {
-            // fp16 operands; row scale 2^-k keeps |x| 2^-k < 2^15 (k >= 0).
-            uint32_t mx = 0u;  // max |x| bit pattern over the stage's 256 k (bf16 magnitudes order like integers)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) mx = max(mx, max(w4[q] & 0x7fffu, (w4[q] >> 16) & 0x7fffu));
-#pragma unroll
-            for (int sh = 1; sh < 32; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-            const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
-            const int kk = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);  // inf/nan: no scaling
-            const float inv = __uint_as_float(static_cast<uint32_t>(127 - kk) << 23);
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -497,7 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               o[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
-            if (lane == 0) sm.xf[slot][m] = __uint_as_float(static_cast<uint32_t>(127 + kk) << 23);
           }
         }
         if constexpr (FMT == kInt4G128) {
