@@ -10,8 +10,8 @@ that every step streams 348 MB (> the 129 MB L2).  The step is replayed from a C
 and timed with CUDA events on its stream.
 
 Secondary measurements in the same run (same JSON line): prefill GEMM TFLOP/s on the
-Qwen2.5-72B shapes at M = 2048, MXFP4 decode, the quantize kernels, and the GEMV/GEMM
-crossover on K = N = 8192.
+Qwen2.5-72B shapes at M = 2048 and M = 8192, MXFP4 decode, the quantize kernels, and the
+GEMV/GEMM crossover on K = N = 8192.
 
 --impl reference times the CPU oracle (test infrastructure, float64) on a bounded sample
 of the same workload on the host cores.
@@ -35,6 +35,7 @@ DECODE_SHAPES = [(4096, 6144), (4096, 4096), (4096, 28672), (14336, 4096)]   # (
 DECODE_M = (1, 4, 16)
 PREFILL_SHAPES = [(8192, 10240), (8192, 8192), (8192, 59136), (29568, 8192)]
 PREFILL_M = 2048
+PREFILL_M_LARGE = 8192
 CROSS_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
 COPIES = 3
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -397,32 +398,36 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
     out = {}
     reps = max(3, min(args.steps, 50))
 
-    # prefill GEMM, Qwen2.5-72B shapes, M = 2048, INT4 g128 (sigma 0.015)
+    # prefill GEMM, Qwen2.5-72B shapes, M = 2048 and 8192, INT4 g128 (sigma 0.015)
     pre = []
     for i, (K, N) in enumerate(PREFILL_SHAPES):
         W = torch.from_numpy(inputs.weights(3000 + i, N, K, 0.015)).to(dev)
         pre.append(binding.quantize_int4_g128(W))
         del W
     torch.cuda.empty_cache()
-    Xp = {K: torch.from_numpy(inputs.activations(3100 + K, PREFILL_M, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
-          for K in {k for k, _ in PREFILL_SHAPES}}
-    Yp = [torch.empty((PREFILL_M, N), dtype=torch.bfloat16, device=dev) for _, N in PREFILL_SHAPES]
-    wsp = binding.Workspace(dev).get(max(binding.gemm_workspace_bytes("int4_g128", PREFILL_M, K, N) for K, N in PREFILL_SHAPES))
-    per_layer = []
-    for i, (K, N) in enumerate(PREFILL_SHAPES):
-        f = (lambda i=i, K=K: binding.gemm_w4a16("int4_g128", Xp[K], pre[i][0], pre[i][1], pre[i][2], out=Yp[i], workspace=wsp))
-        ms = _graph_time(f, stream, dev, max(3, reps // 5))
-        fl = 2.0 * PREFILL_M * N * K
-        per_layer.append({"K": K, "N": N, "M": PREFILL_M, "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12})
-    tot_fl = sum(2.0 * PREFILL_M * N * K for K, N in PREFILL_SHAPES)
-    tot_ms = sum(p["us"] for p in per_layer) / 1e3
-    tf = tot_fl / (tot_ms * 1e-3) / 1e12
-    out["prefill"] = {"metric": "prefill GEMM TFLOP/s (INT4 g128 W4A16, Qwen2.5-72B shapes, M=2048)",
-                      "value": tf, "unit": "TFLOP/s", "layers": per_layer,
-                      "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                                   "frac": tf / bf16_peak, "traffic": profile_traffic("gemm_tc.cu", "gemm_tc_prefill"),
-                                   "note": "fp16 operands (same dense rate as bf16); peak = measured cuBLAS bf16 burst"}}
-    del pre, Xp, Yp
+    for Mp, key in ((PREFILL_M, "prefill"), (PREFILL_M_LARGE, "prefill_m%d" % PREFILL_M_LARGE)):
+        Xp = {K: torch.from_numpy(inputs.activations(3100 + K, Mp, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+              for K in {k for k, _ in PREFILL_SHAPES}}
+        Yp = [torch.empty((Mp, N), dtype=torch.bfloat16, device=dev) for _, N in PREFILL_SHAPES]
+        wsp = binding.Workspace(dev).get(max(binding.gemm_workspace_bytes("int4_g128", Mp, K, N) for K, N in PREFILL_SHAPES))
+        per_layer = []
+        for i, (K, N) in enumerate(PREFILL_SHAPES):
+            f = (lambda i=i, K=K: binding.gemm_w4a16("int4_g128", Xp[K], pre[i][0], pre[i][1], pre[i][2], out=Yp[i], workspace=wsp))
+            ms = _graph_time(f, stream, dev, max(3, reps // (5 if Mp == PREFILL_M else 20)))
+            fl = 2.0 * Mp * N * K
+            per_layer.append({"K": K, "N": N, "M": Mp, "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12})
+        tot_fl = sum(2.0 * Mp * N * K for K, N in PREFILL_SHAPES)
+        tot_ms = sum(q["us"] for q in per_layer) / 1e3
+        tf = tot_fl / (tot_ms * 1e-3) / 1e12
+        out[key] = {"metric": "prefill GEMM TFLOP/s (INT4 g128 W4A16, Qwen2.5-72B shapes, M=%d)" % Mp,
+                    "value": tf, "unit": "TFLOP/s", "layers": per_layer,
+                    "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": tf / bf16_peak,
+                                 "traffic": profile_traffic("gemm_tc.cu", "gemm_tc_prefill") if Mp == PREFILL_M else None,
+                                 "note": "fp16 operands (same dense rate as bf16); peak = measured cuBLAS bf16 burst"}}
+        del Xp, Yp
+        torch.cuda.empty_cache()
+    del pre
     torch.cuda.empty_cache()
 
     # MXFP4 decode (same four shapes, M in {1, 16})
