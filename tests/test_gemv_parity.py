@@ -110,3 +110,72 @@ def test_gemv_full_size_sampled(B, fmt, K, N):
         Y = y_to_host(_run(B, B.gemv_w4a16, fmt, xb, pk))
         ref = linear.linear_rows(fmt, xf, pk[0], pk[1], pk[2] if fmt == "int4_g128" else None, rows)
         assert_close(Y[:, rows], ref, "%s K=%d N=%d M=%d" % (fmt, K, N, M))
+
+
+def _layers(fmt, n_layers, K, seed):
+    return [_pack(fmt, inputs.weights(seed + i, K, K, 0.03)) for i in range(n_layers)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("graph", [False, True])
+def test_gemv_chained_layers_read_the_previous_output(B, fmt, graph):
+    # Each call's activations are the previous call's output, enqueued back to back with no
+    # host synchronisation (and, with graph=True, replayed from one captured graph): every
+    # call must read its input only after the previous kernel finished writing it.
+    import torch
+    M, K, L = 4, 1024, 8
+    pks = _layers(fmt, L, K, 700)
+    dev = [[to_dev(a) for a in pk] for pk in pks]
+    xb, _ = inputs.activations(701, M, K)
+    X0 = x_to_dev(xb)
+    outs = [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ws = torch.zeros(B.gemm_workspace_bytes(fmt, M, K, K), dtype=torch.uint8, device="cuda")
+
+    def chain():
+        x = X0
+        for i in range(L):
+            d = dev[i]
+            B.gemv_w4a16(fmt, x, d[0], d[1], d[2] if fmt == "int4_g128" else None, out=outs[i], workspace=ws)
+            x = outs[i]
+
+    if graph:
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            chain()
+            torch.cuda.synchronize()
+            for o in outs:
+                o.zero_()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                chain()
+            g.replay()
+        torch.cuda.synchronize()
+    else:
+        chain()
+    prev = np.asarray(inputs.activations(701, M, K)[1], dtype=np.float64)
+    for i in range(L):
+        y = y_to_host(outs[i])
+        pk = pks[i]
+        ref = linear.linear_w4a16(fmt, prev, *pk)
+        assert_close(y, ref, "%s layer %d graph=%s" % (fmt, i, graph))
+        prev = y.astype(np.float64)   # the next layer's reference starts from what the GPU produced
+    assert B.read_error_flags() == 0
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_gpu_quantize_then_decode_without_sync(B, fmt):
+    # The decode call is enqueued right behind the quantize kernel that writes its weights.
+    import torch
+    M, N, K = 4, 2048, 2048
+    W = inputs.weights(702, N, K, 0.02)
+    Wd = torch.from_numpy(W).cuda()
+    xb, xf = inputs.activations(703, M, K)
+    X = x_to_dev(xb)
+    if fmt == "int4_g128":
+        Wq, s, z = B.quantize_int4_g128(Wd)
+        Y = B.gemv_w4a16(fmt, X, Wq, s, z)
+    else:
+        Wq, s = B.quantize_mxfp4(Wd)
+        Y = B.gemv_w4a16(fmt, X, Wq, s)
+    ref = linear.linear_w4a16(fmt, xf, *_pack(fmt, W))
+    assert_close(y_to_host(Y), ref, "%s quantize -> decode" % fmt)
