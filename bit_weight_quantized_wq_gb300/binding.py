@@ -87,12 +87,21 @@ def _fmt(fmt) -> int:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+# The current stream's raw handle without building a Stream object (a few microseconds per
+# call otherwise, which dominates small decode calls issued from Python).
+_raw_current_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream=None, device=None):
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_current_stream is not None:
+        idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+        return _raw_current_stream(idx)
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _need(t: torch.Tensor, dtype, name: str) -> None:
@@ -115,8 +124,8 @@ def quantize_int4_g128(W: torch.Tensor, stream=None):
     Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
     scales = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
     zeros = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
-    _check(load_library().wq_quantize_int4_g128(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _ptr(zeros), _stream(stream)),
-           "wq_quantize_int4_g128")
+    _check(load_library().wq_quantize_int4_g128(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _ptr(zeros),
+                                                     _stream(stream, W.device)), "wq_quantize_int4_g128")
     return Wq, scales, zeros
 
 
@@ -126,7 +135,7 @@ def quantize_mxfp4(W: torch.Tensor, stream=None):
     N, K = W.shape
     Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
     scales = torch.empty((N, K // 32), dtype=torch.uint8, device=W.device)
-    _check(load_library().wq_quantize_mxfp4(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _stream(stream)),
+    _check(load_library().wq_quantize_mxfp4(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _stream(stream, W.device)),
            "wq_quantize_mxfp4")
     return Wq, scales
 
@@ -182,12 +191,12 @@ def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     else:
         _need(out, torch.bfloat16, "out")
-    nbytes = gemm_workspace_bytes(f, M, K, N)
-    ws = _workspace_for(X.device, nbytes, workspace)
+    # a caller's workspace is checked by the library itself (WQ_ERR_WORKSPACE when too small)
+    ws = workspace if workspace is not None else _workspace_for(X.device, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     fn = getattr(load_library(), cname)
-    _check(fn(f, _ptr(X), M, K, N, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(out), _ptr(ws), ws_bytes,
-              _stream(stream)), cname)
+    _check(fn(f, X.data_ptr(), M, K, N, Wq.data_ptr(), scales.data_ptr(), _ptr(zeros), out.data_ptr(), _ptr(ws),
+              ws_bytes, _stream(stream, X.device)), cname)
     return out
 
 
@@ -216,7 +225,7 @@ def gemv_w4a16_noalloc(fmt, X, Wq, scales, zeros=None, out=None, stream=None):
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     _check(load_library().wq_gemv_w4a16_noalloc(f, _ptr(X), M, K, N, _ptr(Wq), _ptr(scales), _ptr(zeros),
-                                                _ptr(out), _stream(stream)), "wq_gemv_w4a16_noalloc")
+                                                _ptr(out), _stream(stream, X.device)), "wq_gemv_w4a16_noalloc")
     return out
 
 
