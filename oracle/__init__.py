@@ -16,6 +16,9 @@ section):
 * ``mxfp4``     -- OCP MXFP4: E2M1 codes two per byte, one E8M0 power-of-two
   scale per 32 elements along K (大模型量化推理引擎全景大复盘, 里程碑六 / 方程 3).
 * ``linear``    -- Y = X · dequant(Wq)^T in float64.
+* ``swiglu``    -- the fused gate+up projection with SiLU(gate) * up
+  (推理优化与量化算子深度技术调研 §4.6), and the row interleave of the stacked
+  gate+up weight that the kernels read.
 
 Quantization arithmetic runs in float32 (the precision the pages' torch code
 works in) so that integer decisions -- codes, zero points, exponents -- are
@@ -26,4 +29,4 @@ Pins (tests/test_oracle_pins.py, tests/golden/): the pages' worked example and
 asserts, closed forms, brute force on tiny inputs, invariants and special
 cases.  Every function here is pinned; none is "parity unpinned".
 """
-from . import uniform, int4_g128, mxfp4, linear  # noqa: F401
+from . import uniform, int4_g128, mxfp4, linear, swiglu  # noqa: F401

@@ -14,7 +14,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
-from oracle import int4_g128, linear, mxfp4, uniform
+from oracle import int4_g128, linear, mxfp4, swiglu, uniform
 from bit_weight_quantized_wq_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -376,3 +376,92 @@ def test_linear_sanity_against_unquantized(outliers, bar):
         assert np.isfinite(Y).all()
         cos = float((Y * ref).sum() / math.sqrt((Y * Y).sum() * (ref * ref).sum()))
         assert cos > bar, (fmt, cos)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU on the fused gate+up projection (推理优化与量化算子深度技术调研 §4.6)
+# ---------------------------------------------------------------------------
+
+def test_silu_closed_forms():
+    # SiLU(x) = x sigmoid(x); sigmoid(1) = e / (1 + e), sigmoid(ln 3) = 3/4, sigmoid(0) = 1/2
+    assert swiglu.silu(0.0) == 0.0
+    assert abs(float(swiglu.silu(1.0)) - 0.7310585786300049) < 1e-15
+    assert abs(float(swiglu.silu(-1.0)) + 0.2689414213699951) < 1e-15
+    assert abs(float(swiglu.silu(math.log(3.0))) - 0.75 * math.log(3.0)) < 1e-15
+    assert abs(float(swiglu.silu(-math.log(3.0))) + 0.25 * math.log(3.0)) < 1e-15
+    # far tails: the identity above, zero below, no overflow
+    assert float(swiglu.silu(1000.0)) == 1000.0
+    assert abs(float(swiglu.silu(-1000.0))) < 1e-300
+    # sigmoid(x) + sigmoid(-x) = 1  =>  SiLU(x) - SiLU(-x) = x
+    x = np.linspace(-30, 30, 2001)
+    assert np.allclose(swiglu.silu(x) - swiglu.silu(-x), x, rtol=0, atol=1e-13)
+    # the global minimum: at x = -1 - W(1/e) = -1.27846454..., value -0.27846454...
+    xs = np.linspace(-1.3, -1.25, 50001)
+    v = swiglu.silu(xs)
+    assert abs(xs[np.argmin(v)] + 1.2784645427610738) < 2e-6
+    assert abs(v.min() + 0.2784645427610738) < 1e-10
+
+
+def _one_hot_stacked_int4(F, K=128):
+    """Hand-packed stacked [gate; up] INT4 weight, z = 8 everywhere: only the code at k = 0
+    differs from the zero point (code k = 0 sits in bits 0..3 of word 0)."""
+    Wq = np.full((2 * F, K // 8), 0x88888888, dtype=np.uint32)
+    sc = np.zeros((2 * F, K // 128), dtype=np.float16)
+    z = np.full((2 * F, K // 128), 8, dtype=np.float16)
+    g_exp, u_exp = [], []
+    for j in range(F):
+        qg, qu = 4 + j % 8, 15 - j % 8              # gate (q - 8) * 0.5, up (q - 8) * 0.25
+        Wq[j, 0] = 0x88888880 | qg
+        Wq[F + j, 0] = 0x88888880 | qu
+        sc[j, 0], sc[F + j, 0] = 0.5, 0.25
+        g_exp.append((qg - 8) * 0.5)
+        u_exp.append((qu - 8) * 0.25)
+    return Wq.view(np.int32), sc, z, g_exp, u_exp
+
+
+def test_swiglu_hand_packed_one_hot():
+    # X = e_0: gate_j and up_j are the dequantized k = 0 weights of rows j and F + j.
+    F, K = 16, 128
+    Wq, sc, z, g_exp, u_exp = _one_hot_stacked_int4(F, K)
+    X = np.zeros((1, K))
+    X[0, 0] = 1.0
+    Y = swiglu.swiglu_w4a16("int4_g128", X, Wq, sc, z)
+    assert Y.shape == (1, F)
+    for j in range(F):
+        g, u = g_exp[j], u_exp[j]
+        assert abs(Y[0, j] - g / (1.0 + math.exp(-g)) * u) < 1e-15, j
+    # j = 5: g = 0.5, u = 0.5; gate/up swapped or the sigmoid dropped would differ
+    assert abs(Y[0, 5] - 0.5 * 0.5 / (1.0 + math.exp(-0.5))) < 1e-15
+    # g = 0 (j = 4) zeroes the output whatever up is; u = 0 (j = 7) too
+    assert Y[0, 4] == 0.0 and Y[0, 7] == 0.0
+    # row sampling agrees with the full product
+    cols = np.array([3, 0, 15])
+    assert (swiglu.swiglu_rows("int4_g128", X, Wq, sc, z, F, cols) == Y[:, cols]).all()
+
+
+def test_interleave_order():
+    # F = 8: one block of 8 gate rows then 8 up rows -- already the stacked order
+    assert (swiglu.interleave_index(8) == np.arange(16)).all()
+    # F = 16, written out
+    assert swiglu.interleave_index(16).tolist() == (
+        list(range(0, 8)) + list(range(16, 24)) + list(range(8, 16)) + list(range(24, 32)))
+    for F in (8, 24, 128, 1000):
+        src = swiglu.interleave_index(F)
+        assert sorted(src.tolist()) == list(range(2 * F))          # a permutation
+        r = np.arange(2 * F)
+        gate = (r // 8) % 2 == 0
+        # gate row r and row r + 8 hold gate_j and up_j of the same output j = 8 (r // 16) + r % 8
+        assert (src[r[gate]] == 8 * (r[gate] // 16) + r[gate] % 8).all()
+        assert (src[r[gate] + 8] == src[r[gate]] + F).all()
+    with pytest.raises(ValueError):
+        swiglu.interleave_index(12)
+
+
+def test_interleave_commutes_with_rowwise_quantization():
+    F, K = 24, 256
+    W = inputs.weights(47, 2 * F, K, 0.03)
+    for q in (int4_g128.quantize, mxfp4.quantize):
+        a = [swiglu.interleave_gate_up(t, F) for t in q(W)]
+        b = q(swiglu.interleave_gate_up(W, F))
+        for x, y in zip(a, b):
+            assert (np.asarray(x).view(np.uint8) == np.asarray(y).view(np.uint8)).all()
