@@ -10,8 +10,9 @@ that every step streams 348 MB (> the 129 MB L2).  The step is replayed from a C
 and timed with CUDA events on its stream.
 
 Secondary measurements in the same run (same JSON line): prefill GEMM TFLOP/s on the
-Qwen2.5-72B shapes at M = 2048 and M = 8192, MXFP4 decode, the quantize kernels, and the
-GEMV/GEMM crossover on K = N = 8192.
+Qwen2.5-72B shapes at M = 2048 and M = 8192, MXFP4 decode, the fused gate+up projection with
+its SwiGLU epilogue (decode and prefill, beside the plain projection), the quantize kernels,
+and the GEMV/GEMM crossover on K = N = 8192.
 
 --impl reference times the CPU oracle (test infrastructure, float64) on a bounded sample
 of the same workload on the host cores.
@@ -453,6 +454,19 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                                  "frac": tf / bf16_peak,
                                  "traffic": profile_traffic("gemm_tc.cu", "gemm_tc_prefill") if Mp == PREFILL_M else None,
                                  "note": "fp16 operands (same dense rate as bf16); peak = measured cuBLAS bf16 burst"}}
+        if Mp == PREFILL_M:
+            # SwiGLU on the fused gate+up projection (K = 8192, 2F = 59136), beside the plain one
+            gi = PREFILL_SHAPES.index((8192, 59136))
+            ysw = torch.empty((Mp, 59136 // 2), dtype=torch.bfloat16, device=dev)
+            fsw = (lambda: binding.gemm_w4a16_swiglu("int4_g128", Xp[8192], pre[gi][0], pre[gi][1], pre[gi][2],
+                                                     out=ysw, workspace=wsp))
+            ms = _graph_time(fsw, stream, dev, max(3, reps // 5))
+            fl = 2.0 * Mp * 59136 * 8192
+            out["swiglu_prefill"] = {"workload": "Qwen2.5-72B fused gate+up (K=8192, 2F=59136) with SiLU(gate)*up "
+                                                 "in the epilogue, INT4 g128, M=%d" % Mp,
+                                     "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12,
+                                     "plain_gate_up_us": per_layer[gi]["us"]}
+            del ysw
         del Xp, Yp
         torch.cuda.empty_cache()
     del pre
@@ -497,6 +511,28 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
             gbs = decode_bytes(M, K, N) / (ms * 1e-3) / 1e9
             per.append({"K": K, "N": N, "M": M, "us": ms * 1e3, "GBps": gbs, "frac": gbs / hbm_peak})
     out["decode_layers"] = per
+
+    # SwiGLU epilogue on the fused gate+up projection (LLaMA-3-8B: K = 4096, 2F = 28672), the
+    # same packed weights read as the interleaved gate/up layout; beside the plain projection.
+    gi = DECODE_SHAPES.index((4096, 28672))
+    F = 28672 // 2
+    sw = []
+    for M in DECODE_M:
+        ys = torch.empty((M, F), dtype=torch.bfloat16, device=dev)
+        wss = binding.Workspace(dev).get(binding.gemm_workspace_bytes("int4_g128", M, 4096, 2 * F))
+
+        def fs(M=M, ys=ys, wss=wss):
+            for c in range(COPIES):
+                Wq, s, z = layers[gi][c]
+                binding.gemm_w4a16_swiglu("int4_g128", X[(M, 4096)], Wq, s, z, out=ys, workspace=wss)
+
+        ms = _graph_time(fs, stream, dev, reps) / COPIES
+        b = 0.53125 * 2 * F * 4096 + 2.0 * M * 4096 + 2.0 * M * F
+        plain = next(q["us"] for q in per if q["K"] == 4096 and q["N"] == 2 * F and q["M"] == M)
+        sw.append({"M": M, "us": ms * 1e3, "GBps": b / (ms * 1e-3) / 1e9, "frac": b / (ms * 1e-3) / 1e9 / hbm_peak,
+                   "plain_gate_up_us": plain})
+    out["swiglu_decode"] = {"workload": "LLaMA-3-8B fused gate+up (K=4096, 2F=28672) with SiLU(gate)*up "
+                                        "in the epilogue, INT4 g128, Y [M, 14336]", "points": sw}
 
     # quantize kernels on the decode shapes: fp32 read + packed write
     qres = {}
@@ -562,6 +598,8 @@ def run_ncu_case(args):
              3 weight copies; one step = 12 launches, run warmup + steps times without a graph.
     prefill: the (K, N) = (8192, 8192) layer at M = 2048, INT4 (37 MB weights, 32 MB X).
     mxfp4:   the decode layer in MXFP4.
+    swiglu_decode: the decode layer read as the fused gate+up weight (2F = 28672) with the
+             SwiGLU epilogue, M = 1, INT4.
     quant:   INT4 quantize of the (4096, 28672) weights (470 MB fp32).
     """
     import numpy as np
@@ -594,8 +632,8 @@ def run_ncu_case(args):
         torch.cuda.synchronize()
         print(json.dumps({"ncu_case": case, "launches": n, "launches_per_step": len(DECODE_M) * len(DECODE_SHAPES)}))
         return 0
-    if case in ("decode", "mxfp4"):
-        K, N, M, fmt = 4096, 28672, 1, ("int4_g128" if case == "decode" else "mxfp4")
+    if case in ("decode", "mxfp4", "swiglu_decode"):
+        K, N, M, fmt = 4096, 28672, 1, ("mxfp4" if case == "mxfp4" else "int4_g128")
     elif case == "prefill":
         K, N, M, fmt = 8192, 8192, 2048, "int4_g128"
     else:
@@ -611,12 +649,14 @@ def run_ncu_case(args):
     del W
     copies = [pk] + [tuple(t.clone() for t in pk) for _ in range(COPIES - 1)]
     X = torch.from_numpy(inputs.activations(7, M, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
-    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    sw = case == "swiglu_decode"
+    Y = torch.empty((M, N // 2 if sw else N), dtype=torch.bfloat16, device=dev)
     ws = binding.Workspace(dev).get(binding.gemm_workspace_bytes(fmt, M, K, N))
+    fn = binding.gemm_w4a16_swiglu if sw else binding.gemm_w4a16
     n = 0
     for i in range(args.warmup + args.steps):
         c = copies[i % COPIES]
-        binding.gemm_w4a16(fmt, X, c[0], c[1], c[2] if fmt == "int4_g128" else None, out=Y, workspace=ws)
+        fn(fmt, X, c[0], c[1], c[2] if fmt == "int4_g128" else None, out=Y, workspace=ws)
         n += 1
     torch.cuda.synchronize()
     print(json.dumps({"ncu_case": case, "launches": n, "K": K, "N": N, "M": M, "fmt": fmt}))
@@ -632,7 +672,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-sample", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "quant"],
+    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "swiglu_decode", "quant"],
                     help="run a few plain launches of one kernel (for ncu captures) instead of the bench")
     args = ap.parse_args()
     if args.cpu_sample is not None:

@@ -30,6 +30,7 @@ EXPORTED = [
     "wq_quantize_int4_g128", "wq_quantize_mxfp4", "wq_gemm_workspace_bytes", "wq_gemm_w4a16",
     "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
     "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
+    "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
 ]
 
 _lib = None
@@ -58,6 +59,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_read_error_flags": (I32, [ctypes.POINTER(U32)]),
         "wq_check_device": (I32, []),
         "wq_gemv_w4a16_noalloc": (I32, [I32, P, I64, I64, I64, P, P, P, P, P]),
+        "wq_gemm_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_gemv_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_gemm_tc_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
+        "wq_interleave_gate_up": (I32, [P, P, I64, I64, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -172,7 +177,7 @@ def _workspace_for(device, nbytes, workspace):
     return ws.get(nbytes)
 
 
-def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream):
+def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
     f = _fmt(fmt)
     _need(X, torch.bfloat16, "X")
     _need(Wq, torch.int32, "Wq")
@@ -188,14 +193,14 @@ def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream):
     if Wq.shape[1] * 8 != K:
         raise ValueError("Wq must be [N, K/8]")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+        out = torch.empty((M, N // 2 if swiglu else N), dtype=torch.bfloat16, device=X.device)
     else:
         _need(out, torch.bfloat16, "out")
     # a caller's workspace is checked by the library itself (WQ_ERR_WORKSPACE when too small)
     ws = workspace if workspace is not None else _workspace_for(X.device, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     fn = getattr(load_library(), cname)
-    _check(fn(f, X.data_ptr(), M, K, N, Wq.data_ptr(), scales.data_ptr(), _ptr(zeros), out.data_ptr(), _ptr(ws),
+    _check(fn(f, X.data_ptr(), M, K, N // 2 if swiglu else N, Wq.data_ptr(), scales.data_ptr(), _ptr(zeros), out.data_ptr(), _ptr(ws),
               ws_bytes, _stream(stream, X.device)), cname)
     return out
 
@@ -213,6 +218,40 @@ def gemv_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=
 def gemm_tc_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
     """The tcgen05 tensor-core kernel alone (any M)."""
     return _linear("wq_gemm_tc_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
+
+
+def gemm_w4a16_swiglu(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """Y = SiLU(X Wg^T) * (X Wu^T), bf16 [M, F], for the fused gate+up weight of 2F rows in the
+    interleaved row order of ``interleave_gate_up``; dispatches like ``gemm_w4a16``."""
+    return _linear("wq_gemm_w4a16_swiglu", fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=True)
+
+
+def gemv_w4a16_swiglu(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """The decode kernel alone with the SwiGLU epilogue (M <= 16)."""
+    return _linear("wq_gemv_w4a16_swiglu", fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=True)
+
+
+def gemm_tc_w4a16_swiglu(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
+    """The tensor-core kernel alone with the SwiGLU epilogue (any M)."""
+    return _linear("wq_gemm_tc_w4a16_swiglu", fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=True)
+
+
+def interleave_gate_up(src: torch.Tensor, out=None, stream=None):
+    """Rows of the stacked [gate; up] tensor ``src`` (2F rows, any dtype, contiguous) in the
+    order the SwiGLU entry points read: blocks of 8 gate rows and the matching 8 up rows."""
+    if not src.is_cuda or not src.is_contiguous() or src.dim() < 1:
+        raise ValueError("src must be a contiguous CUDA tensor")
+    F = src.shape[0] // 2
+    if src.shape[0] != 2 * F:
+        raise ValueError("src needs an even number of rows")
+    if out is None:
+        out = torch.empty_like(src)
+    elif out.shape != src.shape or out.dtype != src.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of src's shape and dtype")
+    row_bytes = (src.numel() // max(src.shape[0], 1)) * src.element_size()
+    _check(load_library().wq_interleave_gate_up(_ptr(src), _ptr(out), F, row_bytes, _stream(stream, src.device)),
+           "wq_interleave_gate_up")
+    return out
 
 
 def gemv_w4a16_noalloc(fmt, X, Wq, scales, zeros=None, out=None, stream=None):

@@ -213,6 +213,62 @@ wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
   return wq_gemm_tc_w4a16(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
 }
 
+wq_status wq_gemv_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F, const int32_t* Wq,
+                               const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  if (F < 8 || F % 8 != 0 || F > (1LL << 29)) return WQ_ERR_SHAPE;
+  const int64_t N = 2 * F;
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  if (M > 16) return WQ_ERR_SHAPE;
+  if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
+  const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes,
+                                   static_cast<cudaStream_t>(stream), wq::kEpiSwiglu));
+}
+
+wq_status wq_gemm_tc_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
+                                  const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Y,
+                                  void* workspace, size_t ws_bytes, void* stream) {
+  if (F < 8 || F % 8 != 0 || F > (1LL << 29)) return WQ_ERR_SHAPE;
+  const int64_t N = 2 * F;
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  const size_t need = wq::gemm_tc_workspace_bytes(fmt, M, K, N);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gemm_tc(fmt, X, M, K, N, Wq, scales, zeros, Y, workspace, ws_bytes,
+                                      static_cast<cudaStream_t>(stream), wq::kEpiSwiglu));
+}
+
+wq_status wq_gemm_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F, const int32_t* Wq,
+                               const void* scales, const uint16_t* zeros, uint16_t* Y, void* workspace,
+                               size_t ws_bytes, void* stream) {
+  if (F < 8 || F % 8 != 0 || F > (1LL << 29)) return WQ_ERR_SHAPE;
+  wq_status st = check_linear_args(fmt, X, M, K, 2 * F, Wq, scales, zeros, Y);
+  if (st != WQ_OK) return st;
+  if (M <= wq_dispatch_threshold(fmt, K, 2 * F))
+    return wq_gemv_w4a16_swiglu(fmt, X, M, K, F, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
+  return wq_gemm_tc_w4a16_swiglu(fmt, X, M, K, F, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
+}
+
+wq_status wq_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, void* stream) {
+  if (!src || !dst) return WQ_ERR_NULL;
+  if (F < 8 || F % 8 != 0 || row_bytes < 1 || F > (1LL << 30) || row_bytes > (1LL << 40) / F) return WQ_ERR_SHAPE;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  const uintptr_t bytes = static_cast<uintptr_t>(2 * F) * static_cast<uintptr_t>(row_bytes);
+  if (s0 < d0 + bytes && d0 < s0 + bytes) return WQ_ERR_ARG;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_interleave_gate_up(src, dst, F, row_bytes, static_cast<cudaStream_t>(stream)));
+}
+
 const char* wq_status_str(wq_status s) {
   switch (s) {
     case WQ_OK: return "WQ_OK";

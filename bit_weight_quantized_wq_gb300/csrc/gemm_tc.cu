@@ -184,7 +184,7 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_n, int tiles_m, int
   tn = r / gsize;
 }
 
-template <int FMT>
+template <int FMT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
               const Params p) {
@@ -349,7 +349,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
-        if (row_ok) {
+        if constexpr (EPI == kEpiSwiglu) {
+          // Gate row n (lane bit 3 clear) and its up row n + 8 sit in lanes l and l ^ 8 of
+          // this warp: the gate lane takes the up value by a shuffle and writes SiLU(g) * u.
+          const bool gate = (lane & 8) == 0;
+          const unsigned am = __activemask();   // the whole warp, unless a wait above timed out
+          const int F = p.N >> 1;
+          const long long col = swiglu_col(n);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m0 + c + j;
+            float y = __uint_as_float(v[j]);
+            if constexpr (FMT == kInt4G128) y *= __ldg(p.xscale + (m < p.M ? m : 0));
+            const float u = __shfl_xor_sync(am, y, 8);
+            if (gate && row_ok && m < p.M)
+              p.Y[static_cast<long long>(m) * F + col] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(y) * u));
+          }
+        } else if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int m = m0 + c + j;
@@ -423,8 +439,9 @@ size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int epi) {
   using namespace tc;
+  if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
   if (ws_bytes < gemm_tc_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   Params p{};
   p.scales = scales;
@@ -461,21 +478,19 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem) + 1024;
   const unsigned grid = static_cast<unsigned>(p.tiles_n) * static_cast<unsigned>(p.tiles_m);
-  static bool attr_set[2][64] = {{false}};  // once per (format, device)
+  void (*kern)(CUtensorMap, CUtensorMap, Params) =
+      fmt == kInt4G128 ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu> : k_gemm_tc<kInt4G128, kEpiNone>)
+                       : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu> : k_gemm_tc<kMxfp4, kEpiNone>);
+  static bool attr_set[4][64] = {{false}};  // once per (kernel, device)
   int dev = 0;
   cudaGetDevice(&dev);
-  const int fi = fmt == kInt4G128 ? 0 : 1;
+  const int fi = (fmt == kInt4G128 ? 0 : 1) + (epi == kEpiSwiglu ? 2 : 0);
   if (dev < 0 || dev >= 64 || !attr_set[fi][dev]) {
-    e = fmt == kInt4G128
-            ? cudaFuncSetAttribute(k_gemm_tc<kInt4G128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))
-            : cudaFuncSetAttribute(k_gemm_tc<kMxfp4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[fi][dev] = true;
   }
-  if (fmt == kInt4G128)
-    k_gemm_tc<kInt4G128><<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  else
-    k_gemm_tc<kMxfp4><<<grid, kThreads, smem, stream>>>(tx, tw, p);
+  kern<<<grid, kThreads, smem, stream>>>(tx, tw, p);
   return cudaGetLastError();
 }
 

@@ -222,7 +222,48 @@ __device__ BandContrib band_contributors(const Params& p, int band) {
 // contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
 // of the M x kBand outputs; bf16 results to Y.
 template <int MT>
+__device__ __forceinline__ float4 sum_contributors(const float* base, BandContrib bc) {
+  const long long cstride = 2LL * MT * kBand;
+  float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(bc.c_lo) * 2 + bc.lo_side) * MT * kBand);
+  for (int c = bc.c_lo + 1; c <= bc.c_hi; c += 4) {
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      v[q] = (c + q <= bc.c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c + q <= bc.c_hi) {
+        acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
+      }
+  }
+  return acc4;
+}
+
+template <int MT, int EPI>
 __device__ __forceinline__ void reduce_band_share(const Params& p, int band, BandContrib bc, int first, int step) {
+  if constexpr (EPI == kEpiSwiglu) {
+    // Gate rows 16q .. 16q + 7 of the band pair with up rows 16q + 8 .. 16q + 15: one item
+    // is a float4 of gate rows and the float4 of up rows 8 below it.
+    const int F = p.N >> 1;
+    for (int idx = first; idx < p.M * (kBand / 8); idx += step) {
+      const int m = idx / (kBand / 8);
+      const int k = idx % (kBand / 8);
+      const int r4 = 16 * (k >> 1) + 4 * (k & 1);
+      const float* base = p.part + static_cast<long long>(m) * kBand + r4;
+      const float4 g4 = sum_contributors<MT>(base, bc);
+      const float4 u4 = sum_contributors<MT>(base + 8, bc);
+      const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int n = band * kBand + r4 + q;
+        if (n < p.N)
+          p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(gv[q]) * uv[q]));
+      }
+    }
+    return;
+  }
   const long long cstride = 2LL * MT * kBand;   // floats between two CTAs' partial slots
   for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
     const int m = idx / (kBand / 4);
@@ -274,7 +315,7 @@ struct Cursor {
   }
 };
 
-template <int FMT, int MT>
+template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
            const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
@@ -749,15 +790,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
                           (st.seg_end == static_cast<long long>(band + 1) * p.GP);
         if (full) {
+          if constexpr (EPI == kEpiSwiglu) {
+            // r1 = r0 + 8: this lane holds gate (e = 0, 1) and up (e = 2, 3) of one output
+            const int n = band * kBand + r0;
+            const int F = p.N >> 1;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int m = 2 * t + (e & 1) + 8 * nt;
-              const int n = band * kBand + ((e >> 1) ? r1 : r0);
-              if (m < p.M && n < p.N)
-                p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
-            }
+              for (int e = 0; e < 2; ++e) {
+                const int m = 2 * t + e + 8 * nt;
+                if (m < p.M && n < p.N)
+                  p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
+                      __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(acc[nt][e]) * acc[nt][e + 2]));
+              }
+          } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int m = 2 * t + (e & 1) + 8 * nt;
+                const int n = band * kBand + ((e >> 1) ? r1 : r0);
+                if (m < p.M && n < p.N)
+                  p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
+              }
+          }
         } else {
           // partial sums; the prep warp owning this activation slot publishes them
           const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
@@ -786,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b1 = ld_acquire_cta(&sm.req_band[k]);
         if (b1 == 0) break;
         const BandContrib bc = sm.ci[sm.ci_band[0] == b1 - 1 ? 0 : 1];
-        reduce_band_share<MT>(p, b1 - 1, bc, cw * 32 + lane, 32 * kConsumerWarps);
+        reduce_band_share<MT, EPI>(p, b1 - 1, bc, cw * 32 + lane, 32 * kConsumerWarps);
       }
     }
   }
@@ -809,7 +865,7 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   return kWsCounterBytes + static_cast<size_t>(P) * 2 * MT * gemv::kBand * sizeof(float);
 }
 
-template <int FMT, int MT>
+template <int FMT, int MT, int EPI>
 static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
                                  const gemv::Params& p, cudaStream_t stream) {
   // activations: MT rows x 256 k per stage; rows >= M and columns >= K come back as zeros
@@ -821,7 +877,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   using S = gemv::Smem<FMT, MT>;
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(S) + 1024;
-  auto kern = gemv::k_gemv<FMT, MT>;
+  auto kern = gemv::k_gemv<FMT, MT, EPI>;
   static bool attr_set[64] = {false};  // once per device
   int dev = 0;
   cudaGetDevice(&dev);
@@ -848,7 +904,8 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
 
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                             const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int epi) {
+  if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
   gemv::Params p{};
   p.X = X;
   p.scales = scales;
@@ -900,9 +957,18 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
     }
   }
   const bool small = M <= 8;
+  if (epi == kEpiSwiglu) {
+    if (fmt == kInt4G128)
+      return small ? launch_gemv_t<kInt4G128, 8, kEpiSwiglu>(tw, ts, tz, p, stream)
+                   : launch_gemv_t<kInt4G128, 16, kEpiSwiglu>(tw, ts, tz, p, stream);
+    return small ? launch_gemv_t<kMxfp4, 8, kEpiSwiglu>(tw, ts, tz, p, stream)
+                 : launch_gemv_t<kMxfp4, 16, kEpiSwiglu>(tw, ts, tz, p, stream);
+  }
   if (fmt == kInt4G128)
-    return small ? launch_gemv_t<kInt4G128, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kInt4G128, 16>(tw, ts, tz, p, stream);
-  return small ? launch_gemv_t<kMxfp4, 8>(tw, ts, tz, p, stream) : launch_gemv_t<kMxfp4, 16>(tw, ts, tz, p, stream);
+    return small ? launch_gemv_t<kInt4G128, 8, kEpiNone>(tw, ts, tz, p, stream)
+                 : launch_gemv_t<kInt4G128, 16, kEpiNone>(tw, ts, tz, p, stream);
+  return small ? launch_gemv_t<kMxfp4, 8, kEpiNone>(tw, ts, tz, p, stream)
+               : launch_gemv_t<kMxfp4, 16, kEpiNone>(tw, ts, tz, p, stream);
 }
 
 // The decode entry points run the mma.sync kernel above.  (A tcgen05 variant was measured
@@ -912,8 +978,8 @@ size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return g
 
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                         const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
-  return launch_gemv_mma(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream);
+                        cudaStream_t stream, int epi) {
+  return launch_gemv_mma(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream, epi);
 }
 
 // ---------------------------------------------------------------------------------------

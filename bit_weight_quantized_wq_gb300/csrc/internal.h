@@ -13,6 +13,12 @@ namespace wq {
 // Format codes (same values as wq_fmt in include/wq.h).
 enum Fmt : int { kInt4G128 = 0, kMxfp4 = 1 };
 
+// Epilogue of the linear layer.  kEpiSwiglu: the weight is the fused gate+up projection of
+// 2F rows with gate and up rows interleaved in blocks of 8 (row 16q + i is gate row 8q + i,
+// row 16q + 8 + i the matching up row), and the kernel writes Y[M, F] = SiLU(gate) * up,
+// applied to the fp32 accumulators before the one bf16 rounding.
+enum Epi : int { kEpiNone = 0, kEpiSwiglu = 1 };
+
 // Encodes a 2-D tiled TMA descriptor through the driver entry point (no libcuda link).
 // dims/strides in elements/bytes, innermost first.
 cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
@@ -39,7 +45,7 @@ cudaError_t launch_quant_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq
 size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                         const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int epi = kEpiNone);
 uint32_t gemv_read_and_clear_error();
 size_t gemv_noalloc_scratch_bytes();
 cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -50,7 +56,10 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int epi = kEpiNone);
 uint32_t gemm_tc_read_and_clear_error();
+
+// layout.cu -- row re-layout of the stacked gate+up weight
+cudaError_t launch_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, cudaStream_t stream);
 
 }  // namespace wq

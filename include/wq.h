@@ -157,6 +157,54 @@ wq_status wq_gemm_tc_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, 
                            uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The fused gate+up projection of a SwiGLU FFN with its activation in the epilogue:
+ *   Y[M, F] = SiLU(X * dequant(W_gate)^T) * (X * dequant(W_up)^T),   SiLU(g) = g / (1 + e^-g).
+ * Defined by: 推理优化与量化算子深度技术调研 §4.6 (GEMM + activation fusion: W_gate and W_up
+ * stacked into one GEMM, SiLU(gate) * up computed in registers, the intermediate never written
+ * to memory).  The activation is applied to the fp32 accumulators; Y is rounded to bf16 once.
+ * No bias (the SwiGLU projections of LLaMA-style models have none).
+ *   X       [M, K] bf16 bits.
+ *   F       output features (the FFN's intermediate size); F >= 8, F % 8 == 0.
+ *   Wq, scales, zeros
+ *           the packed weight of the stacked [W_gate; W_up] (2F rows, format fmt, same
+ *           per-row layouts as wq_gemm_w4a16 with N = 2F), with its rows in the INTERLEAVED
+ *           order of wq_interleave_gate_up (apply it to each of the three arrays).
+ *   Y       [M, F] bf16 bits output.
+ *   workspace / ws_bytes: at least wq_gemm_workspace_bytes(fmt, M, K, 2F) bytes.
+ * Dispatch, errors and workspace rules as wq_gemm_w4a16 with N = 2F (threshold
+ * T(fmt, K, 2F)); WQ_ERR_SHAPE also when F % 8 != 0.
+ */
+wq_status wq_gemm_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
+                               const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                               uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/* The decode kernel alone with the SwiGLU epilogue (M <= 16, 2F <= 2097152). */
+wq_status wq_gemv_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
+                               const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                               uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/* The tensor-core kernel alone with the SwiGLU epilogue (any M >= 1). */
+wq_status wq_gemm_tc_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
+                                  const int32_t* Wq, const void* scales, const uint16_t* zeros,
+                                  uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Row re-layout of a stacked [gate; up] array (2F rows of row_bytes bytes each: the packed
+ * codes, the scales or the zeros of the fused gate+up weight) into the order the SwiGLU
+ * entry points read: gate and up rows alternate in blocks of 8,
+ *   dst row 16q + 8h + i = src row h*F + 8q + i     (h = 0: gate, h = 1: up; i < 8).
+ * A one-time offline transform, as the weight re-layout after loading of
+ * 第 6 课：量化源码走读 §2.  Row-wise quantization commutes with it, so it may equally be
+ * applied to the float weight before wq_quantize_*.
+ *   src, dst  device pointers to 2F * row_bytes bytes; distinct, non-overlapping buffers.
+ *             Here (only) any alignment is accepted; 16-byte aligned bases and
+ *             row_bytes % 16 == 0 copy 16 bytes at a time.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless F >= 8, F % 8 == 0, row_bytes >= 1; WQ_ERR_ARG if
+ *         the buffers overlap; WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+wq_status wq_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, void* stream);
+
+/*
  * Dispatch threshold T(fmt, K, N): wq_gemm_w4a16 uses the decode kernel when M <= T.
  * wq_set_dispatch_threshold overrides it for one (fmt, K, N) (T in [0, 16]; K = N = 0 sets
  * the default for the format).  Returns WQ_ERR_ARG / WQ_ERR_SHAPE on bad input.  Host-side

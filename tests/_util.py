@@ -18,10 +18,13 @@ def y_to_host(Y):
     return Y.float().cpu().numpy().astype(np.float64)
 
 
-def assert_close(y, ref, what=""):
+def assert_close(y, ref, what="", extra=None):
+    """|y - ref| <= TOL (1 + |ref|) (+ ``extra``, an elementwise allowance derived by the caller)."""
     y = np.asarray(y, np.float64)
     err = np.abs(y - ref)
     lim = TOL * (1 + np.abs(ref))
+    if extra is not None:
+        lim = lim + extra
     bad = ~(err <= lim)
     if bad.any():
         i = np.unravel_index(np.argmax(np.where(bad, err / lim, 0)), err.shape)

@@ -1,0 +1,216 @@
+"""Fused gate+up projection with the SwiGLU epilogue (推理优化与量化算子深度技术调研 §4.6)
+against the float64 oracle, and the gate/up row interleave against the oracle's permutation.
+
+Tolerance, derived from each path's arithmetic:
+* Exact operands (the decode kernel in both formats; the tensor-core kernel on MXFP4, whose
+  dequantized weights are exact in bf16): g and u are fp32 sums of exact products, off the
+  float64 values by ~1e-6 of the sum of |x w|; the one bf16 rounding of SiLU(g) * u
+  (2^-9 relative) dominates.  Bound: the linear layer's |y - ref| <= 1e-2 (1 + |ref|).
+* The tensor-core kernel on INT4 multiplies fp16-rounded dequantized weights (the 16-bit
+  operand of the method): each w_hat carries a relative error of at most 2^-11, uniform,
+  so g is off by a sum of K independent terms with standard deviation at most
+  sigma_g = 2^-11 / sqrt(3) * sqrt(sum_k (x_k w_hat_k)^2).  The linear layer absorbs that in
+  1e-2 (1 + |g|), but SiLU(g) * u multiplies it by |SiLU'(g) u|, which exceeds 10 where
+  g ~ 0 and |u| is large.  Bound: 1e-2 (1 + |ref|) + |SiLU'(g) u| 6 sigma_g + |SiLU(g)| 6 sigma_u.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from bit_weight_quantized_wq_gb300 import inputs
+from oracle import int4_g128, linear, mxfp4, swiglu
+from tests._util import assert_close, to_dev, x_to_dev, y_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import torch
+    from bit_weight_quantized_wq_gb300 import binding
+    binding.check_device()
+    torch.cuda.init()
+    return binding
+
+
+def _pack(fmt, W):
+    return int4_g128.quantize(W) if fmt == "int4_g128" else mxfp4.quantize(W)
+
+
+def _stacked(fmt, F, K, seed, sigma=0.05):
+    """Packed stacked [W_gate; W_up] (2F rows) from the oracle's quantizer."""
+    return _pack(fmt, inputs.weights(seed, 2 * F, K, sigma))
+
+
+def _run(fn, fmt, xbits, pk_stacked, F, gpu_interleave=None):
+    """Interleaves the stacked packed arrays (on the CPU with the oracle's permutation, or with
+    the library's kernel when gpu_interleave is the binding) and runs ``fn``."""
+    if gpu_interleave is None:
+        d = [to_dev(swiglu.interleave_gate_up(a, F)) for a in pk_stacked]
+    else:
+        d = [gpu_interleave.interleave_gate_up(to_dev(a)) for a in pk_stacked]
+    X = x_to_dev(xbits)
+    if fmt == "int4_g128":
+        return fn(fmt, X, d[0], d[1], d[2])
+    return fn(fmt, X, d[0], d[1])
+
+
+def _ref(fmt, xf, pk):
+    return swiglu.swiglu_w4a16(fmt, xf, pk[0], pk[1], pk[2] if fmt == "int4_g128" else None)
+
+
+def _fp16_operand_allowance(xf, pk, F, cols=None):
+    """The propagated 6-sigma bound of fp16-rounded INT4 weights (module docstring), for the
+    output columns ``cols`` (all when None), from the float64 dequantized weights."""
+    cols = np.arange(F) if cols is None else np.asarray(cols)
+    x = np.asarray(xf, np.float64)
+    W = [linear.dequantize("int4_g128", pk[0][r], pk[1][r], pk[2][r]) for r in (cols, cols + F)]
+    g, u = x @ W[0].T, x @ W[1].T
+    sig = [2.0 ** -11 / math.sqrt(3.0) * np.sqrt((x * x) @ (w * w).T) for w in W]
+    sg = 0.5 * (1.0 + np.tanh(0.5 * g))                  # sigmoid(g)
+    dsilu = sg * (1.0 + g * (1.0 - sg))
+    return 6.0 * (np.abs(dsilu * u) * sig[0] + np.abs(g * sg) * sig[1])
+
+
+# ------------------------------------------------------------------ the interleave, bit-exact
+
+@pytest.mark.parametrize("F", [8, 24, 1000, 4104])
+@pytest.mark.parametrize("kind", ["codes", "int4_meta", "mxfp4_scales_odd"])
+def test_interleave_bit_exact(B, F, kind):
+    rng = np.random.default_rng(F + len(kind))
+    if kind == "codes":          # [2F, K/8] int32, 16-byte rows
+        a = rng.integers(-2 ** 31, 2 ** 31, size=(2 * F, 64), dtype=np.int64).astype(np.int32)
+    elif kind == "int4_meta":    # [2F, 3] fp16 bits: 6-byte rows, the byte path
+        a = rng.integers(0, 2 ** 16, size=(2 * F, 3), dtype=np.int64).astype(np.uint16).view(np.float16)
+    else:                        # [2F, 3] E8M0 bytes (K = 96)
+        a = rng.integers(0, 256, size=(2 * F, 3), dtype=np.int64).astype(np.uint8)
+    got = B.interleave_gate_up(to_dev(a)).cpu().numpy()
+    assert (got.view(np.uint8) == swiglu.interleave_gate_up(a, F).view(np.uint8)).all()
+
+
+def test_interleave_rejects_bad_arguments(B):
+    import torch
+    a = torch.zeros((24, 16), dtype=torch.uint8, device="cuda")   # F = 12: not a multiple of 8
+    with pytest.raises(ValueError):
+        B.interleave_gate_up(a)
+    b = torch.zeros((32, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):
+        B.interleave_gate_up(b, out=b)                            # in place: buffers overlap
+
+
+# ------------------------------------------------------------------ decode kernel
+
+# (F, K): one 256-row band split over many CTAs (F = 128, K = 4096), whole bands per CTA
+# (F = 2048, K = 256), a ragged last band (F = 1000), the smallest F, and a K tail group.
+DECODE_CASES = [(8, 128), (128, 4096), (2048, 256), (1000, 1152), (520, 512), (1408, 2048)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("F,K", DECODE_CASES)
+def test_swiglu_decode(B, fmt, M, F, K):
+    pk = _stacked(fmt, F, K, F * 3 + K)
+    xb, xf = inputs.activations(M + F, M, K)
+    Y = _run(B.gemv_w4a16_swiglu, fmt, xb, pk, F)
+    assert Y.shape == (M, F)
+    assert_close(y_to_host(Y), _ref(fmt, xf, pk), "%s M=%d F=%d K=%d" % (fmt, M, F, K))
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_swiglu_decode_gpu_interleave_and_large_gate(B, fmt):
+    # Larger weights: gate values of several units, both tails of SiLU exercised.
+    F, K, M = 512, 1024, 4
+    pk = _stacked(fmt, F, K, 77, sigma=0.3)
+    xb, xf = inputs.activations(78, M, K)
+    Y = _run(B.gemv_w4a16_swiglu, fmt, xb, pk, F, gpu_interleave=B)
+    ref = _ref(fmt, xf, pk)
+    assert np.abs(ref).max() > 10.0
+    assert_close(y_to_host(Y), ref, fmt)
+    assert B.read_error_flags() == 0
+
+
+# ------------------------------------------------------------------ tensor-core kernel
+
+TC_CASES = [(8, 128), (200, 256), (1000, 1152), (1024, 4096)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 17, 300])
+@pytest.mark.parametrize("F,K", TC_CASES)
+def test_swiglu_tc(B, fmt, M, F, K):
+    pk = _stacked(fmt, F, K, F * 5 + K + 1)
+    xb, xf = inputs.activations(M * 3 + F, M, K)
+    Y = _run(B.gemm_tc_w4a16_swiglu, fmt, xb, pk, F)
+    assert Y.shape == (M, F)
+    extra = _fp16_operand_allowance(xf, pk, F) if fmt == "int4_g128" else None
+    assert_close(y_to_host(Y), _ref(fmt, xf, pk), "%s M=%d F=%d K=%d" % (fmt, M, F, K), extra)
+
+
+@pytest.mark.parametrize("M", [5, 40])
+def test_swiglu_dispatch(B, M):
+    F, K = 256, 512
+    for fmt in ("int4_g128", "mxfp4"):
+        pk = _stacked(fmt, F, K, 9 + M)
+        xb, xf = inputs.activations(10 + M, M, K)
+        Y = _run(B.gemm_w4a16_swiglu, fmt, xb, pk, F)
+        extra = _fp16_operand_allowance(xf, pk, F) if fmt == "int4_g128" and M > 16 else None
+        assert_close(y_to_host(Y), _ref(fmt, xf, pk), "%s M=%d" % (fmt, M), extra)
+
+
+def test_swiglu_rejects_bad_shapes(B):
+    import torch
+    F, K = 12, 128                      # F % 8 != 0
+    pk = [to_dev(a) for a in _stacked("int4_g128", F, K, 1)]
+    X = torch.zeros((1, K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        B.gemm_w4a16_swiglu("int4_g128", X, *pk)
+    pk = [to_dev(a) for a in _stacked("int4_g128", 16, K, 2)]
+    X = torch.zeros((17, K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):     # the decode kernel takes M <= 16
+        B.gemv_w4a16_swiglu("int4_g128", X, *pk)
+
+
+# ------------------------------------------------------------------ full-size, sampled columns
+
+def test_swiglu_full_size_decode_llama3_8b(B):
+    # LLaMA-3-8B gate+up: K = 4096, F = 14336 (2F = 28672 weight rows), M in {1, 4, 16}.
+    # INT4 only at this size: the oracle's MXFP4 quantizer needs minutes for 117 M weights
+    # (MXFP4 runs the same kernel code paths in the smaller cases above).
+    F, K = 14336, 4096
+    for fmt in ("int4_g128",):
+        pk = _stacked(fmt, F, K, 5001, sigma=0.02)
+        cols = np.sort(np.random.default_rng(5002).choice(F, 256, replace=False))
+        d = [B.interleave_gate_up(to_dev(a)) for a in pk]
+        for M in (1, 4, 16):
+            xb, xf = inputs.activations(5003 + M, M, K)
+            X = x_to_dev(xb)
+            Y = B.gemm_w4a16_swiglu(fmt, X, *d) if fmt == "int4_g128" else B.gemm_w4a16_swiglu(fmt, X, d[0], d[1])
+            ref = swiglu.swiglu_rows(fmt, xf, pk[0], pk[1], pk[2] if fmt == "int4_g128" else None, F, cols)
+            assert_close(y_to_host(Y)[:, cols], ref, "%s M=%d" % (fmt, M))
+    assert B.read_error_flags() == 0
+
+
+def test_swiglu_full_size_prefill_qwen25_72b(B):
+    # Qwen2.5-72B gate+up: K = 8192, F = 29568 (2F = 59136 weight rows), M = 2048.
+    F, K, M = 29568, 8192, 2048
+    pk = _stacked("int4_g128", F, K, 6001, sigma=0.015)
+    cols = np.sort(np.random.default_rng(6002).choice(F, 128, replace=False))
+    d = [B.interleave_gate_up(to_dev(a)) for a in pk]
+    xb, xf = inputs.activations(6003, M, K)
+    Y = B.gemm_w4a16_swiglu("int4_g128", x_to_dev(xb), *d)
+    ref = swiglu.swiglu_rows("int4_g128", xf, pk[0], pk[1], pk[2], F, cols)
+    assert_close(y_to_host(Y)[:, cols], ref, "int4 M=2048", _fp16_operand_allowance(xf, pk, F, cols))
+    assert B.read_error_flags() == 0
+
+
+def test_swiglu_paths_agree_where_operands_are_exact(B):
+    # The K = 4096 case that needs the fp16-operand allowance on the INT4 tensor-core path
+    # passes the plain bound on the decode kernel (exact products) at M <= 16.
+    F, K, M = 1024, 4096, 16
+    pk = _stacked("int4_g128", F, K, F * 5 + K + 1)
+    xb, xf = inputs.activations(M * 3 + F, M, K)
+    ref = _ref("int4_g128", xf, pk)
+    assert_close(y_to_host(_run(B.gemv_w4a16_swiglu, "int4_g128", xb, pk, F)), ref, "decode")
+    y_tc = y_to_host(_run(B.gemm_tc_w4a16_swiglu, "int4_g128", xb, pk, F))
+    assert_close(y_tc, ref, "tc", _fp16_operand_allowance(xf, pk, F))
