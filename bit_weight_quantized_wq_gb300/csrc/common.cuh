@@ -159,9 +159,10 @@ __device__ __forceinline__ bool elect_one() {
 // Loads through L2 only (data written by other CTAs of the same kernel).
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
-// SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), fp32, e^-g from the CUDA intrinsic.  For
-// g << 0 the exponential overflows to +inf and the quotient is -0, the function's limit.
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.f + __expf(-g)); }
+// SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), fp32, with the CUDA fast exponential and fast
+// divide intrinsics (a few ulp: far inside the bf16 rounding of the result).  For g << 0 the
+// denominator is huge or +inf and the quotient is 0, the function's limit.
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
 // Output column of interleaved gate row n of the fused gate+up weight (row 16q + i, i < 8,
 // holds gate row 8q + i; its up row is n + 8).

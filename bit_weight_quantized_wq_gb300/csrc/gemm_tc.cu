@@ -351,19 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_ld();
         if constexpr (EPI == kEpiSwiglu) {
           // Gate row n (lane bit 3 clear) and its up row n + 8 sit in lanes l and l ^ 8 of
-          // this warp: the gate lane takes the up value by a shuffle and writes SiLU(g) * u.
+          // this warp.  Per pair of accumulator columns (j, j + 1) one shuffle gives the gate
+          // lane the up value of column j and the up lane the gate value of column j + 1, so
+          // every lane evaluates SiLU(g) * u once per two columns.
           const bool gate = (lane & 8) == 0;
           const unsigned am = __activemask();   // the whole warp, unless a wait above timed out
           const int F = p.N >> 1;
-          const long long col = swiglu_col(n);
+          const long long col = swiglu_col(n & ~8);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m0 + c + j;
-            float y = __uint_as_float(v[j]);
-            if constexpr (FMT == kInt4G128) y *= __ldg(p.xscale + (m < p.M ? m : 0));
-            const float u = __shfl_xor_sync(am, y, 8);
-            if (gate && row_ok && m < p.M)
-              p.Y[static_cast<long long>(m) * F + col] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(y) * u));
+          for (int j = 0; j < 32; j += 2) {
+            const int ma = m0 + c + j, mb = ma + 1;
+            float y0 = __uint_as_float(v[j]), y1 = __uint_as_float(v[j + 1]);
+            if constexpr (FMT == kInt4G128) {
+              y0 *= __ldg(p.xscale + (ma < p.M ? ma : 0));
+              y1 *= __ldg(p.xscale + (mb < p.M ? mb : 0));
+            }
+            const float recv = __shfl_xor_sync(am, gate ? y1 : y0, 8);
+            const float g = gate ? y0 : recv, u = gate ? recv : y1;
+            const int m = gate ? ma : mb;
+            if (row_ok && m < p.M)
+              p.Y[static_cast<long long>(m) * F + col] = __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(g) * u));
           }
         } else if (row_ok) {
 #pragma unroll

@@ -221,53 +221,22 @@ __device__ BandContrib band_contributors(const Params& p, int band) {
 // One share of the deterministic split-K reduction of a band: the partial sums of every
 // contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
 // of the M x kBand outputs; bf16 results to Y.
-template <int MT>
-__device__ __forceinline__ float4 sum_contributors(const float* base, BandContrib bc) {
-  const long long cstride = 2LL * MT * kBand;
-  float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(bc.c_lo) * 2 + bc.lo_side) * MT * kBand);
-  for (int c = bc.c_lo + 1; c <= bc.c_hi; c += 4) {
-    float4 v[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      v[q] = (c + q <= bc.c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (c + q <= bc.c_hi) {
-        acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
-      }
-  }
-  return acc4;
-}
-
 template <int MT, int EPI>
 __device__ __forceinline__ void reduce_band_share(const Params& p, int band, BandContrib bc, int first, int step) {
-  if constexpr (EPI == kEpiSwiglu) {
-    // Gate rows 16q .. 16q + 7 of the band pair with up rows 16q + 8 .. 16q + 15: one item
-    // is a float4 of gate rows and the float4 of up rows 8 below it.
-    const int F = p.N >> 1;
-    for (int idx = first; idx < p.M * (kBand / 8); idx += step) {
-      const int m = idx / (kBand / 8);
-      const int k = idx % (kBand / 8);
-      const int r4 = 16 * (k >> 1) + 4 * (k & 1);
-      const float* base = p.part + static_cast<long long>(m) * kBand + r4;
-      const float4 g4 = sum_contributors<MT>(base, bc);
-      const float4 u4 = sum_contributors<MT>(base + 8, bc);
-      const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = band * kBand + r4 + q;
-        if (n < p.N)
-          p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
-              __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(gv[q]) * uv[q]));
-      }
-    }
-    return;
-  }
   const long long cstride = 2LL * MT * kBand;   // floats between two CTAs' partial slots
+  [[maybe_unused]] const unsigned am = __activemask();   // the whole warp unless a wait timed out
   for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
-    const int m = idx / (kBand / 4);
-    const int r4 = 4 * (idx % (kBand / 4));
+    int m, r4;
+    if constexpr (EPI == kEpiSwiglu) {
+      // slots idx and idx ^ 1 (lanes l and l ^ 1 of one warp): gate rows 16q + 4h .. + 3 and
+      // the up rows 8 below them
+      const int pr = idx >> 1, k = pr % (kBand / 8);
+      m = pr / (kBand / 8);
+      r4 = 16 * (k >> 1) + 4 * (k & 1) + 8 * (idx & 1);
+    } else {
+      m = idx / (kBand / 4);
+      r4 = 4 * (idx % (kBand / 4));
+    }
     const float* base = p.part + static_cast<long long>(m) * kBand + r4;
     float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(bc.c_lo) * 2 + bc.lo_side) * MT * kBand);
     for (int c = bc.c_lo + 1; c <= bc.c_hi; c += 8) {
@@ -283,10 +252,28 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, Ban
         }
     }
     const float o4[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
+    if constexpr (EPI == kEpiSwiglu) {
+      // p.M * kBand / 4 is a multiple of 64 and every warp's idx range is 32-aligned: whole
+      // warps run each iteration, so the shuffles below are converged
+      float u4[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int n = band * kBand + r4 + q;
-      if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o4[q]));
+      for (int q = 0; q < 4; ++q) u4[q] = __shfl_xor_sync(am, o4[q], 1);
+      if ((idx & 1) == 0) {
+        const int F = p.N >> 1;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int n = band * kBand + r4 + q;
+          if (n < p.N)
+            p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(o4[q]) * u4[q]));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int n = band * kBand + r4 + q;
+        if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o4[q]));
+      }
     }
   }
 }
