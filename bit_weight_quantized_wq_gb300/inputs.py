@@ -12,7 +12,12 @@ Qwen2.5-72B shapes):
   (推理优化与量化算子深度技术调研, §1.3 AWQ: about 1 % of channels matter most);
 * activations ``X`` [M, K] ~ Normal(0, 1), rounded to bfloat16 with
   round-to-nearest-even, returned both as raw bf16 bit patterns and as the
-  exact float32 values those patterns encode.
+  exact float32 values those patterns encode;
+* calibration activations for GPTQ [n, K], n = 128 samples (推理优化与量化算子深度技术调研 §1.3:
+  128 calibration samples usually suffice): correlated channels -- independent
+  Normal(0, 1) noise plus a shared rank-16 component Z B (Z [n, 16], B [16, K], both
+  standard normal, B scaled by 1/2) -- and 1 % of the channels multiplied by 10 (the
+  salient channels of the same section).
 
 Generator: numpy ``Generator(PCG64(seed))``; draws are float32 standard normals.
 """
@@ -25,6 +30,7 @@ __all__ = [
     "activations",
     "bf16_bits_from_f32",
     "f32_from_bf16_bits",
+    "calibration",
     "SEEDS",
 ]
 
@@ -79,3 +85,18 @@ def activations(seed: int, M: int, K: int, scale: float = 1.0):
         x *= np.float32(scale)
     bits = bf16_bits_from_f32(x)
     return bits, f32_from_bf16_bits(bits)
+
+
+def calibration(seed: int, n: int, K: int, rank: int = 16, outlier_frac: float = 0.01,
+                outlier_gain: float = 10.0) -> np.ndarray:
+    """float32 [n, K] calibration activations with correlated and salient channels."""
+    rng = _rng(seed + 104729)
+    X = rng.standard_normal((n, K), dtype=np.float32)
+    Z = rng.standard_normal((n, rank), dtype=np.float32)
+    B = rng.standard_normal((rank, K), dtype=np.float32) * np.float32(0.5)
+    X += Z @ B
+    n_out = int(round(outlier_frac * K))
+    if n_out > 0:
+        cols = rng.choice(K, size=n_out, replace=False)
+        X[:, cols] *= np.float32(outlier_gain)
+    return X

@@ -40,16 +40,31 @@ def quantize(W: np.ndarray):
     if K % GROUP != 0:
         raise ValueError("K must be a multiple of 128")
     x = W.reshape(N, K // GROUP, GROUP)
+    s16, z = group_params(x)
+    q = codes(x, s16, z)
+    return pack(q.reshape(N, K)), s16, z.astype(np.float16)
+
+
+def group_params(x: np.ndarray):
+    """Steps 1-4 for groups ``x`` float32 [..., 128]: ``(s fp16 [...], z int32 [...])``."""
+    x = np.asarray(x, dtype=np.float32)
     x_min = np.minimum(x.min(axis=-1), np.float32(0))
     x_max = np.maximum(x.max(axis=-1), np.float32(0))
     s32 = (x_max - x_min) / np.float32(LEVELS)                 # float32, round to nearest
-    s16 = s32.astype(np.float16)                                # stored scale
+    s16 = np.asarray(s32.astype(np.float16))                    # stored scale
     s16[s16 == 0] = np.float16(1)
     s = s16.astype(np.float32)
     z = np.rint((-x_min) / s).astype(np.int32)                  # non-negative integer
-    q = np.clip(np.rint(x / s[..., None]) + z[..., None].astype(np.float32), 0, LEVELS)
-    q = q.astype(np.uint32).reshape(N, K)
-    return pack(q), s16, z.astype(np.float16)
+    return s16, z
+
+
+def codes(x: np.ndarray, s16: np.ndarray, z: np.ndarray) -> np.ndarray:
+    """Step 5 for values ``x`` float32 [..., n] of groups with scale ``s16`` / zero ``z`` [...]:
+    ``q = clamp(round(x / s) + z, 0, 15)`` (uint32)."""
+    s = np.asarray(s16).astype(np.float32)[..., None]
+    zf = np.asarray(z).astype(np.float32)[..., None]
+    q = np.clip(np.rint(np.asarray(x, dtype=np.float32) / s) + zf, 0, LEVELS)
+    return q.astype(np.uint32)
 
 
 def pack(q: np.ndarray) -> np.ndarray:

@@ -14,7 +14,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
-from oracle import int4_g128, linear, mxfp4, swiglu, uniform
+from oracle import gptq, int4_g128, linear, mxfp4, swiglu, uniform
 from bit_weight_quantized_wq_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -465,3 +465,82 @@ def test_interleave_commutes_with_rowwise_quantization():
         b = q(swiglu.interleave_gate_up(W, F))
         for x, y in zip(a, b):
             assert (np.asarray(x).view(np.uint8) == np.asarray(y).view(np.uint8)).all()
+
+
+# ---------------------------------------------------------------------------
+# GPTQ (第 1 章：推理加速全景 §4.2; 推理优化与量化算子深度技术调研 §1.3)
+# ---------------------------------------------------------------------------
+
+def test_gptq_hessian_closed_form():
+    # X^T X = [[2, 1], [1, 5]] -> 2 X^T X = [[4, 2], [2, 10]], lambda = 0.01 * 7
+    X = np.array([[1.0, 0.0], [0.0, 2.0], [1.0, 1.0]])
+    H = gptq.hessian(X)
+    assert np.allclose(H, [[4.07, 2.0], [2.0, 10.07]], rtol=0, atol=1e-12)
+
+
+def test_gptq_inverse_cholesky_closed_form():
+    # H = [[4, 2], [2, 3]]: H^-1 = [[3, -2], [-2, 4]] / 8 = U^T U with
+    # U = [[sqrt(3/8), -(1/4)/sqrt(3/8)], [0, sqrt(1/3)]]
+    U = gptq.inverse_cholesky_upper(np.array([[4.0, 2.0], [2.0, 3.0]]))
+    u11 = math.sqrt(3.0 / 8.0)
+    ref = np.array([[u11, -0.25 / u11], [0.0, math.sqrt(1.0 / 3.0)]])
+    assert np.allclose(U, ref, rtol=0, atol=1e-14)
+    # a larger case: upper triangular, positive diagonal, U^T U H = I
+    X = inputs.calibration(5, 64, 48)
+    H = gptq.hessian(X)
+    U = gptq.inverse_cholesky_upper(H)
+    assert np.allclose(np.tril(U, -1), 0) and (np.diag(U) > 0).all()
+    assert np.allclose(U.T @ U @ H, np.eye(48), atol=1e-9)
+
+
+def test_gptq_diagonal_hessian_is_round_to_nearest():
+    # H diagonal -> U diagonal -> no compensation: the sweep is the plain INT4 g128 quantizer
+    N, K = 24, 384
+    W = inputs.weights(61, N, K, 0.05)
+    d = np.random.default_rng(62).uniform(0.5, 2.0, K).astype(np.float32)
+    got = gptq.sweep(W, np.diag(d))
+    ref = int4_g128.quantize(W)
+    for a, b in zip(got, ref):
+        assert (np.asarray(a).view(np.uint8) == np.asarray(b).view(np.uint8)).all()
+
+
+def _gptq_case(N=16, K=384, seed=63):
+    W = inputs.weights(seed, N, K, 0.05)
+    X = inputs.calibration(seed, 128, K)
+    H = gptq.hessian(X)
+    U64 = gptq.inverse_cholesky_upper(H)
+    U = U64.astype(np.float32)
+    Wq, s, z, e, seen = gptq.sweep(W, U, return_trace=True)
+    W_hat = int4_g128.dequantize(Wq, s, z)
+    return W, X, H, U64, U, (Wq, s, z), e, seen, W_hat
+
+
+def test_gptq_error_is_e_times_u_and_the_loss_decomposes():
+    # With w_j updated by -e_i U[i, j] for every i < j and w_hat_j = w_j(current) - e_j U[j, j]:
+    # w - w_hat = e U exactly; with H^-1 = U^T U that gives (w - w_hat) H (w - w_hat)^T = |e|^2.
+    W, X, H, U64, U, pk, e, seen, W_hat = _gptq_case()
+    delta = W.astype(np.float64) - W_hat
+    eU = e.astype(np.float64) @ U.astype(np.float64)
+    assert np.abs(delta - eU).max() <= 1e-4 * np.abs(delta).max()
+    Hf = np.linalg.inv(U.astype(np.float64).T @ U.astype(np.float64))
+    loss = np.einsum("nk,kl,nl->n", delta, Hf, delta)
+    assert np.allclose(loss, (e.astype(np.float64) ** 2).sum(axis=1), rtol=1e-3)
+
+
+def test_gptq_group_parameters_come_from_compensated_values():
+    W, X, H, U64, U, (Wq, s, z), e, seen, W_hat = _gptq_case()
+    s_ref, z_ref = int4_g128.group_params(seen)
+    assert (s_ref.view(np.uint16) == s.view(np.uint16)).all()
+    assert (z_ref.astype(np.float16).view(np.uint16) == z.view(np.uint16)).all()
+    # the first group starts from the original weights, later ones from compensated values
+    assert (seen[:, 0, :] == W[:, :128]).all()
+    assert not (seen[:, 1, :] == W[:, 128:256]).all()
+
+
+def test_gptq_lowers_the_calibration_objective():
+    # The point of the method: sum over rows of (w - w_hat) H (w - w_hat)^T falls below
+    # round-to-nearest's on the calibration set.
+    W, X, H, U64, U, pk, e, seen, W_hat = _gptq_case(N=32)
+    rtn = int4_g128.dequantize(*int4_g128.quantize(W))
+    obj = lambda Wh: float(np.einsum("nk,kl,nl->", W - Wh, H, W - Wh))
+    assert obj(W_hat) < 0.8 * obj(rtn)
