@@ -31,6 +31,7 @@ EXPORTED = [
     "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
     "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
     "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
+    "wq_gptq_int4_g128",
 ]
 
 _lib = None
@@ -63,6 +64,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_gemv_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
         "wq_gemm_tc_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
         "wq_interleave_gate_up": (I32, [P, P, I64, I64, P]),
+        "wq_gptq_int4_g128": (I32, [P, I64, I64, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -143,6 +145,22 @@ def quantize_mxfp4(W: torch.Tensor, stream=None):
     _check(load_library().wq_quantize_mxfp4(_ptr(W), N, K, _ptr(Wq), _ptr(scales), _stream(stream, W.device)),
            "wq_quantize_mxfp4")
     return Wq, scales
+
+
+def gptq_int4_g128(W: torch.Tensor, U: torch.Tensor, stream=None):
+    """GPTQ of W float32 [N, K] (CUDA) with U float32 [K, K], the upper Cholesky factor of the
+    inverse Hessian (H^-1 = U^T U) -> (Wq int32 [N, K/8], scales fp16 [N, K/128], zeros fp16)."""
+    _need(W, torch.float32, "W")
+    _need(U, torch.float32, "U")
+    N, K = W.shape
+    if tuple(U.shape) != (K, K):
+        raise ValueError("U must be [K, K]")
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    _check(load_library().wq_gptq_int4_g128(_ptr(W), N, K, _ptr(U), _ptr(Wq), _ptr(scales), _ptr(zeros),
+                                            _stream(stream, W.device)), "wq_gptq_int4_g128")
+    return Wq, scales, zeros
 
 
 def gemm_workspace_bytes(fmt, M: int, K: int, N: int) -> int:

@@ -124,6 +124,16 @@ wq_status wq_quantize_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq, u
   return from_cuda(wq::launch_quant_mxfp4(W, N, K, Wq, scales, static_cast<cudaStream_t>(stream)));
 }
 
+wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq, uint16_t* scales,
+                            uint16_t* zeros, void* stream) {
+  if (!W || !U || !Wq || !scales || !zeros) return WQ_ERR_NULL;
+  if (N < 1 || K < 128 || K % 128 != 0 || N > (1LL << 30) || wq::gptq_rows_per_cta(K) < 1) return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(U) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zeros)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gptq_int4_g128(W, N, K, U, Wq, scales, zeros, static_cast<cudaStream_t>(stream)));
+}
+
 int64_t wq_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N) {
   if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return -1;
   std::lock_guard<std::mutex> lk(g_thr_mu);

@@ -59,6 +59,11 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
                            cudaStream_t stream, int epi = kEpiNone);
 uint32_t gemm_tc_read_and_clear_error();
 
+// gptq.cu -- GPTQ sweep (INT4 g128) with a caller-provided inverse-Hessian Cholesky factor
+int gptq_rows_per_cta(int64_t K);
+cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
+                                  uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
+
 // layout.cu -- row re-layout of the stacked gate+up weight
 cudaError_t launch_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, cudaStream_t stream);
 

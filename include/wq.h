@@ -84,6 +84,34 @@ wq_status wq_quantize_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq,
                             uint8_t* scales, void* stream);
 
 /*
+ * GPTQ quantize + pack into the WQ_FMT_INT4_G128_ASYM format: the columns of W are quantized
+ * in order, each column's quantization error compensated on the columns not yet quantized
+ * through the inverse Hessian of the layer's calibration objective.
+ * Defined by: 第 1 章：推理加速全景 §4.2 (objective sum_j (W_j - Q(W_j))^T H (W_j - Q(W_j)) with
+ * H = 2 X^T X + lambda I; quantize column i, e_i = W[i] - W_q[i], W[j] -= (e_i / H^-1[i,i])
+ * H^-1[i,j] for j > i; H^-1 through its Cholesky factor) and 推理优化与量化算子深度技术调研 §1.3.
+ * With U the upper Cholesky factor of H^-1 (H^-1 = U^T U) the ratio H^-1[i,j] / H^-1[i,i] of
+ * the update is U[i,j] / U[i,i], so for every row, in float32 with each operation rounded on
+ * its own:
+ *   at i % 128 == 0: s, z of group i/128 from the row's CURRENT values of its 128 columns, by
+ *                    the rules of wq_quantize_int4_g128;
+ *   q_i = clamp(rint(w_i / s) + z, 0, 15);  e_i = (w_i - (q_i - z) s) / U[i,i];
+ *   w_j = w_j - e_i * U[i,j]  for j > i.
+ * With U diagonal (no correlation between input channels) this is wq_quantize_int4_g128.
+ *   W       [N, K] float32 input (not modified).
+ *   U       [K, K] float32, row-major: the upper Cholesky factor of H^-1 for the layer's
+ *           calibration activations (the caller computes H and the factor; only the upper
+ *           triangle including the positive diagonal is read).
+ *   Wq, scales, zeros   outputs, as wq_quantize_int4_g128.
+ * Work: N K^2 / 2 multiply-subtracts; rows are independent.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless N >= 1, K >= 128, K % 128 == 0 and K <= 46208
+ *         (a row's values and codes must fit one CTA's shared memory); WQ_ERR_ALIGN;
+ *         WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
+                            uint16_t* scales, uint16_t* zeros, void* stream);
+
+/*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
  * Every layout starts with the same 64 KiB header of split-K counters.  Zero the
  * workspace once before its first use; every call that completes leaves the header at zero

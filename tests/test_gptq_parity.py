@@ -1,0 +1,75 @@
+"""GPTQ sweep on the GPU against the oracle's sweep (第 1 章：推理加速全景 §4.2): codes, scales
+and zero points bit-exact.  Both sides take every decision in float32 with each operation
+rounded on its own, from the same inputs: W and the float32 inverse-Hessian factor U that the
+oracle computes from seeded calibration activations."""
+import numpy as np
+import pytest
+
+from bit_weight_quantized_wq_gb300 import inputs
+from oracle import gptq, int4_g128
+from tests._util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import torch
+    from bit_weight_quantized_wq_gb300 import binding
+    binding.check_device()
+    torch.cuda.init()
+    return binding
+
+
+def _factor(K, seed, n=128):
+    return gptq.inverse_cholesky_upper(gptq.hessian(inputs.calibration(seed, n, K))).astype(np.float32)
+
+
+def _same(got, ref, what):
+    for name, a, b in zip(("Wq", "scales", "zeros"), got, ref):
+        a = a.cpu().numpy() if hasattr(a, "cpu") else np.asarray(a)
+        bad = np.asarray(a).view(np.uint8) != np.asarray(b).view(np.uint8)
+        assert not bad.any(), "%s %s: %d of %d bytes differ" % (what, name, int(bad.sum()), bad.size)
+
+
+# (N, K): rows per CTA is 8 up to K = 5760, fewer above; N ragged against it
+@pytest.mark.parametrize("N,K", [(1, 128), (16, 128), (37, 384), (64, 1024), (9, 4096), (5, 6144)])
+def test_gptq_bit_exact(B, N, K):
+    W = inputs.weights(N * 31 + K, N, K, 0.05)
+    U = _factor(K, K + 3)
+    got = B.gptq_int4_g128(to_dev(W), to_dev(U))
+    _same(got, gptq.sweep(W, U), "N=%d K=%d" % (N, K))
+
+
+def test_gptq_diagonal_factor_equals_the_plain_quantizer(B):
+    # With U diagonal there is no compensation: the GPU sweep must reproduce the plain INT4
+    # quantizer (the GPU's and the oracle's).
+    N, K = 40, 512
+    W = inputs.weights(71, N, K, 0.05)
+    U = np.diag(np.random.default_rng(72).uniform(0.5, 2.0, K)).astype(np.float32)
+    got = B.gptq_int4_g128(to_dev(W), to_dev(U))
+    _same(got, int4_g128.quantize(W), "diagonal")
+    _same(got, [t.cpu().numpy() for t in B.quantize_int4_g128(to_dev(W))], "diagonal vs GPU quantizer")
+
+
+def test_gptq_full_size_sampled_rows(B):
+    # LLaMA-3-8B o_proj shape (K = N = 4096): every row on the GPU, 8 sampled rows on the
+    # oracle (rows are independent).
+    N = K = 4096
+    W = inputs.weights(73, N, K, 0.02)
+    U = _factor(K, 74)
+    got = [t.cpu().numpy() for t in B.gptq_int4_g128(to_dev(W), to_dev(U))]
+    rows = np.sort(np.random.default_rng(75).choice(N, 8, replace=False))
+    ref = gptq.sweep(W[rows], U)
+    _same([g[rows] for g in got], ref, "sampled rows")
+
+
+def test_gptq_rejects_bad_shapes(B):
+    import torch
+    W = torch.zeros((4, 200), dtype=torch.float32, device="cuda")
+    U = torch.zeros((200, 200), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        B.gptq_int4_g128(W, U)                  # K % 128 != 0
+    W = torch.zeros((4, 256), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        B.gptq_int4_g128(W, U)                  # U not [K, K]
