@@ -296,7 +296,7 @@ const char* wq_status_str(wq_status s) {
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
-  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error();
+  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() | wq::gptq_read_and_clear_error();
   return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 

@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* desc, in
       : "memory");
 }
 
+// Untiled bulk copy global -> shared: both addresses 16-byte aligned, `bytes` a multiple of 16;
+// completion counted on an mbarrier (expect_tx armed by the caller).
+__device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Warm L2 with a 2-D tile (no shared-memory destination, no completion tracking).  L2 is the
 // point of coherence, so a later write to the same lines by another kernel is never hidden.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* desc, int32_t c0, int32_t c1) {

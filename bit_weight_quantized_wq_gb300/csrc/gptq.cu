@@ -10,14 +10,27 @@
 // caller provides.  Each operation is rounded on its own (no contraction), so every code is
 // reproducible bit for bit.
 //
-// Rows are independent: one CTA owns R rows and keeps their current values (fp32) and codes
-// (one byte each) in shared memory for the whole sweep -- the pages' lazy block update exists
-// to avoid re-streaming W, which residency in shared memory avoids altogether.  Per column:
-// R threads take the decisions, then all threads apply the compensation to the later
-// columns, reading row i of U once (coalesced) for all R rows.
+// Rows are independent: one CTA owns R rows and keeps their current values on chip for the
+// whole sweep -- the pages' lazy block update exists to avoid re-streaming W, which on-chip
+// residency avoids altogether.  Two kernels:
+//   K <= 16384  registers: thread t owns columns t + 512 k; the owner of column i takes its
+//               decisions, publishes e_i through shared memory (double-buffered, one barrier
+//               per column) and every thread updates its own later columns with row i of U,
+//               which a bulk async copy brought into shared memory four columns ahead.
+//   larger K    shared memory: the rows' values live in shared memory; R threads decide, all
+//               threads update, two barriers per column.
 #include "internal.h"
 
 namespace wq {
+
+__device__ uint32_t g_gptq_err;
+
+uint32_t gptq_read_and_clear_error() {
+  uint32_t v = 0, z = 0;
+  cudaMemcpyFromSymbol(&v, g_gptq_err, sizeof(v));
+  cudaMemcpyToSymbol(g_gptq_err, &z, sizeof(z));
+  return v;
+}
 
 namespace {
 
@@ -115,6 +128,194 @@ __global__ void __launch_bounds__(kGptqThreads, 1)
   }
 }
 
+// INT4 g128 group parameters from a group's range [lo, hi] (lo <= 0 <= hi), the rules of the
+// quantize kernel: s = fp16(rn((hi - lo) / 15)) (0 -> 1), z = rint(-lo / s).
+__device__ __forceinline__ void group_params(float lo, float hi, __half& s16, float& s, int& z) {
+  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  s16 = __float2half_rn(s32);
+  if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
+  s = __half2float(s16);
+  z = __float2int_rn(__fdiv_rn(-lo, s));
+}
+
+template <int NJ>
+__device__ __forceinline__ float pick(const float (&a)[NJ], int k) {
+  float x = a[0];
+#pragma unroll
+  for (int m = 1; m < NJ; ++m)
+    if (k == m) x = a[m];
+  return x;
+}
+
+constexpr int kRegThreads = 512;
+constexpr uint32_t kErrGptqWait = 1u;
+
+// Register-resident sweep, R rows per CTA, columns t + 512 k (k < NJ) owned by thread t.  Row
+// i of U reaches shared memory by a bulk copy issued D columns ahead (a ring of D rows).
+template <int NJ, int R, int D>
+__global__ void __launch_bounds__(kRegThreads, 1)
+    k_gptq_int4_g128_reg(const float* __restrict__ W, int N, int K, const float* __restrict__ U,
+                         uint32_t* __restrict__ Wq, __half* __restrict__ scales, __half* __restrict__ zeros) {
+  constexpr int T = kRegThreads;
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* urow = reinterpret_cast<float*>(smem);                                  // [D][K]
+  uint8_t* code = smem + static_cast<size_t>(D) * K * sizeof(float);             // [R][K] codes
+  __shared__ __align__(8) uint64_t full[D];
+  __shared__ float s_err[2][R];
+  __shared__ float s_scale[R], s_zero[R];
+  __shared__ float s_lo[4][R], s_hi[4][R];
+  const int row0 = blockIdx.x * R;
+  const int rows = min(R, N - row0);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int G = K / 128;
+
+  // copy of row i of U from its 16-byte aligned column i & ~3 (covers the diagonal)
+  auto issue = [&](int i) {
+    const int c0 = i & ~3;
+    float* dst = urow + static_cast<size_t>(i % D) * K + c0;
+    const uint32_t bytes = static_cast<uint32_t>(K - c0) * 4u;
+    mbar_arrive_expect_tx(&full[i % D], bytes);
+    bulk_load_1d(dst, U + static_cast<long long>(i) * K + c0, bytes, &full[i % D]);
+  };
+  if (t == 0) {
+    for (int q = 0; q < D; ++q) mbar_init(&full[q], 1);
+    fence_barrier_init();
+    for (int q = 0; q < D && q < K; ++q) issue(q);
+  }
+
+  float v[R][NJ];   // current values of the owned columns
+#pragma unroll
+  for (int k = 0; k < NJ; ++k) {
+    const int j = t + T * k;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      v[r][k] = (r < rows && j < K) ? __ldg(W + static_cast<long long>(row0 + r) * K + j) : 0.f;
+  }
+  __syncthreads();
+
+  int i = 0;
+  for (; i < K; ++i) {
+    const int ki = i / T;
+    const int owner = i & (T - 1);
+    const float* ui = urow + static_cast<size_t>(i % D) * K;
+    bool bad = false;
+    if ((i & 127) == 0) {
+      // group parameters: the 4 warps owning columns i .. i + 127 reduce each row's range
+      const int w0 = owner >> 5;
+      if (warp >= w0 && warp < w0 + 4) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float x = pick<NJ>(v[r], ki);
+          float lo = fminf(0.f, x), hi = fmaxf(0.f, x);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+          }
+          if (lane == 0) {
+            s_lo[warp - w0][r] = lo;
+            s_hi[warp - w0][r] = hi;
+          }
+        }
+      }
+      __syncthreads();
+      if (t == owner) {
+        // every row slot, padding rows included (their values are 0: s = 1, z = 0), so the
+        // rows' independent chains can interleave; only real rows are stored
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float lo = fminf(fminf(s_lo[0][r], s_lo[1][r]), fminf(s_lo[2][r], s_lo[3][r]));
+          const float hi = fmaxf(fmaxf(s_hi[0][r], s_hi[1][r]), fmaxf(s_hi[2][r], s_hi[3][r]));
+          __half s16;
+          float sc;
+          int z;
+          group_params(lo, hi, s16, sc, z);
+          s_scale[r] = sc;
+          s_zero[r] = static_cast<float>(z);
+          if (r < rows) {
+            const long long gi = static_cast<long long>(row0 + r) * G + (i >> 7);
+            scales[gi] = s16;
+            zeros[gi] = __int2half_rn(z);
+          }
+        }
+      }
+    }
+    // row i of U has landed (every thread waits: all of them read it below)
+    bad = !mbar_wait(&full[i % D], (i / D) & 1, &g_gptq_err, kErrGptqWait);
+    if (t == owner && !bad) {
+      const float d = ui[i];   // U[i, i]
+#pragma unroll
+      for (int r = 0; r < R; ++r) {   // padding rows too (value 0, error 0)
+        const float x = pick<NJ>(v[r], ki);
+        const float sc = s_scale[r], zf = s_zero[r];
+        float q = __fadd_rn(rintf(__fdiv_rn(x, sc)), zf);
+        q = fminf(fmaxf(q, 0.f), 15.f);
+        code[static_cast<size_t>(r) * K + i] = static_cast<uint8_t>(q);
+        s_err[i & 1][r] = __fdiv_rn(__fsub_rn(x, __fmul_rn(__fsub_rn(q, zf), sc)), d);
+      }
+    }
+    // one barrier per column; a timed-out wait anywhere stops every thread here together
+    if (__syncthreads_or(bad)) break;
+    // slot of row i - 1 is free: every thread finished reading it (column i - 1) before this
+    // barrier, and nothing wrote it from the generic proxy, so the copy needs no proxy fence
+    if (t == 0 && i >= 1 && i - 1 + D < K) issue(i - 1 + D);
+    float e[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) e[r] = s_err[i & 1][r];
+#pragma unroll
+    for (int k = 0; k < NJ; ++k) {
+      const int j = t + T * k;
+      if (j > i && j < K) {
+        const float u = ui[j];
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r][k] = __fsub_rn(v[r][k], __fmul_rn(e[r], u));
+      }
+    }
+  }
+  __syncthreads();
+  if (i < K) {
+    // stopped early at column i: rows i .. last were issued and may still be in flight; let
+    // them land before the CTA exits
+    if (t == 0) {
+      const int last = (i == 0) ? min(K - 1, D - 1) : min(K - 1, i - 2 + D);
+      for (int q = i; q <= last; ++q) mbar_wait(&full[q % D], (q / D) & 1, &g_gptq_err, kErrGptqWait);
+    }
+    __syncthreads();
+    return;
+  }
+  for (int r = 0; r < rows; ++r) {
+    const uint8_t* c = code + static_cast<size_t>(r) * K;
+    uint32_t* out = Wq + static_cast<long long>(row0 + r) * (K / 8);
+    for (int j = t; j < K / 8; j += T) {
+      uint32_t word = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) word |= static_cast<uint32_t>(c[8 * j + k]) << (4 * k);
+      out[j] = word;
+    }
+  }
+}
+
+template <int NJ, int R, int D>
+cudaError_t launch_reg(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq, uint16_t* scales,
+                       uint16_t* zeros, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(D) * K * sizeof(float) + static_cast<size_t>(R) * K;
+  const long long grid = (N + R - 1) / R;
+  if (grid > 0x7fffffffLL || smem > static_cast<size_t>(kGptqSmem)) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_gptq_int4_g128_reg<NJ, R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGptqSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  k_gptq_int4_g128_reg<NJ, R, D><<<static_cast<unsigned>(grid), kRegThreads, smem, stream>>>(
+      W, static_cast<int>(N), static_cast<int>(K), U, reinterpret_cast<uint32_t*>(Wq),
+      reinterpret_cast<__half*>(scales), reinterpret_cast<__half*>(zeros));
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int gptq_rows_per_cta(int64_t K) {
@@ -126,6 +327,14 @@ int gptq_rows_per_cta(int64_t K) {
 
 cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
                                   uint16_t* scales, uint16_t* zeros, cudaStream_t stream) {
+  // R NJ values per thread within the 128 registers of a 512-thread CTA; the U ring (D rows)
+  // and the codes (R rows) within shared memory
+  if (K <= 512) return launch_reg<1, 8, 4>(W, N, K, U, Wq, scales, zeros, stream);
+  if (K <= 1024) return launch_reg<2, 8, 4>(W, N, K, U, Wq, scales, zeros, stream);
+  if (K <= 2048) return launch_reg<4, 8, 4>(W, N, K, U, Wq, scales, zeros, stream);
+  if (K <= 4096) return launch_reg<8, 8, 4>(W, N, K, U, Wq, scales, zeros, stream);
+  if (K <= 8192) return launch_reg<16, 5, 4>(W, N, K, U, Wq, scales, zeros, stream);
+  if (K <= 16384) return launch_reg<32, 2, 2>(W, N, K, U, Wq, scales, zeros, stream);
   const int R = gptq_rows_per_cta(K);
   if (R < 1) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(R) * K * 5;

@@ -61,6 +61,7 @@ uint32_t gemm_tc_read_and_clear_error();
 
 // gptq.cu -- GPTQ sweep (INT4 g128) with a caller-provided inverse-Hessian Cholesky factor
 int gptq_rows_per_cta(int64_t K);
+uint32_t gptq_read_and_clear_error();
 cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
                                   uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
 

@@ -31,6 +31,7 @@ __all__ = [
     "bf16_bits_from_f32",
     "f32_from_bf16_bits",
     "calibration",
+    "upper_factor",
     "SEEDS",
 ]
 
@@ -100,3 +101,14 @@ def calibration(seed: int, n: int, K: int, rank: int = 16, outlier_frac: float =
         cols = rng.choice(K, size=n_out, replace=False)
         X[:, cols] *= np.float32(outlier_gain)
     return X
+
+
+def upper_factor(seed: int, K: int, off_sigma: float = 0.3) -> np.ndarray:
+    """float32 [K, K] upper-triangular matrix with diagonal ~ Uniform(0.5, 1) and strictly
+    upper entries ~ Normal(0, off_sigma / sqrt(K)): a stand-in for an inverse-Hessian Cholesky
+    factor at sizes where computing one from calibration data would take minutes."""
+    rng = _rng(seed + 130363)
+    U = rng.standard_normal((K, K), dtype=np.float32) * np.float32(off_sigma / np.sqrt(K))
+    U = np.triu(U, 1)
+    U[np.arange(K), np.arange(K)] = rng.uniform(0.5, 1.0, K).astype(np.float32)
+    return U
