@@ -398,6 +398,20 @@ def run_ours(args):
     return 0
 
 
+def device_fp32_lane_ops_per_s(dev):
+    """SM count x 128 fp32 lanes x the maximum SM clock, the fp32 ALU ceiling."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = 2070.0   # the part's maximum SM clock, unless nvidia-smi reports it
+    try:
+        r = subprocess.run(["nvidia-smi", "-i", str(dev.index or 0), "--query-gpu=clocks.max.sm",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+        mhz = float(r.stdout.strip().splitlines()[0])
+    except Exception:
+        pass
+    return sms * 128 * mhz * 1e6
+
+
 def _graph_time(fn, stream, dev, reps, warm=3):
     import torch
     with torch.cuda.stream(stream):
@@ -533,6 +547,22 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                    "plain_gate_up_us": plain})
     out["swiglu_decode"] = {"workload": "LLaMA-3-8B fused gate+up (K=4096, 2F=28672) with SiLU(gate)*up "
                                         "in the epilogue, INT4 g128, Y [M, 14336]", "points": sw}
+
+    # GPTQ sweep (INT4 g128) on a LLaMA-3-8B projection (N = K = 4096).  The factor is the
+    # seeded stand-in (the sweep's work does not depend on its values).  Bound: fp32 ALU, one
+    # multiply and one subtract per update, N K^2 / 2 updates.
+    Wg = torch.from_numpy(inputs.weights(5100, 4096, 4096, 0.02)).to(dev)
+    Ug = torch.from_numpy(inputs.upper_factor(5101, 4096)).to(dev)
+    ms = _graph_time(lambda: binding.gptq_int4_g128(Wg, Ug), stream, dev, 2, warm=1)
+    upd = 4096.0 * 4096 * 4096 / 2
+    alu_peak = device_fp32_lane_ops_per_s(dev) / 2 / 1e12   # T updates/s
+    out["gptq_int4_g128"] = {"workload": "GPTQ sweep, N = K = 4096 (LLaMA-3-8B o_proj), INT4 g128",
+                             "ms": ms, "T_updates_per_s": upd / (ms * 1e-3) / 1e12,
+                             "roofline": {"bound": "alu", "achieved": upd / (ms * 1e-3) / 1e12, "peak": alu_peak,
+                                          "unit": "T updates/s", "frac": upd / (ms * 1e-3) / 1e12 / alu_peak,
+                                          "note": "peak = SMs x 128 fp32 lanes x max SM clock / 2 ops per update"}}
+    del Wg, Ug
+    torch.cuda.empty_cache()
 
     # quantize kernels on the decode shapes: fp32 read + packed write
     qres = {}
