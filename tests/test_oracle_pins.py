@@ -14,7 +14,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
-from oracle import gptq, int4_g128, linear, mxfp4, swiglu, uniform
+from oracle import awq, gptq, int4_g128, linear, mxfp4, swiglu, uniform
 from bit_weight_quantized_wq_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -544,3 +544,66 @@ def test_gptq_lowers_the_calibration_objective():
     rtn = int4_g128.dequantize(*int4_g128.quantize(W))
     obj = lambda Wh: float(np.einsum("nk,kl,nl->", W - Wh, H, W - Wh))
     assert obj(W_hat) < 0.8 * obj(rtn)
+
+
+# ---------------------------------------------------------------------------
+# AWQ (第 1 章：推理加速全景 §4.4; 推理优化与量化算子深度技术调研 §1.3; 量化与加速)
+# ---------------------------------------------------------------------------
+
+def test_awq_importance_and_salient_set():
+    X = np.array([[1.0, -2.0, 0.5], [3.0, 0.0, -0.5]], dtype=np.float32)
+    assert awq.importance(X).tolist() == [2.0, 1.0, 0.5]
+    # ceil(K / 100) channels: 3 of 201; equal importances rank by channel index
+    imp = np.ones(201)
+    imp[[7, 50, 199]] = [4.0, 9.0, 4.0]
+    assert np.flatnonzero(awq.salient(imp)).tolist() == [7, 50, 199]
+    imp[199] = 1.0
+    assert np.flatnonzero(awq.salient(imp)).tolist() == [0, 7, 50]
+    assert awq.salient(np.arange(100.0)).sum() == 1
+
+
+def test_awq_scales_closed_forms():
+    imp = np.array([4.0, 9.0, 2.25, 1.0])
+    mask = np.array([True, True, False, False])
+    assert awq.scales(imp, mask, 0).tolist() == [1.0, 1.0, 1.0, 1.0]
+    assert awq.scales(imp, mask, 20).tolist() == [4.0, 9.0, 1.0, 1.0]     # alpha = 1
+    assert awq.scales(imp, mask, 10).tolist() == [2.0, 3.0, 1.0, 1.0]     # alpha = 1/2
+
+
+def test_awq_alpha_zero_is_round_to_nearest():
+    W = inputs.weights(83, 32, 512, 0.05)
+    X = inputs.calibration(84, 64, 512)
+    s = awq.scales(awq.importance(X), awq.salient(awq.importance(X)), 0)
+    got = awq.quantize_scaled(W, s)
+    ref = int4_g128.quantize(W)
+    for a, b in zip(got, ref):
+        assert (np.asarray(a).view(np.uint8) == np.asarray(b).view(np.uint8)).all()
+    W_hat = int4_g128.dequantize(*ref)
+    E = X.astype(np.float64) @ (W_hat - W.astype(np.float64)).T
+    assert abs(awq.loss(W, X, s) - float((E * E).sum())) <= 1e-9 * float((E * E).sum())
+
+
+def test_awq_loss_is_the_runtime_error_with_divided_activations():
+    # Q(W s) applied to x / s, minus W x: the same number as the loss computed on W_hat = Q(W s) / s,
+    # which pins the direction of the scaling (weights times s, activations divided by s).
+    W = inputs.weights(85, 24, 384, 0.05)
+    X = inputs.calibration(86, 32, 384)
+    imp = awq.importance(X)
+    s = awq.scales(imp, awq.salient(imp), 12)
+    assert (s > 1).any()
+    Qws = int4_g128.dequantize(*awq.quantize_scaled(W, s))
+    Y_q = (X.astype(np.float64) / s.astype(np.float64)[None, :]) @ Qws.T
+    Y = X.astype(np.float64) @ W.astype(np.float64).T
+    ref = float(((Y_q - Y) ** 2).sum())
+    assert abs(awq.loss(W, X, s) - ref) <= 1e-9 * ref
+
+
+def test_awq_search_protects_salient_channels():
+    # With 1 % of the activation channels ten times larger, scaling them lowers the output error
+    # well below round-to-nearest's; alpha = 0 is in the grid, so the search never does worse.
+    W = inputs.weights(87, 64, 1024, 0.05)
+    X = inputs.calibration(88, 128, 1024)
+    a, s, losses, pk = awq.search(W, X)
+    assert losses[a] == losses.min() and 0 < a < awq.GRID
+    assert losses[a] < 0.8 * losses[0]
+    assert (np.asarray(pk[0]) == np.asarray(awq.quantize_scaled(W, s)[0])).all()
