@@ -31,7 +31,7 @@ EXPORTED = [
     "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
     "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
     "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
-    "wq_gptq_int4_g128",
+    "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128",
 ]
 
 _lib = None
@@ -65,6 +65,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_gemm_tc_w4a16_swiglu": (I32, [I32, P, I64, I64, I64, P, P, P, P, P, SZ, P]),
         "wq_interleave_gate_up": (I32, [P, P, I64, I64, P]),
         "wq_gptq_int4_g128": (I32, [P, I64, I64, P, P, P, P, P]),
+        "wq_awq_workspace_bytes": (SZ, [I64, I64, I64]),
+        "wq_awq_int4_g128": (I32, [P, I64, I64, P, I64, P, P, P, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -161,6 +163,32 @@ def gptq_int4_g128(W: torch.Tensor, U: torch.Tensor, stream=None):
     _check(load_library().wq_gptq_int4_g128(_ptr(W), N, K, _ptr(U), _ptr(Wq), _ptr(scales), _ptr(zeros),
                                             _stream(stream, W.device)), "wq_gptq_int4_g128")
     return Wq, scales, zeros
+
+
+def awq_int4_g128(W: torch.Tensor, X: torch.Tensor, workspace=None, stream=None):
+    """AWQ of W float32 [N, K] with calibration activations X float32 [n, K] (both CUDA) ->
+    (Wq, scales, zeros, s float32 [K], alpha_index int32 [1], losses float64 [21]); the layer's
+    activations are divided by s at run time."""
+    _need(W, torch.float32, "W")
+    _need(X, torch.float32, "X")
+    N, K = W.shape
+    n = X.shape[0]
+    if X.shape[1] != K:
+        raise ValueError("X must be [n, K]")
+    dev = W.device
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=dev)
+    scales = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+    zeros = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+    s = torch.empty((K,), dtype=torch.float32, device=dev)
+    a = torch.empty((1,), dtype=torch.int32, device=dev)
+    losses = torch.empty((21,), dtype=torch.float64, device=dev)
+    lib = load_library()
+    if workspace is None:
+        workspace = torch.empty((int(lib.wq_awq_workspace_bytes(N, K, n)),), dtype=torch.uint8, device=dev)
+    _check(lib.wq_awq_int4_g128(_ptr(W), N, K, _ptr(X), n, _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(s), _ptr(a),
+                                _ptr(losses), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream, dev)), "wq_awq_int4_g128")
+    return Wq, scales, zeros, s, a, losses
 
 
 def gemm_workspace_bytes(fmt, M: int, K: int, N: int) -> int:

@@ -134,6 +134,30 @@ wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U
   return from_cuda(wq::launch_gptq_int4_g128(W, N, K, U, Wq, scales, zeros, static_cast<cudaStream_t>(stream)));
 }
 
+size_t wq_awq_workspace_bytes(int64_t N, int64_t K, int64_t n) {
+  if (N < 1 || n < 1 || K < 128 || K % 128 != 0 || N > (1LL << 30) || K > (1LL << 30) || n > (1LL << 30)) return 0;
+  return wq::awq_workspace_bytes(N, K, n);
+}
+
+wq_status wq_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X, int64_t n, int32_t* Wq,
+                           uint16_t* scales, uint16_t* zeros, float* s, int32_t* alpha_index, double* losses,
+                           void* workspace, size_t ws_bytes, void* stream) {
+  if (!W || !X || !Wq || !scales || !zeros || !s) return WQ_ERR_NULL;
+  if (N < 1 || n < 1 || K < 128 || K % 128 != 0 || N > (1LL << 30) || K > (1LL << 30) || n > (1LL << 30))
+    return WQ_ERR_SHAPE;
+  if (N * K > (1LL << 40)) return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zeros) || !aligned16(s) ||
+      (alpha_index && (reinterpret_cast<uintptr_t>(alpha_index) & 3u)) ||
+      (losses && (reinterpret_cast<uintptr_t>(losses) & 7u)))
+    return WQ_ERR_ALIGN;
+  if (!workspace || ws_bytes < wq::awq_workspace_bytes(N, K, n)) return WQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_awq_int4_g128(W, N, K, X, n, Wq, scales, zeros, s, alpha_index, losses, workspace,
+                                            ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
 int64_t wq_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N) {
   if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return -1;
   std::lock_guard<std::mutex> lk(g_thr_mu);

@@ -65,6 +65,12 @@ uint32_t gptq_read_and_clear_error();
 cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
                                   uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
 
+// awq.cu -- AWQ scale search + INT4 g128 quantize of the scaled weight
+size_t awq_workspace_bytes(int64_t N, int64_t K, int64_t n);
+cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X, int64_t n, int32_t* Wq,
+                                 uint16_t* scales, uint16_t* zeros, float* s_out, int32_t* a_out, double* losses_out,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
+
 // layout.cu -- row re-layout of the stacked gate+up weight
 cudaError_t launch_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, cudaStream_t stream);
 

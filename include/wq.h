@@ -112,6 +112,37 @@ wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U
                             uint16_t* scales, uint16_t* zeros, void* stream);
 
 /*
+ * AWQ: scales the salient input channels of W before INT4 g128 quantization, the scale's
+ * exponent chosen by a grid search on calibration activations.
+ * Defined by: 第 1 章：推理加速全景 §4.4 (importance_j = mean |X_j| over the calibration set;
+ * the top 1 % channels are salient; s_j = importance_j ^ alpha, alpha by grid search in [0, 1];
+ * quantize W' = W diag(s)), 推理优化与量化算子深度技术调研 §1.3 (W'' = W * s, x'' = x / s, s minimising
+ * || Q(W * s) * (x / s) - W x ||) and 量化与加速 (only the top 1 % channels are scaled).
+ * Computed:
+ *   importance_j = (sum over the n samples, in order, of |X[n, j]|) / n in float64;
+ *   salient = the ceil(K / 100) channels of largest importance (equal: lower index first);
+ *   for a = 0 .. 20: s_j = float32(importance_j ^ (a / 20)) on salient channels with
+ *     importance > 0, else 1; L(a) = || X (Q(W diag(s)) diag(s)^-1 - W)^T ||_F^2 (fp32 products,
+ *     fp64 sums of squares);  a* = the smallest a with minimal L(a);
+ *   Wq, scales, zeros = wq_quantize_int4_g128 of float32(W_ij * s*_j).
+ * At run time the layer's activations must be divided by s* (x / s*, usually folded into the
+ * operation that produces x).
+ *   W       [N, K] float32.       X  [n, K] float32 calibration activations (n >= 1).
+ *   Wq, scales, zeros   outputs, as wq_quantize_int4_g128.
+ *   s       [K] float32 output: s*.
+ *   alpha_index   int32 output (may be NULL): a*.      losses  [21] double output (may be NULL).
+ *   workspace / ws_bytes: at least wq_awq_workspace_bytes(N, K, n) bytes of device memory
+ *           (includes an N x K fp32 scratch matrix); no initialisation needed.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless N >= 1, n >= 1, K >= 128, K % 128 == 0;
+ *         WQ_ERR_ALIGN (losses: 8 bytes; the others 16); WQ_ERR_WORKSPACE;
+ *         WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+size_t wq_awq_workspace_bytes(int64_t N, int64_t K, int64_t n);
+wq_status wq_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X, int64_t n, int32_t* Wq,
+                           uint16_t* scales, uint16_t* zeros, float* s, int32_t* alpha_index, double* losses,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
  * Every layout starts with the same 64 KiB header of split-K counters.  Zero the
  * workspace once before its first use; every call that completes leaves the header at zero

@@ -17,8 +17,10 @@ Readings:
       W diag(s)^-1 and X diag(s) while its comments say the salient weights are enlarged and
       the activations shrunk; its formulas are read as garbled.
 * A2  Only the top ceil(K / 100) channels by importance are scaled (量化与加速: only the top
-      1 % most important channels; 第 1 章 step 1 selects them); s_j = 1 elsewhere.  Equal
-      importances: the lower channel index ranks first.
+      1 % most important channels; 第 1 章 step 1 selects them); s_j = 1 elsewhere, and also
+      on a selected channel whose importance is 0 (all its calibration values are 0, so any
+      scale leaves the loss unchanged; s = 0 would not be invertible).  Equal importances: the
+      lower channel index ranks first.
 * A3  The grid is alpha = a / 20, a = 0 .. 20 (第 1 章 gives [0, 1] without a step).  alpha = 0
       is plain round-to-nearest.  Among equal losses the smallest alpha wins.
 * A4  The loss is || X (W_hat - W)^T ||_F^2 with W_hat = dequant(Q(W diag(s))) diag(s)^-1,
@@ -60,7 +62,8 @@ def scales(imp: np.ndarray, mask: np.ndarray, a: int) -> np.ndarray:
     """float32 s for alpha = a / GRID (A2, A5)."""
     alpha = a / float(GRID)
     s = np.ones(imp.shape[0], dtype=np.float64)
-    s[mask] = imp[mask] ** alpha
+    sel = mask & (imp > 0)
+    s[sel] = imp[sel] ** alpha
     return s.astype(np.float32)
 
 
