@@ -564,6 +564,22 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
     del Wg, Ug
     torch.cuda.empty_cache()
 
+    # AWQ search (21 exponents) + packing on the same projection, 128 calibration samples.
+    # Bound: the fp32 error GEMM, 2 n N K per exponent.
+    Wa = torch.from_numpy(inputs.weights(5200, 4096, 4096, 0.02)).to(dev)
+    Xa = torch.from_numpy(inputs.calibration(5201, 128, 4096)).to(dev)
+    wsa = torch.empty(binding.load_library().wq_awq_workspace_bytes(4096, 4096, 128), dtype=torch.uint8, device=dev)
+    ms = _graph_time(lambda: binding.awq_int4_g128(Wa, Xa, workspace=wsa), stream, dev, 3, warm=1)
+    fl = 21 * 2.0 * 128 * 4096 * 4096
+    fp32_peak = device_fp32_lane_ops_per_s(dev) * 2 / 1e12    # TFLOP/s, FMA = 2
+    out["awq_int4_g128"] = {"workload": "AWQ search (21 exponents) + packing, N = K = 4096, 128 calibration samples",
+                            "ms": ms,
+                            "roofline": {"bound": "alu", "achieved": fl / (ms * 1e-3) / 1e12, "peak": fp32_peak,
+                                         "unit": "TFLOP/s", "frac": fl / (ms * 1e-3) / 1e12 / fp32_peak,
+                                         "note": "error-GEMM flops over the whole search time; peak = fp32 FMA rate"}}
+    del Wa, Xa, wsa
+    torch.cuda.empty_cache()
+
     # quantize kernels on the decode shapes: fp32 read + packed write
     qres = {}
     for name, fn, ob in (("int4_g128", binding.quantize_int4_g128, 0.53125), ("mxfp4", binding.quantize_mxfp4, 0.53125)):
