@@ -647,6 +647,8 @@ def run_ncu_case(args):
     swiglu_decode: the decode layer read as the fused gate+up weight (2F = 28672) with the
              SwiGLU epilogue, M = 1, INT4.
     quant:   INT4 quantize of the (4096, 28672) weights (470 MB fp32).
+    gptq:    the GPTQ sweep, N = K = 4096, seeded stand-in inverse-Hessian factor.
+    awq:     the AWQ search + packing, N = K = 4096, 128 calibration samples.
     """
     import numpy as np
     import torch
@@ -677,6 +679,21 @@ def run_ncu_case(args):
                     n += 1
         torch.cuda.synchronize()
         print(json.dumps({"ncu_case": case, "launches": n, "launches_per_step": len(DECODE_M) * len(DECODE_SHAPES)}))
+        return 0
+    if case in ("gptq", "awq"):
+        W = torch.from_numpy(inputs.weights(5100, 4096, 4096, 0.02)).to(dev)
+        if case == "gptq":
+            U = torch.from_numpy(inputs.upper_factor(5101, 4096)).to(dev)
+            fn = lambda: binding.gptq_int4_g128(W, U)
+        else:
+            X = torch.from_numpy(inputs.calibration(5201, 128, 4096)).to(dev)
+            wsa = torch.empty(binding.load_library().wq_awq_workspace_bytes(4096, 4096, 128), dtype=torch.uint8,
+                              device=dev)
+            fn = lambda: binding.awq_int4_g128(W, X, workspace=wsa)
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": case, "calls": args.warmup + args.steps}))
         return 0
     if case in ("decode", "mxfp4", "swiglu_decode"):
         K, N, M, fmt = 4096, 28672, 1, ("mxfp4" if case == "mxfp4" else "int4_g128")
@@ -718,7 +735,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-sample", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "swiglu_decode", "quant"],
+    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "swiglu_decode", "quant", "gptq", "awq"],
                     help="run a few plain launches of one kernel (for ncu captures) instead of the bench")
     args = ap.parse_args()
     if args.cpu_sample is not None:

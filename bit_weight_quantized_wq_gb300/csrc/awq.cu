@@ -10,8 +10,8 @@
 //
 // Per candidate a: one pass quantizes W diag(s) group by group (the rules of the quantize
 // kernel) and writes the weight error D = Q(W s) / s - W in fp32; an fp32 GEMM-shaped kernel
-// forms E = X D^T tile by tile and reduces sum(E^2) into per-tile partials, which one thread
-// adds in a fixed order.  The candidates, the arg-min and the final packing run back to back
+// forms E = X D^T tile by tile in K slices, a second pass adds the slices and squares, and the
+// partial sums are added in a fixed order.  The candidates, the arg-min and the final packing run back to back
 // on the stream with no host synchronisation.
 #include "internal.h"
 
@@ -128,19 +128,21 @@ __global__ void __launch_bounds__(256) k_awq_quant(const float* __restrict__ W, 
   }
 }
 
-// E = X D^T (X [n, K], D [N, K], both K-contiguous) in 64 x 64 tiles, 4 x 4 per thread, fp32;
-// each tile's sum of squares (fp64) goes to partial[tile].
+// E = X D^T (X [n, K], D [N, K], both K-contiguous) in 64 x 64 tiles, 4 x 4 per thread, fp32,
+// split along K into gridDim.z slices (more CTAs than SMs, so loads overlap compute): slice z
+// writes its partial product to Epart[z][m][i].
 constexpr int kTM = 64, kTN = 64, kTK = 32;
 
 __global__ void __launch_bounds__(256) k_awq_err(const float* __restrict__ X, const float* __restrict__ D, int n,
-                                                 int N, int K, double* __restrict__ partial) {
+                                                 int N, int K, float* __restrict__ Epart) {
   __shared__ float xs[kTK][kTM + 4];
   __shared__ float ds[kTK][kTN + 4];
-  __shared__ double red[256];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
+  const int kslice = K / gridDim.z;
+  const int kbeg = blockIdx.z * kslice, kend = kbeg + kslice;
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += kTK) {
+  for (int k0 = kbeg; k0 < kend; k0 += kTK) {
     // 64 x 32 floats of each operand, 8 per thread: element e = threadIdx.x + 256 q
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
@@ -163,22 +165,45 @@ __global__ void __launch_bounds__(256) k_awq_err(const float* __restrict__ X, co
     }
     __syncthreads();
   }
-  double sq = 0.0;
+  float* out = Epart + static_cast<long long>(blockIdx.z) * n * N;
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
+  for (int u = 0; u < 4; ++u) {
+    const int m = m0 + ty * 4 + u;
+    if (m >= n) continue;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      const double e = static_cast<double>(acc[u][v]);
-      sq += e * e;   // outside the matrix both operands were 0, so e = 0
+      const int i = n0 + tx * 4 + v;
+      if (i < N) out[static_cast<long long>(m) * N + i] = acc[u][v];
     }
+  }
+}
+
+// Sum of squares of E = sum over slices of Epart (slices added in order): each CTA takes a
+// contiguous chunk of the n N elements and writes its fp64 sum to partial[blockIdx.x].
+__global__ void __launch_bounds__(256) k_awq_sq(const float* __restrict__ Epart, int slices, long long count,
+                                                double* __restrict__ partial) {
+  __shared__ double red[256];
+  const long long chunk = (count + gridDim.x - 1) / gridDim.x;
+  const long long beg = static_cast<long long>(blockIdx.x) * chunk;
+  const long long end = min(count, beg + chunk);
+  double sq = 0.0;
+  for (long long e = beg + threadIdx.x; e < end; e += blockDim.x) {
+    float v = Epart[e];
+    for (int z = 1; z < slices; ++z) v += Epart[static_cast<long long>(z) * count + e];
+    sq += static_cast<double>(v) * static_cast<double>(v);
+  }
   red[threadIdx.x] = sq;
   __syncthreads();
   for (int o = 128; o > 0; o >>= 1) {
     if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
     __syncthreads();
   }
-  if (threadIdx.x == 0) partial[blockIdx.y * gridDim.x + blockIdx.x] = red[0];
+  if (threadIdx.x == 0) partial[blockIdx.x] = red[0];
 }
+
+constexpr int kSqCtas = 256;
+
+int awq_kslices(int64_t K) { return K >= 512 ? 4 : (K >= 256 ? 2 : 1); }
 
 __global__ void k_awq_sum(const double* __restrict__ partial, int count, double* __restrict__ out) {
   double acc = 0.0;
@@ -201,9 +226,9 @@ size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 }  // namespace
 
 size_t awq_workspace_bytes(int64_t N, int64_t K, int64_t n) {
-  const size_t tiles = static_cast<size_t>((N + kTN - 1) / kTN) * static_cast<size_t>((n + kTM - 1) / kTM);
   return align256(K * sizeof(double)) + align256(K) + align256(K * sizeof(float)) +
-         align256(static_cast<size_t>(N) * K * sizeof(float)) + align256(tiles * sizeof(double)) +
+         align256(static_cast<size_t>(N) * K * sizeof(float)) +
+         align256(static_cast<size_t>(awq_kslices(K)) * n * N * sizeof(float)) + align256(kSqCtas * sizeof(double)) +
          align256((kAwqGrid + 1) * sizeof(double)) + align256(sizeof(int));
 }
 
@@ -220,9 +245,13 @@ cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const flo
   p += align256(K * sizeof(float));
   float* D = reinterpret_cast<float*>(p);
   p += align256(static_cast<size_t>(N) * K * sizeof(float));
+  const int slices = awq_kslices(K);
+  float* Epart = reinterpret_cast<float*>(p);
+  p += align256(static_cast<size_t>(slices) * n * N * sizeof(float));
   double* partial = reinterpret_cast<double*>(p);
-  const dim3 egrid(static_cast<unsigned>((N + kTN - 1) / kTN), static_cast<unsigned>((n + kTM - 1) / kTM));
-  p += align256(static_cast<size_t>(egrid.x) * egrid.y * sizeof(double));
+  p += align256(kSqCtas * sizeof(double));
+  const dim3 egrid(static_cast<unsigned>((N + kTN - 1) / kTN), static_cast<unsigned>((n + kTM - 1) / kTM),
+                   static_cast<unsigned>(slices));
   double* losses = reinterpret_cast<double*>(p);
   p += align256((kAwqGrid + 1) * sizeof(double));
   int* a_best = reinterpret_cast<int*>(p);
@@ -239,8 +268,9 @@ cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const flo
     k_awq_scales<<<kb, 256, 0, stream>>>(imp, mask, static_cast<int>(K), a, nullptr, s);
     k_awq_quant<<<static_cast<unsigned>(qgrid), 256, 0, stream>>>(W, s, groups, static_cast<int>(K), D, nullptr,
                                                                    nullptr, nullptr);
-    k_awq_err<<<egrid, 256, 0, stream>>>(X, D, static_cast<int>(n), static_cast<int>(N), static_cast<int>(K), partial);
-    k_awq_sum<<<1, 1, 0, stream>>>(partial, static_cast<int>(egrid.x * egrid.y), losses + a);
+    k_awq_err<<<egrid, 256, 0, stream>>>(X, D, static_cast<int>(n), static_cast<int>(N), static_cast<int>(K), Epart);
+    k_awq_sq<<<kSqCtas, 256, 0, stream>>>(Epart, slices, n * N, partial);
+    k_awq_sum<<<1, 1, 0, stream>>>(partial, kSqCtas, losses + a);
   }
   k_awq_pick<<<1, 1, 0, stream>>>(losses, kAwqGrid + 1, a_best, a_out);
   k_awq_scales<<<kb, 256, 0, stream>>>(imp, mask, static_cast<int>(K), 0, a_best, s_out);
