@@ -53,7 +53,7 @@ def inverse_cholesky_upper(H: np.ndarray) -> np.ndarray:
     Li = np.linalg.solve(L, np.eye(H.shape[0]))     # L^-1
     Hinv = Li.T @ Li                                # H^-1
     Hinv = 0.5 * (Hinv + Hinv.T)
-    return np.linalg.cholesky(Hinv).T               # H^-1 = (L')(L')^T = U^T U, U = L'^T
+    return np.ascontiguousarray(np.linalg.cholesky(Hinv).T)   # H^-1 = (L')(L')^T = U^T U, U = L'^T
 
 
 def sweep(W: np.ndarray, U: np.ndarray, return_trace: bool = False):
