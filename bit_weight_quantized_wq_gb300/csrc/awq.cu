@@ -186,13 +186,14 @@ __global__ void __launch_bounds__(256) k_awq_sq(const float* __restrict__ Epart,
   const long long chunk = (count + gridDim.x - 1) / gridDim.x;
   const long long beg = static_cast<long long>(blockIdx.x) * chunk;
   const long long end = min(count, beg + chunk);
-  double sq = 0.0;
+  // each thread's few elements in fp32 (fp64 throughput is low), then fp64 across threads
+  float sq32 = 0.f;
   for (long long e = beg + threadIdx.x; e < end; e += blockDim.x) {
     float v = Epart[e];
     for (int z = 1; z < slices; ++z) v += Epart[static_cast<long long>(z) * count + e];
-    sq += static_cast<double>(v) * static_cast<double>(v);
+    sq32 = fmaf(v, v, sq32);
   }
-  red[threadIdx.x] = sq;
+  red[threadIdx.x] = static_cast<double>(sq32);
   __syncthreads();
   for (int o = 128; o > 0; o >>= 1) {
     if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
@@ -205,10 +206,13 @@ constexpr int kSqCtas = 256;
 
 int awq_kslices(int64_t K) { return K >= 512 ? 4 : (K >= 256 ? 2 : 1); }
 
-__global__ void k_awq_sum(const double* __restrict__ partial, int count, double* __restrict__ out) {
+// One warp: lane l adds partials l, l + 32, ... in order, then a fixed shuffle tree.
+__global__ void __launch_bounds__(32) k_awq_sum(const double* __restrict__ partial, int count, double* __restrict__ out) {
   double acc = 0.0;
-  for (int i = 0; i < count; ++i) acc += partial[i];
-  *out = acc;
+  for (int i = threadIdx.x; i < count; i += 32) acc += partial[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (threadIdx.x == 0) *out = acc;
 }
 
 // the smallest a among the minimal losses
@@ -270,7 +274,7 @@ cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const flo
                                                                    nullptr, nullptr);
     k_awq_err<<<egrid, 256, 0, stream>>>(X, D, static_cast<int>(n), static_cast<int>(N), static_cast<int>(K), Epart);
     k_awq_sq<<<kSqCtas, 256, 0, stream>>>(Epart, slices, n * N, partial);
-    k_awq_sum<<<1, 1, 0, stream>>>(partial, kSqCtas, losses + a);
+    k_awq_sum<<<1, 32, 0, stream>>>(partial, kSqCtas, losses + a);
   }
   k_awq_pick<<<1, 1, 0, stream>>>(losses, kAwqGrid + 1, a_best, a_out);
   k_awq_scales<<<kb, 256, 0, stream>>>(imp, mask, static_cast<int>(K), 0, a_best, s_out);
