@@ -102,3 +102,37 @@ def test_dispatch_threshold_table(lib):
     with pytest.raises(ValueError):
         binding.set_dispatch_threshold("int4_g128", 4096, 4096, 17)
     assert lib.wq_set_dispatch_threshold(3, 0, 0, 1) == 7
+
+
+def test_validation_errors_swiglu_interleave_gptq_awq(lib):
+    # SwiGLU: F % 8, F >= 8, and the decode-only M bound
+    sw = lambda fn, M=1, K=128, F=8, **kw: getattr(lib, fn)(0, FAKE, M, K, F, FAKE, FAKE, FAKE, FAKE,
+                                                            kw.get("ws"), kw.get("wsb", 0), None)
+    assert sw("wq_gemm_w4a16_swiglu", F=12) == 2
+    assert sw("wq_gemm_w4a16_swiglu", F=0) == 2
+    assert sw("wq_gemv_w4a16_swiglu", M=17, F=16) == 2
+    assert sw("wq_gemm_tc_w4a16_swiglu", K=64, F=16) == 2
+    assert sw("wq_gemv_w4a16_swiglu", F=4096) == 4          # workspace missing
+    # interleave: NULL, F, row bytes, overlap (src == dst)
+    assert lib.wq_interleave_gate_up(None, FAKE, 8, 16, None) == 1
+    assert lib.wq_interleave_gate_up(FAKE, ctypes.c_void_p(0x900000), 12, 16, None) == 2
+    assert lib.wq_interleave_gate_up(FAKE, ctypes.c_void_p(0x900000), 8, 0, None) == 2
+    assert lib.wq_interleave_gate_up(FAKE, FAKE, 8, 16, None) == 7
+    assert lib.wq_interleave_gate_up(FAKE, ctypes.c_void_p(0x10000 + 8 * 16), 8, 16, None) == 7   # overlaps
+    # GPTQ: NULL factor, K % 128, K beyond one CTA's shared memory, alignment
+    assert lib.wq_gptq_int4_g128(FAKE, 4, 128, None, FAKE, FAKE, FAKE, None) == 1
+    assert lib.wq_gptq_int4_g128(FAKE, 4, 200, FAKE, FAKE, FAKE, FAKE, None) == 2
+    assert lib.wq_gptq_int4_g128(FAKE, 4, 46336, FAKE, FAKE, FAKE, FAKE, None) == 2
+    assert lib.wq_gptq_int4_g128(ODD, 4, 128, FAKE, FAKE, FAKE, FAKE, None) == 3
+    # AWQ: workspace size, shapes, NULLs, alignment
+    assert lib.wq_awq_workspace_bytes(4096, 4096, 128) >= 4096 * 4096 * 4
+    assert lib.wq_awq_workspace_bytes(4096, 100, 128) == 0
+    aw = lambda W=FAKE, N=4, K=128, X=FAKE, n=8, s=FAKE, ws=FAKE, wsb=1 << 30: lib.wq_awq_int4_g128(
+        W, N, K, X, n, FAKE, FAKE, FAKE, s, None, None, ws, wsb, None)
+    assert aw(X=None) == 1
+    assert aw(s=None) == 1
+    assert aw(n=0) == 2
+    assert aw(K=96) == 2
+    assert aw(X=ODD) == 3
+    assert aw(ws=None) == 4
+    assert aw(wsb=16) == 4
