@@ -31,7 +31,7 @@ EXPORTED = [
     "wq_gemv_w4a16", "wq_gemm_tc_w4a16", "wq_dispatch_threshold", "wq_set_dispatch_threshold",
     "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
     "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
-    "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128",
+    "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128", "wq_selftest_wait_timeout",
 ]
 
 _lib = None
@@ -67,6 +67,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_gptq_int4_g128": (I32, [P, I64, I64, P, P, P, P, P]),
         "wq_awq_workspace_bytes": (SZ, [I64, I64, I64]),
         "wq_awq_int4_g128": (I32, [P, I64, I64, P, I64, P, P, P, P, P, P, P, SZ, P]),
+        "wq_selftest_wait_timeout": (I32, [U32, ctypes.POINTER(U32), P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -320,6 +321,14 @@ def dispatch_threshold(fmt, K: int, N: int) -> int:
 
 def set_dispatch_threshold(fmt, K: int, N: int, T: int) -> None:
     _check(load_library().wq_set_dispatch_threshold(_fmt(fmt), K, N, T), "wq_set_dispatch_threshold")
+
+
+def selftest_wait_timeout(limit_us: int = 10000, stream=None) -> int:
+    """Runs the bounded-wait diagnostic; returns 1 when the wait ran out (the expected result)."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().wq_selftest_wait_timeout(limit_us, ctypes.byref(v), _stream(stream)),
+           "wq_selftest_wait_timeout")
+    return int(v.value)
 
 
 def read_error_flags() -> int:

@@ -320,8 +320,18 @@ const char* wq_status_str(wq_status s) {
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
-  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() | wq::gptq_read_and_clear_error();
+  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() | wq::gptq_read_and_clear_error() |
+         wq::selftest_read_and_clear_error();
   return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
+}
+
+wq_status wq_selftest_wait_timeout(uint32_t limit_us, uint32_t* timed_out, void* stream) {
+  if (!timed_out) return WQ_ERR_NULL;
+  if (limit_us < 1 || limit_us > 2000000) return WQ_ERR_ARG;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::run_selftest_wait(static_cast<uint64_t>(limit_us) * 1000ull, timed_out,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 wq_status wq_check_device(void) { return check_device_cached(); }

@@ -18,6 +18,7 @@ enum : uint32_t {
   kErrWaitAccum = 1u << 2,    // epilogue gave up waiting for the accumulator
   kErrWaitReduce = 1u << 3,   // split-K reduction gave up
   kErrDrain = 1u << 4,        // TMA drain at exit gave up
+  kErrSelftestWait = 1u << 5, // the diagnostic wait of wq_selftest_wait_timeout ran out (expected)
 };
 
 // About two seconds of polling, measured on the global nanosecond timer.
@@ -89,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
         atomicOr(err, code);
         return false;
       }
+    }
+  }
+}
+
+// The same bounded wait with the limit given in nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t code,
+                                              uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(err, code);
+      return false;
     }
   }
 }

@@ -71,6 +71,10 @@ cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const flo
                                  uint16_t* scales, uint16_t* zeros, float* s_out, int32_t* a_out, double* losses_out,
                                  void* ws, size_t ws_bytes, cudaStream_t stream);
 
+// selftest.cu -- the bounded-wait path, exercised on demand
+uint32_t selftest_read_and_clear_error();
+cudaError_t run_selftest_wait(uint64_t limit_ns, uint32_t* timed_out_host, cudaStream_t stream);
+
 // layout.cu -- row re-layout of the stacked gate+up weight
 cudaError_t launch_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, cudaStream_t stream);
 

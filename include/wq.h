@@ -281,6 +281,16 @@ const char* wq_status_str(wq_status s);
  */
 wq_status wq_read_error_flags(uint32_t* out);
 
+/*
+ * Diagnostic of the bounded waits every kernel uses: launches one CTA that waits on an
+ * mbarrier phase nothing completes, with a limit of limit_us microseconds (1 .. 2000000).
+ * The wait runs out, records bit 1 << 5 in the error word (see wq_read_error_flags) and the
+ * kernel returns; *timed_out (host) receives 1.  Synchronizes `stream`.  No fault, trap or
+ * endless loop is involved, so the context stays usable.
+ * Errors: WQ_ERR_NULL, WQ_ERR_ARG, WQ_ERR_UNSUPPORTED_ARCH, WQ_ERR_CUDA.
+ */
+wq_status wq_selftest_wait_timeout(uint32_t limit_us, uint32_t* timed_out, void* stream);
+
 /* WQ_OK when the current device is a GB300-class part (compute capability 10.3). */
 wq_status wq_check_device(void);
 

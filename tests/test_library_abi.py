@@ -136,3 +136,10 @@ def test_validation_errors_swiglu_interleave_gptq_awq(lib):
     assert aw(X=ODD) == 3
     assert aw(ws=None) == 4
     assert aw(wsb=16) == 4
+
+
+def test_selftest_argument_checks(lib):
+    v = ctypes.c_uint32(0)
+    assert lib.wq_selftest_wait_timeout(1000, None, None) == 1
+    assert lib.wq_selftest_wait_timeout(0, ctypes.byref(v), None) == 7
+    assert lib.wq_selftest_wait_timeout(2000001, ctypes.byref(v), None) == 7
