@@ -11,8 +11,10 @@
 //       round trip for the dequantized operand.
 //   B = X tile [256 x 64]    -- TMA, 128-byte swizzle, K-major, read by the MMA from smem.
 //   MMA = tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, issued by one thread.
-// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2-5 dequant
-// (then epilogue: tcgen05.ld -> scale -> bf16 -> global).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2-9 dequant in
+// two sets of four (one warp per TMEM lane quarter) that take alternate stages, so one set's
+// tensor-memory stores overlap the other's unpacking; then the epilogue, each set half of the
+// tile's columns (tcgen05.ld -> scale -> bf16 -> global).
 //
 // Operand types.  MXFP4: w_hat = E2M1 * 2^e is exact in bf16, so the MMA runs in bf16 on X
 // as given.  INT4: (q - z) * s needs up to 15 significant bits; rounding it to bf16 (8 bits)
@@ -41,7 +43,8 @@ constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of 16-
 constexpr int kStages = 4;
 constexpr int kXBytes = BM * BK * 2;        // 32 KB
 constexpr int kWBytes = BN * BK / 2;        // 4 KB packed weights
-constexpr int kThreads = 192;               // 6 warps
+constexpr int kDequantSets = 2;             // dequant warp sets, alternating stages
+constexpr int kThreads = 64 + 128 * kDequantSets;   // producer + MMA warp + 4 dequant warps per set
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;                  // D: columns [0, 256)
 constexpr int kACol = 256;                  // A stage s: columns [256 + 32 s, +32)
@@ -267,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- dequant, then epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int set = (warp - 2) >> 2;        // stages set, set + kDequantSets, ... are this set's
     const int r = q * 32 + lane;            // weight row inside the tile == TMEM lane
     const int n = n0 + r;
     const bool row_ok = n < p.N;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     bool ok = true;
-    for (int i = 0; i < KS; ++i) {
+    for (int i = set; i < KS; i += kDequantSets) {
       const int s = i % kStages;
       const uint32_t ph = (i / kStages) & 1;
       uint32_t a[32];
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BM; c += 32) {
+      for (int c = set * (BM / kDequantSets); c < (set + 1) * (BM / kDequantSets); c += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
