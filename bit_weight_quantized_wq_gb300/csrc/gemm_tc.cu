@@ -43,7 +43,7 @@ constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of 16-
 constexpr int kStages = 4;
 constexpr int kXBytes = BM * BK * 2;        // 32 KB
 constexpr int kWBytes = BN * BK / 2;        // 4 KB packed weights
-constexpr int kDequantSets = 2;             // dequant warp sets, alternating stages
+constexpr int kDequantSets = 3;             // dequant warp sets, alternating stages
 constexpr int kThreads = 64 + 128 * kDequantSets;   // producer + MMA warp + 4 dequant warps per set
 constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;                  // D: columns [0, 256)
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = set * (BM / kDequantSets); c < (set + 1) * (BM / kDequantSets); c += 32) {
+      for (int c = 32 * set; c < BM; c += 32 * kDequantSets) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
