@@ -40,7 +40,7 @@ namespace tc {
 constexpr int BN = 128;          // weight rows per tile (MMA M)
 constexpr int BM = 256;          // activation rows per tile (MMA N)
 constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of 16-bit X)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kXBytes = BM * BK * 2;        // 32 KB
 constexpr int kWBytes = BN * BK / 2;        // 4 KB packed weights
 constexpr int kDequantSets = 3;             // dequant warp sets, alternating stages
@@ -49,6 +49,8 @@ constexpr int kTmemCols = 512;
 constexpr int kAccCol = 0;                  // D: columns [0, 256)
 constexpr int kACol = 256;                  // A stage s: columns [256 + 32 s, +32)
 constexpr int kGroupM = 8;                  // tile raster: 8 activation tiles per group
+
+static_assert(kACol + 32 * kStages <= kTmemCols, "the A stages must fit the tensor-memory allocation");
 
 struct Smem {
   uint8_t x[kStages][kXBytes];    // 1024-aligned (SWIZZLE_128B atoms)
@@ -487,6 +489,7 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
                    static_cast<uint64_t>(K / 2), BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
+  static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "tensor-core kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(Smem) + 1024;
   const unsigned grid = static_cast<unsigned>(p.tiles_n) * static_cast<unsigned>(p.tiles_m);
   void (*kern)(CUtensorMap, CUtensorMap, Params) =
