@@ -71,6 +71,7 @@ struct Params {
   int KB;                // MXFP4 scale bytes per row (K / 32)
   int G;                 // INT4 groups per row (K / 128)
   int tiles_n, tiles_m;
+  int full_tiles;        // tiles [0, full_tiles) run whole; each later tile runs as two halves
   int k_stages;          // ceil(K / BK)
 };
 
@@ -143,8 +144,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulate, A/B K-major, M = 128, N = 256.
-__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt /*0 f16, 1 bf16*/) {
-  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((uint32_t(BM) >> 3) << 17) | ((uint32_t(BN) >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulate, A/B both fp16 or both bf16, MMA N = n
+// (activation rows: BM for a whole tile, BM / 2 for a half tile), M = BN.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt /*0 f16, 1 bf16*/, uint32_t n) {
+  return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((n >> 3) << 17) | ((uint32_t(BN) >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -197,9 +200,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + smem_align_pad(smem_raw));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Tiles past full_tiles (the last, partial wave) run as two half tiles of BM / 2 activation
+  // rows on two CTAs, so that wave ends sooner.  A half tile loads the same 256-row activation
+  // box from its own first row and uses the first 128 rows of it.
+  int t = blockIdx.x, half = -1;
+  if (t >= p.full_tiles) {
+    const int j = t - p.full_tiles;
+    t = p.full_tiles + (j >> 1);
+    half = j & 1;
+  }
   int tn, tm;
-  tile_coords(blockIdx.x, p.tiles_n, p.tiles_m, tn, tm);
-  const int n0 = tn * BN, m0 = tm * BM;
+  tile_coords(t, p.tiles_n, p.tiles_m, tn, tm);
+  const int n0 = tn * BN, m0 = tm * BM + (half > 0 ? BM / 2 : 0);
+  const int bm = half >= 0 ? BM / 2 : BM;
   const int KS = p.k_stages;
 
   if (threadIdx.x == 0) {
@@ -244,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u);
+      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u, static_cast<uint32_t>(bm));
       bool ok = true;
       for (int i = 0; i < KS; ++i) {
         const int s = i % kStages;
@@ -351,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 32 * set; c < BM; c += 32 * kDequantSets) {
+      for (int c = 32 * set; c < bm; c += 32 * kDequantSets) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
@@ -491,7 +504,12 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   if (e != cudaSuccess) return e;
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "tensor-core kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(Smem) + 1024;
-  const unsigned grid = static_cast<unsigned>(p.tiles_n) * static_cast<unsigned>(p.tiles_m);
+  // The last, partial wave runs as half tiles when at most half the SMs would hold it.
+  const long long tiles = static_cast<long long>(p.tiles_n) * p.tiles_m;
+  const long long sms = device_sm_count();
+  const long long rem = tiles % sms;
+  p.full_tiles = static_cast<int>((rem > 0 && 2 * rem <= sms) ? tiles - rem : tiles);
+  const unsigned grid = static_cast<unsigned>(p.full_tiles + 2 * (tiles - p.full_tiles));
   void (*kern)(CUtensorMap, CUtensorMap, Params) =
       fmt == kInt4G128 ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu> : k_gemm_tc<kInt4G128, kEpiNone>)
                        : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu> : k_gemm_tc<kMxfp4, kEpiNone>);
