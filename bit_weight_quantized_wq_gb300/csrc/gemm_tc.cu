@@ -60,6 +60,7 @@ struct Smem {
   uint64_t empty[kStages];
   uint64_t accum_full;
   uint32_t tmem_base;
+  int second;            // split tile: this CTA finished second and writes the outputs
 };
 
 struct Params {
@@ -71,8 +72,11 @@ struct Params {
   int KB;                // MXFP4 scale bytes per row (K / 32)
   int G;                 // INT4 groups per row (K / 128)
   int tiles_n, tiles_m;
-  int full_tiles;        // tiles [0, full_tiles) run whole; each later tile runs as two halves
+  int full_tiles;        // tiles [0, full_tiles) run whole; each later tile as two K halves
+  int split_stage;       // first stage of a split tile's second half
   int k_stages;          // ceil(K / BK)
+  uint32_t* cnt;         // split tiles: one counter each (workspace header, left at zero)
+  float* part;           // split tiles: [tile][half][BN][BM] fp32 partial accumulators
 };
 
 // ------------------------------------------------------------------------ tcgen05 helpers
@@ -180,6 +184,29 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
   return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
 }
 
+// Barrier 1 among the dequant / epilogue warps (all warps but the producer and the MMA warp).
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("barrier.sync 1, %0;" ::"n"(kThreads - 64) : "memory");
+}
+// The same barrier, returning whether every one of those threads passed `v`.
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kThreads - 64)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Tile index -> (n tile, m tile), grouped so that a wave of CTAs shares activation tiles
 // (kGroupM of them) and weight tiles in L2.
 __device__ __forceinline__ void tile_coords(int t, int tiles_n, int tiles_m, int& tn, int& tm) {
@@ -200,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw + smem_align_pad(smem_raw));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Tiles past full_tiles (the last, partial wave) run as two half tiles of BM / 2 activation
-  // rows on two CTAs, so that wave ends sooner.  A half tile loads the same 256-row activation
-  // box from its own first row and uses the first 128 rows of it.
+  // Tiles past full_tiles (the last, partial wave) run split along K on two CTAs, stages
+  // [0, split_stage) and [split_stage, k_stages), so that wave ends in about half the time.
+  // Each half stores its fp32 accumulator; the second to finish adds the other's and writes Y.
   int t = blockIdx.x, half = -1;
   if (t >= p.full_tiles) {
     const int j = t - p.full_tiles;
@@ -211,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   int tn, tm;
   tile_coords(t, p.tiles_n, p.tiles_m, tn, tm);
-  const int n0 = tn * BN, m0 = tm * BM + (half > 0 ? BM / 2 : 0);
-  const int bm = half >= 0 ? BM / 2 : BM;
-  const int KS = p.k_stages;
+  const int n0 = tn * BN, m0 = tm * BM;
+  const int kb = half == 1 ? p.split_stage : 0;                     // first stage of this CTA
+  const int KS = (half == 0 ? p.split_stage : p.k_stages) - kb;      // stages this CTA runs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -246,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (i / kStages) & 1;
         if (!mbar_wait(&sm.empty[s], ph ^ 1, &g_gemm_err, kErrWaitEmpty)) break;
         mbar_arrive_expect_tx(&sm.full[s], kXBytes + kWBytes);
-        tma_load_2d(&sm.x[s][0], &tmap_x, i * BK, m0, &sm.full[s], pol_x);
-        tma_load_2d(&sm.w[s][0], &tmap_w, i * (BK / 2), n0, &sm.full[s], pol_w);
+        tma_load_2d(&sm.x[s][0], &tmap_x, (kb + i) * BK, m0, &sm.full[s], pol_x);
+        tma_load_2d(&sm.w[s][0], &tmap_w, (kb + i) * (BK / 2), n0, &sm.full[s], pol_w);
       }
       for (int j = i - kStages; j < i; ++j) {  // drain: the last fill of each slot landed
         if (j < 0) continue;
@@ -257,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u, static_cast<uint32_t>(bm));
+      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u, static_cast<uint32_t>(BM));
       bool ok = true;
       for (int i = 0; i < KS; ++i) {
         const int s = i % kStages;
@@ -298,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // metadata of this stage (loaded before the waits)
       uint32_t s2 = 0, zz = 0;          // INT4: f16x2 scale, f16x2 (1024 + z)
       uint32_t e2 = 0;                  // MXFP4: two E8M0 bytes
-      const int k0 = i * BK;
+      const int k0 = (kb + i) * BK;
       if constexpr (FMT == kInt4G128) {
         const int g = k0 / 128;
         uint16_t sb = 0, zb = 0;
@@ -361,13 +388,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.a_ready[s]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum)) {
+    // The dequant threads agree first that none of them timed out, so the barriers below are
+    // reached by all of them or by none.
+    const bool ready = ok && mbar_wait(&sm.accum_full, 0, &g_gemm_err, kErrWaitAccum);
+    if (epi_bar_and(ready)) {
       tc_fence_after();
+      bool write_y = true;
+      const float* other = nullptr;
+      if (half >= 0) {
+        // this half's accumulator to its slot; then one GPU-scope counter update per CTA
+        // (release: after the barrier, covers every thread's stores) tells the second CTA to
+        // finish the tile
+        const long long slot = static_cast<long long>(t - p.full_tiles) * 2;
+        float* mine = p.part + (slot + half) * (BN * BM) + static_cast<long long>(r) * BM;
 #pragma unroll 1
-      for (int c = 32 * set; c < bm; c += 32 * kDequantSets) {
+        for (int c = 32 * set; c < BM; c += 32 * kDequantSets) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kAccCol + c, v);
+          tc_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(mine + c);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            __stcg(dst + u, make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                                        __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
+        }
+        epi_bar();
+        if (threadIdx.x == 64) {
+          uint32_t* c = p.cnt + (t - p.full_tiles);
+          const uint32_t old = atom_add_acq_rel_gpu(c, 1u);
+          sm.second = old == 1u ? 1 : 0;
+          if (old == 1u) atomicExch(c, 0u);   // ready for the next call
+        }
+        epi_bar();
+        write_y = sm.second != 0;
+        if (write_y) {
+          __threadfence();
+          other = p.part + (slot + (1 - half)) * (BN * BM) + static_cast<long long>(r) * BM;
+        }
+      }
+#pragma unroll 1
+      for (int c = 32 * set; c < BM && write_y; c += 32 * kDequantSets) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
+        if (other) {
+          // the two halves' sum: a two-term fp32 sum, the same whichever half finished first
+          const float4* src = reinterpret_cast<const float4*>(other + c);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 o = __ldcg(src + u);
+            v[4 * u + 0] = __float_as_uint(__uint_as_float(v[4 * u + 0]) + o.x);
+            v[4 * u + 1] = __float_as_uint(__uint_as_float(v[4 * u + 1]) + o.y);
+            v[4 * u + 2] = __float_as_uint(__uint_as_float(v[4 * u + 2]) + o.z);
+            v[4 * u + 3] = __float_as_uint(__uint_as_float(v[4 * u + 3]) + o.w);
+          }
+        }
         if constexpr (EPI == kEpiSwiglu) {
           // Gate row n (lane bit 3 clear) and its up row n + 8 sit in lanes l and l ^ 8 of
           // this warp.  Per pair of accumulator columns (j, j + 1) one shuffle gives the gate
@@ -456,11 +531,29 @@ __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X
 
 }  // namespace tc
 
+namespace {
+
+// Tiles of the last, partial wave that run split along K (0: none): when that wave fits in
+// half the SMs and a tile has at least two stages.
+long long split_tiles(int64_t M, int64_t K, int64_t N) {
+  using namespace tc;
+  const long long tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  const long long sms = device_sm_count();
+  const long long rem = tiles % sms;
+  const long long ks = (K + BK - 1) / BK;
+  return (rem > 0 && 2 * rem <= sms && ks >= 2) ? rem : 0;
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
-  (void)N;
-  if (fmt != kInt4G128) return 0;
-  const size_t xh = ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256;
-  return kWsCounterBytes + xh + ((static_cast<size_t>(M) * 4 + 255) / 256) * 256;
+  using namespace tc;
+  const size_t part = static_cast<size_t>(split_tiles(M, K, N)) * 2 * BN * BM * sizeof(float);
+  if (fmt != kInt4G128) return part ? kWsCounterBytes + part : 0;
+  const size_t xh = round256(static_cast<size_t>(M) * K * 2);
+  return kWsCounterBytes + xh + round256(static_cast<size_t>(M) * 4) + part;
 }
 
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -482,6 +575,17 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   p.tiles_m = static_cast<int>((M + BM - 1) / BM);
   p.k_stages = static_cast<int>((K + BK - 1) / BK);
 
+  const long long nsplit = split_tiles(M, K, N);
+  const long long tiles = static_cast<long long>(p.tiles_n) * p.tiles_m;
+  p.full_tiles = static_cast<int>(tiles - nsplit);
+  p.split_stage = p.k_stages / 2;
+  p.cnt = reinterpret_cast<uint32_t*>(ws);
+  p.part = nullptr;
+  if (nsplit) {
+    size_t off = kWsCounterBytes;
+    if (fmt == kInt4G128) off += round256(static_cast<size_t>(M) * K * 2) + round256(static_cast<size_t>(M) * 4);
+    p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + off);
+  }
   const void* xsrc = X;
   if (fmt == kInt4G128) {
     uint8_t* base = reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes;  // never touch the counter header
@@ -504,12 +608,7 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   if (e != cudaSuccess) return e;
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "tensor-core kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(Smem) + 1024;
-  // The last, partial wave runs as half tiles when at most half the SMs would hold it.
-  const long long tiles = static_cast<long long>(p.tiles_n) * p.tiles_m;
-  const long long sms = device_sm_count();
-  const long long rem = tiles % sms;
-  p.full_tiles = static_cast<int>((rem > 0 && 2 * rem <= sms) ? tiles - rem : tiles);
-  const unsigned grid = static_cast<unsigned>(p.full_tiles + 2 * (tiles - p.full_tiles));
+  const unsigned grid = static_cast<unsigned>(p.full_tiles + 2 * nsplit);
   void (*kern)(CUtensorMap, CUtensorMap, Params) =
       fmt == kInt4G128 ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu> : k_gemm_tc<kInt4G128, kEpiNone>)
                        : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu> : k_gemm_tc<kMxfp4, kEpiNone>);
