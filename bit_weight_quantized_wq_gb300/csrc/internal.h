@@ -27,9 +27,10 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void
 
 int device_sm_count();
 
-// Every workspace layout starts with this fixed header of split-K counters.  Only the
-// decode kernel touches it and every call leaves it at zero, so one workspace zeroed once
-// can be shared by calls of any shape and by both kernels.
+// Every workspace layout starts with this fixed header of split-K counters (the decode
+// kernel's bands, the tensor-core kernel's split last-wave tiles).  Every call that completes
+// leaves it at zero, so one workspace zeroed once can be shared by calls of any shape and by
+// both kernels.
 constexpr size_t kWsCounterBytes = 64 * 1024;
 constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
 // Weight rows per split-K band of the decode kernel: N <= kWsMaxCounters * kDecodeBand.

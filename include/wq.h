@@ -144,11 +144,14 @@ wq_status wq_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X,
 
 /*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
- * Every layout starts with the same 64 KiB header of split-K counters.  Zero the
- * workspace once before its first use; every call that completes leaves the header at zero
- * again, so one workspace can serve calls of any shape and either kernel.  One workspace
- * must not be used by two calls that can run at the same time.  Returns 0 for invalid
- * arguments.
+ * Every layout starts with the same 64 KiB header of split-K counters (used by the decode
+ * kernel, and by the tensor-core kernel when it splits the tiles of a last, partial wave
+ * along K; the size depends on the device's SM count, so query it on the device that runs
+ * the call).  Zero the workspace once before its first use; every call that completes leaves
+ * the header at zero again, so one workspace can serve calls of any shape and either kernel
+ * (after a call that reported a timed-out wait, zero it again).  One workspace must not be
+ * used by two calls that can run at the same time.  Returns 0 for invalid arguments, and 0
+ * when the shape needs no workspace.
  */
 size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N);
 
