@@ -13,10 +13,11 @@
 // Rows are independent: one CTA owns R rows and keeps their current values on chip for the
 // whole sweep -- the pages' lazy block update exists to avoid re-streaming W, which on-chip
 // residency avoids altogether.  Two kernels:
-//   K <= 16384  registers: thread t owns columns t + 512 k; the owner of column i takes its
-//               decisions, publishes e_i through shared memory (double-buffered, one barrier
+//   K <= 16384  registers: thread t owns columns t + 512 k; the warp of the owner of column i
+//               takes its decisions (lane r for row r, the owner's values broadcast by
+//               shuffle), publishes e_i through shared memory (double-buffered, one barrier
 //               per column) and every thread updates its own later columns with row i of U,
-//               which a bulk async copy brought into shared memory four columns ahead.
+//               which a bulk async copy brought into shared memory two to four columns ahead.
 //   larger K    shared memory: the rows' values live in shared memory; R threads decide, all
 //               threads update, two barriers per column.
 #include "internal.h"
@@ -219,39 +220,44 @@ __global__ void __launch_bounds__(kRegThreads, 1)
         }
       }
       __syncthreads();
-      if (t == owner) {
-        // every row slot, padding rows included (their values are 0: s = 1, z = 0), so the
-        // rows' independent chains can interleave; only real rows are stored
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float lo = fminf(fminf(s_lo[0][r], s_lo[1][r]), fminf(s_lo[2][r], s_lo[3][r]));
-          const float hi = fmaxf(fmaxf(s_hi[0][r], s_hi[1][r]), fmaxf(s_hi[2][r], s_hi[3][r]));
-          __half s16;
-          float sc;
-          int z;
-          group_params(lo, hi, s16, sc, z);
-          s_scale[r] = sc;
-          s_zero[r] = static_cast<float>(z);
-          if (r < rows) {
-            const long long gi = static_cast<long long>(row0 + r) * G + (i >> 7);
-            scales[gi] = s16;
-            zeros[gi] = __int2half_rn(z);
-          }
+      if (warp == (owner >> 5) && lane < R) {
+        // lane r of the owner's warp: row r's parameters (padding rows too: their values are
+        // 0, so s = 1 and z = 0; only real rows are stored)
+        const int r = lane;
+        const float lo = fminf(fminf(s_lo[0][r], s_lo[1][r]), fminf(s_lo[2][r], s_lo[3][r]));
+        const float hi = fmaxf(fmaxf(s_hi[0][r], s_hi[1][r]), fmaxf(s_hi[2][r], s_hi[3][r]));
+        __half s16;
+        float sc;
+        int z;
+        group_params(lo, hi, s16, sc, z);
+        s_scale[r] = sc;
+        s_zero[r] = static_cast<float>(z);
+        if (r < rows) {
+          const long long gi = static_cast<long long>(row0 + r) * G + (i >> 7);
+          scales[gi] = s16;
+          zeros[gi] = __int2half_rn(z);
         }
       }
     }
     // row i of U has landed (every thread waits: all of them read it below)
     bad = !mbar_wait(&full[i % D], (i / D) & 1, &g_gptq_err, kErrGptqWait);
-    if (t == owner && !bad) {
-      const float d = ui[i];   // U[i, i]
+    if (warp == (owner >> 5)) {
+      // The owner's warp decides column i: every lane picks its slot values in step, the
+      // owner lane's R values are broadcast, and lane r takes row r's decision.
+      const int ol = owner & 31;
+      float xr = 0.f;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {   // padding rows too (value 0, error 0)
-        const float x = pick<NJ>(v[r], ki);
-        const float sc = s_scale[r], zf = s_zero[r];
-        float q = __fadd_rn(rintf(__fdiv_rn(x, sc)), zf);
+      for (int r = 0; r < R; ++r) {
+        const float x = __shfl_sync(0xffffffffu, pick<NJ>(v[r], ki), ol);
+        if (lane == r) xr = x;
+      }
+      if (lane < R && !bad) {   // padding rows too (value 0, error 0)
+        const float d = ui[i];   // U[i, i]
+        const float sc = s_scale[lane], zf = s_zero[lane];
+        float q = __fadd_rn(rintf(__fdiv_rn(xr, sc)), zf);
         q = fminf(fmaxf(q, 0.f), 15.f);
-        code[static_cast<size_t>(r) * K + i] = static_cast<uint8_t>(q);
-        s_err[i & 1][r] = __fdiv_rn(__fsub_rn(x, __fmul_rn(__fsub_rn(q, zf), sc)), d);
+        code[static_cast<size_t>(lane) * K + i] = static_cast<uint8_t>(q);
+        s_err[i & 1][lane] = __fdiv_rn(__fsub_rn(xr, __fmul_rn(__fsub_rn(q, zf), sc)), d);
       }
     }
     // one barrier per column; a timed-out wait anywhere stops every thread here together
