@@ -15,7 +15,7 @@ Sources
   quantization with a zero block mapped to scale 1 and Python ``round``
   (ties to even); invalid geometry raises ``ValueError``.
 
-Readings taken where the pages are silent (each listed in the design doc):
+Readings taken where the pages are silent:
 * R1 the asymmetric range always contains 0 (``x_min <= 0 <= x_max``);
 * R2 a zero range uses scale 1 (the lesson's zero-block rule);
 * R4 ``round`` is round-half-to-even (Python ``round`` / ``torch.round``).
