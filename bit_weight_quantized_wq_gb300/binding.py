@@ -224,32 +224,63 @@ def _workspace_for(device, nbytes, workspace):
     return ws.get(nbytes)
 
 
+_fns = {}
+_BF16, _F16, _I32, _U8 = torch.bfloat16, torch.float16, torch.int32, torch.uint8
+
+
+def _fn(cname: str):
+    f = _fns.get(cname)
+    if f is None:
+        f = _fns[cname] = getattr(load_library(), cname)
+    return f
+
+
 def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
-    f = _fmt(fmt)
-    _need(X, torch.bfloat16, "X")
-    _need(Wq, torch.int32, "Wq")
-    if f == FMT_INT4_G128:
-        _need(scales, torch.float16, "scales")
-        _need(zeros, torch.float16, "zeros")
-    else:
-        _need(scales, torch.uint8, "scales")
-        if zeros is not None:
-            raise ValueError("zeros must be None for MXFP4")
+    # Marshalling for every layer call, kept lean: a decode layer runs in ~10 us, so the host
+    # side of the call must not be the slower one.  Types, devices and contiguity are checked
+    # here (the library sees raw pointers); shapes, alignment and the workspace size in C.
+    f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
+    int4 = f == FMT_INT4_G128
+    if (X.dtype is not _BF16 or Wq.dtype is not _I32 or scales.dtype is not (_F16 if int4 else _U8)
+            or (zeros is not None and (not int4 or zeros.dtype is not _F16)) or (int4 and zeros is None)):
+        _linear_explain(f, X, Wq, scales, zeros)
+    if not (X.is_cuda and Wq.is_cuda and scales.is_cuda and X.is_contiguous() and Wq.is_contiguous()
+            and scales.is_contiguous() and (zeros is None or (zeros.is_cuda and zeros.is_contiguous()))):
+        _linear_explain(f, X, Wq, scales, zeros)
     M, K = X.shape
     N = Wq.shape[0]
     if Wq.shape[1] * 8 != K:
         raise ValueError("Wq must be [N, K/8]")
+    dev = X.device
     if out is None:
-        out = torch.empty((M, N // 2 if swiglu else N), dtype=torch.bfloat16, device=X.device)
-    else:
-        _need(out, torch.bfloat16, "out")
+        out = torch.empty((M, N // 2 if swiglu else N), dtype=_BF16, device=dev)
+    elif out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
+        _need(out, _BF16, "out")
     # a caller's workspace is checked by the library itself (WQ_ERR_WORKSPACE when too small)
-    ws = workspace if workspace is not None else _workspace_for(X.device, gemm_workspace_bytes(f, M, K, N), None)
+    ws = workspace if workspace is not None else _workspace_for(dev, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
-    fn = getattr(load_library(), cname)
-    _check(fn(f, X.data_ptr(), M, K, N // 2 if swiglu else N, Wq.data_ptr(), scales.data_ptr(), _ptr(zeros), out.data_ptr(), _ptr(ws),
-              ws_bytes, _stream(stream, X.device)), cname)
+    st = _fn(cname)(f, X.data_ptr(), M, K, N // 2 if swiglu else N, Wq.data_ptr(), scales.data_ptr(),
+                    None if zeros is None else zeros.data_ptr(), out.data_ptr(),
+                    None if ws is None else ws.data_ptr(), ws_bytes, _stream(stream, dev))
+    if st:
+        _check(st, cname)
     return out
+
+
+def _linear_explain(f, X, Wq, scales, zeros):
+    """Raises the precise error for a call that failed the fast type/device checks."""
+    _need(X, _BF16, "X")
+    _need(Wq, _I32, "Wq")
+    if f == FMT_INT4_G128:
+        _need(scales, _F16, "scales")
+        if zeros is None:
+            raise ValueError("zeros is required for INT4 g128")
+        _need(zeros, _F16, "zeros")
+    else:
+        _need(scales, _U8, "scales")
+        if zeros is not None:
+            raise ValueError("zeros must be None for MXFP4")
+    raise ValueError("invalid arguments")
 
 
 def gemm_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
