@@ -235,11 +235,10 @@ def _fn(cname: str):
     return f
 
 
-def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
-    # Marshalling for every layer call, kept lean: a decode layer runs in ~10 us, so the host
-    # side of the call must not be the slower one.  Types, devices and contiguity are checked
-    # here (the library sees raw pointers); shapes, alignment and the workspace size in C.
-    f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
+def _prepare(f, X, Wq, scales, zeros, out, swiglu):
+    """The checks every layer call makes before its pointers reach the library, which sees
+    only raw addresses and sizes: dtypes, devices, contiguity, and the shapes of Wq, scales,
+    zeros and out against (M, K, N).  Returns (M, K, N, out), allocating out when None."""
     int4 = f == FMT_INT4_G128
     if (X.dtype is not _BF16 or Wq.dtype is not _I32 or scales.dtype is not (_F16 if int4 else _U8)
             or (zeros is not None and (not int4 or zeros.dtype is not _F16)) or (int4 and zeros is None)):
@@ -247,16 +246,40 @@ def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swigl
     if not (X.is_cuda and Wq.is_cuda and scales.is_cuda and X.is_contiguous() and Wq.is_contiguous()
             and scales.is_contiguous() and (zeros is None or (zeros.is_cuda and zeros.is_contiguous()))):
         _linear_explain(f, X, Wq, scales, zeros)
+    if X.dim() != 2 or Wq.dim() != 2:
+        raise ValueError("X must be [M, K] and Wq [N, K/8]")
     M, K = X.shape
     N = Wq.shape[0]
     if Wq.shape[1] * 8 != K:
         raise ValueError("Wq must be [N, K/8]")
+    meta = (N, K // 128) if int4 else (N, K // 32)
+    if scales.shape != meta or (zeros is not None and zeros.shape != meta):
+        raise ValueError("scales%s must be [N, K/%d]" % (" and zeros" if int4 else "", 128 if int4 else 32))
     dev = X.device
+    if Wq.device != dev or scales.device != dev or (zeros is not None and zeros.device != dev):
+        raise ValueError("X, Wq, scales and zeros must be on the same device")
+    ncol = N // 2 if swiglu else N
     if out is None:
-        out = torch.empty((M, N // 2 if swiglu else N), dtype=_BF16, device=dev)
-    elif out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
-        _need(out, _BF16, "out")
+        out = torch.empty((M, ncol), dtype=_BF16, device=dev)
+    else:
+        if out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
+            _need(out, _BF16, "out")
+        if out.shape != (M, ncol) or out.device != dev:
+            raise ValueError("out must be [M, %s] on X's device" % ("N/2" if swiglu else "N"))
+    return M, K, N, out
+
+
+def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
+    # Marshalling for every layer call, kept lean: a decode layer runs in a few microseconds,
+    # so the host side of the call must not be the slower one.  Types, devices, contiguity and
+    # shapes are checked here (the library sees raw pointers); alignment, size limits and the
+    # workspace size in C.
+    f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
+    M, K, N, out = _prepare(f, X, Wq, scales, zeros, out, swiglu)
+    dev = X.device
     # a caller's workspace is checked by the library itself (WQ_ERR_WORKSPACE when too small)
+    if workspace is not None and (not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on X's device")
     ws = workspace if workspace is not None else _workspace_for(dev, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     st = _fn(cname)(f, X.data_ptr(), M, K, N // 2 if swiglu else N, Wq.data_ptr(), scales.data_ptr(),
@@ -334,15 +357,15 @@ def interleave_gate_up(src: torch.Tensor, out=None, stream=None):
 
 def gemv_w4a16_noalloc(fmt, X, Wq, scales, zeros=None, out=None, stream=None):
     """The decode kernel with the library's own fixed scratch: no workspace, no allocation
-    inside the library (``out`` is allocated here with torch when it is not given)."""
-    f = _fmt(fmt)
-    _need(X, torch.bfloat16, "X")
-    M, K = X.shape
-    N = Wq.shape[0]
-    if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
-    _check(load_library().wq_gemv_w4a16_noalloc(f, _ptr(X), M, K, N, _ptr(Wq), _ptr(scales), _ptr(zeros),
-                                                _ptr(out), _stream(stream, X.device)), "wq_gemv_w4a16_noalloc")
+    inside the library (``out`` is allocated here with torch when it is not given).  Same
+    argument checks as ``gemv_w4a16``."""
+    f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
+    M, K, N, out = _prepare(f, X, Wq, scales, zeros, out, False)
+    st = _fn("wq_gemv_w4a16_noalloc")(f, X.data_ptr(), M, K, N, Wq.data_ptr(), scales.data_ptr(),
+                                       None if zeros is None else zeros.data_ptr(), out.data_ptr(),
+                                       _stream(stream, X.device))
+    if st:
+        _check(st, "wq_gemv_w4a16_noalloc")
     return out
 
 

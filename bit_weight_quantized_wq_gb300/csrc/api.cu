@@ -1,5 +1,6 @@
 // The C ABI (include/wq.h): argument validation, per-shape dispatch, TMA descriptor
 // encoding, status strings and the device error word.
+#include <atomic>
 #include <mutex>
 
 #include "../../include/wq.h"
@@ -43,15 +44,58 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+CUcontext current_context() {
+  using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
 int device_sm_count() {
-  static int cached[64] = {0};
+  // per-device cache; atomics because several host threads may make their first call at once
+  static std::atomic<int> cached[64];
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   if (n <= 0) return 1;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+cudaError_t set_smem_attr_once(const void* kern, size_t smem_bytes) {
+  // (kernel, device) pairs whose dynamic shared-memory limit is already raised; guarded by a
+  // mutex because several host threads may make their first call at once
+  static std::mutex mu;
+  static const void* done_kern[256];
+  static int done_dev[256];
+  static int n_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done_kern[i] == kern && done_dev[i] == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes));
+  if (e != cudaSuccess) return e;
+  if (n_done < 256) {
+    done_kern[n_done] = kern;
+    done_dev[n_done] = dev;
+    ++n_done;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace wq
@@ -72,16 +116,19 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 wq_status check_device_cached() {
   // Compute capability 10.3 (GB300) only: the kernels use sm_103a-specific instructions.
-  static int ok_dev[64] = {0};  // 0 unknown, 1 ok, 2 bad
+  static std::atomic<int> ok_dev[64];  // 0 unknown, 1 ok, 2 bad (atomic: concurrent first calls)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return WQ_ERR_CUDA;
-  if (dev >= 0 && dev < 64 && ok_dev[dev]) return ok_dev[dev] == 1 ? WQ_OK : WQ_ERR_UNSUPPORTED_ARCH;
+  if (dev >= 0 && dev < 64) {
+    const int k = ok_dev[dev].load(std::memory_order_relaxed);
+    if (k) return k == 1 ? WQ_OK : WQ_ERR_UNSUPPORTED_ARCH;
+  }
   int maj = 0, min = 0;
   if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return WQ_ERR_CUDA;
   const bool ok = (maj == 10 && min == 3);
-  if (dev >= 0 && dev < 64) ok_dev[dev] = ok ? 1 : 2;
+  if (dev >= 0 && dev < 64) ok_dev[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok ? WQ_OK : WQ_ERR_UNSUPPORTED_ARCH;
 }
 

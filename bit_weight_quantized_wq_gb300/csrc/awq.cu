@@ -95,12 +95,8 @@ __global__ void __launch_bounds__(256) k_awq_quant(const float* __restrict__ W, 
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-  __half s16 = __float2half_rn(s32);
-  if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
-  const float sc = __half2float(s16);
-  const int z = __float2int_rn(__fdiv_rn(-lo, sc));
-  const float zf = static_cast<float>(z);
+  float sc, zf;
+  const __half s16 = int4_group_params(lo, hi, sc, zf);
 
   uint32_t w0 = 0u, w1 = 0u;
   float d[16];
@@ -123,7 +119,7 @@ __global__ void __launch_bounds__(256) k_awq_quant(const float* __restrict__ W, 
     reinterpret_cast<uint2*>(Wq + g * 16)[sub] = make_uint2(w0, w1);
     if (sub == 0) {
       scales[g] = s16;
-      zeros[g] = __int2half_rn(z);
+      zeros[g] = __float2half_rn(zf);
     }
   }
 }

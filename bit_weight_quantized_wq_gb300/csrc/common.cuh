@@ -181,6 +181,39 @@ __device__ __forceinline__ bool elect_one() {
 // Loads through L2 only (data written by other CTAs of the same kernel).
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
+// Power-of-two exponent k that carries bf16 values into fp16 exactly: given mx, the largest
+// |x| of a row (or tile) as a bf16 bit pattern without its sign, x * 2^-k is computed for every
+// x of the row.  k = max(floor(log2 mx) - 14, -109) puts the largest value in [2^14, 2^15) when
+// it can (no overflow: fp16's largest finite value is below 2^16) and scales small rows UP as
+// well as large ones down.  Every bf16 value within 2^31 of the row's largest (normal fp16
+// results keep all 8 significant bits), and every bf16 value at all when k = -109 (the scaled
+// values are multiples of 2^-24, fp16's subnormal spacing), converts exactly.  Non-finite rows
+// use k = 0.  Both 2^k and 2^-k are normal floats for k in [-109, 113].
+__device__ __forceinline__ int bf16_to_f16_exponent(uint32_t mx) {
+  if (mx >= 0x7f80u) return 0;
+  const int ex = static_cast<int>(mx >> 7) - 127;   // floor(log2 mx); -127 for 0 and subnormals
+  return max(ex - 14, -109);
+}
+// 2^k as a float for k in [-126, 127] (normal range only).
+__device__ __forceinline__ float pow2_normal(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
+
+// INT4 g128 group parameters from a group's range [lo, hi] (lo <= 0 <= hi), float32 with each
+// operation rounded on its own (推理优化与量化算子深度技术调研 §1.2, 第 1 章：推理加速全景 §4.1):
+//   s32 = (hi - lo) / 15;  s = fp16_rn(min(s32, 65504)), and 1 when that is 0;
+//   z = min(rint(-lo / s), 15).
+// The min on s32 saturates the stored scale at the largest finite fp16 value instead of
+// letting it round to +inf (a group range above 15 * 65504); the min on z keeps the zero point
+// a code (it exceeds 15 only when the stored scale is far below s32: an fp16-subnormal or a
+// saturated scale).  Returns the stored scale, its float value and z as a float.
+__device__ __forceinline__ __half int4_group_params(float lo, float hi, float& s, float& zf) {
+  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
+  __half s16 = __float2half_rn(fminf(s32, 65504.0f));
+  if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
+  s = __half2float(s16);
+  zf = fminf(rintf(__fdiv_rn(-lo, s)), 15.0f);
+  return s16;
+}
+
 // SiLU(g) = g * sigmoid(g) = g / (1 + e^-g), fp32, with the CUDA fast exponential and fast
 // divide intrinsics (a few ulp: far inside the bf16 rounding of the result).  For g << 0 the
 // denominator is huge or +inf and the quotient is 0, the function's limit.

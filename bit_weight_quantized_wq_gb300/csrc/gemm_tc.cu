@@ -11,17 +11,17 @@
 //       round trip for the dequantized operand.
 //   B = X tile [256 x 64]    -- TMA, 128-byte swizzle, K-major, read by the MMA from smem.
 //   MMA = tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, issued by one thread.
-// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2-9 dequant in
-// two sets of four (one warp per TMEM lane quarter) that take alternate stages, so one set's
-// tensor-memory stores overlap the other's unpacking; then the epilogue, each set half of the
-// tile's columns (tcgen05.ld -> scale -> bf16 -> global).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer, warps 2-13 dequant in
+// three sets of four (one warp per TMEM lane quarter) that take stages in turn, so one set's
+// tensor-memory stores overlap the others' unpacking; then the epilogue, each set a third of
+// the tile's columns in interleaved 32-column chunks (tcgen05.ld -> scale -> bf16 -> global).
 //
 // Operand types.  MXFP4: w_hat = E2M1 * 2^e is exact in bf16, so the MMA runs in bf16 on X
 // as given.  INT4: (q - z) * s needs up to 15 significant bits; rounding it to bf16 (8 bits)
 // would put the layer outside 1e-2 (1 + |y|) of the float64 result at K = 4096..29568, so
 // the MMA runs in fp16 (11 bits): a pre-pass converts X exactly to fp16, each row scaled by a
-// power of two 2^-k_m chosen so that |x| 2^-k_m < 2^15 (k_m = 0 for ordinary activations),
-// and the epilogue multiplies row m of Y by 2^k_m.
+// power of two 2^-k_m that puts its largest |x| in [2^14, 2^15) (down for large rows, up for
+// small ones), and the epilogue multiplies row m of Y by 2^k_m.
 #include "internal.h"
 
 namespace wq {
@@ -488,9 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// X (bf16) -> fp16 with a per-row power-of-two scale: |x| 2^-k < 2^15, k >= 0; writes
-// xs[m] = 2^k.  One CTA per row; the row is read twice (max, then convert), the second
-// time from L2.
+// X (bf16) -> fp16 with a per-row power-of-two scale 2^-k (bf16_to_f16_exponent: |x| 2^-k <
+// 2^15, small rows scaled up so that their values stay out of fp16's subnormal range); writes
+// xs[m] = 2^k.  One CTA per row; the row is read twice (max, then convert), the second time
+// from L2.
 __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X, int K, uint16_t* __restrict__ Xh,
                                                   float* __restrict__ xs) {
   const int m = blockIdx.x;
@@ -512,9 +513,8 @@ __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X
   mx = 0u;
 #pragma unroll
   for (int w = 0; w < 8; ++w) mx = max(mx, red[w]);
-  const int ex = static_cast<int>(mx >> 7) - 127;
-  const int k = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+  const int k = bf16_to_f16_exponent(mx);
+  const float inv = pow2_normal(-k);
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
     const uint4 r = __ldg(row + v);
     const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X
     }
     out[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  if (threadIdx.x == 0) xs[m] = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+  if (threadIdx.x == 0) xs[m] = pow2_normal(k);
 }
 
 }  // namespace tc
@@ -612,15 +612,8 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   void (*kern)(CUtensorMap, CUtensorMap, Params) =
       fmt == kInt4G128 ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu> : k_gemm_tc<kInt4G128, kEpiNone>)
                        : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu> : k_gemm_tc<kMxfp4, kEpiNone>);
-  static bool attr_set[4][64] = {{false}};  // once per (kernel, device)
-  int dev = 0;
-  cudaGetDevice(&dev);
-  const int fi = (fmt == kInt4G128 ? 0 : 1) + (epi == kEpiSwiglu ? 2 : 0);
-  if (dev < 0 || dev >= 64 || !attr_set[fi][dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[fi][dev] = true;
-  }
+  e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(tx, tw, p);
   return cudaGetLastError();
 }

@@ -486,9 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r)
           cur[r] = (r < mlive) ? xs4[(8 * nt + r) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
-        // MXFP4: one power-of-two scale 2^-k per stage and 8-row tile keeps every operand inside
-        // fp16 (|x| 2^-k < 2^15, k >= 0); values below 2^-29 of the tile's largest lose bits only
-        // as fp16 subnormals.  max |x| over the tile: bf16 magnitudes order like integers.
+        // MXFP4: one power-of-two scale 2^-k per stage and 8-row tile carries every operand into
+        // fp16 exactly (bf16_to_f16_exponent: the largest in [2^14, 2^15), small tiles scaled up);
+        // only values more than 2^31 below the tile's largest lose bits, as fp16 subnormals.
+        // max |x| over the tile: bf16 magnitudes order like integers.
         float inv = 1.f, xf = 1.f;
         if constexpr (FMT != kInt4G128) {
           uint32_t mx2 = 0u;   // per 16-bit half
@@ -501,10 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t mx = max(mx2 & 0xffffu, mx2 >> 16);
 #pragma unroll
           for (int sh = 1; sh < 32; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-          const int ex = static_cast<int>(mx >> 7) - 127;        // floor(log2 max) for normals
-          const int kk = (mx >= 0x7f80u) ? 0 : max(0, ex - 14);  // inf/nan: no scaling
-          inv = __uint_as_float(static_cast<uint32_t>(127 - kk) << 23);
-          xf = __uint_as_float(static_cast<uint32_t>(127 + kk) << 23);
+          const int kk = bf16_to_f16_exponent(mx);
+          inv = pow2_normal(-kk);
+          xf = pow2_normal(kk);
           if (lane < 8) sm.xf[slot][8 * nt + lane] = xf;
         }
 #pragma unroll
@@ -865,14 +865,8 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT, EPI>;
-  static bool attr_set[64] = {false};  // once per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+  cudaError_t ea = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
+  if (ea != cudaSuccess) return ea;
   // Programmatic stream serialization: the CTAs may launch while the previous kernel of the
   // stream is still running; the kernel itself waits (griddepcontrol.wait) before it reads
   // anything that kernel may have written.
@@ -988,10 +982,13 @@ size_t gemv_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
 cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                                 const void* scales, const uint16_t* zeros, uint16_t* Y, cudaStream_t stream) {
-  // Set-up, once per device with that device current: the array's name is only a host-side
-  // handle, so the kernel gets the device address from cudaGetSymbolAddress.
+  // Set-up, once per device (and again if the device's context was replaced, e.g. after a
+  // cudaDeviceReset, which unloads the module and can move the array), with that device
+  // current: the array's name is only a host-side handle, so the kernel gets the device
+  // address from cudaGetSymbolAddress.
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static CUcontext addr_ctx[64] = {nullptr};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -999,11 +996,12 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || current_context() != addr_ctx[dev]) {
       void* a = nullptr;
       e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
       if (e != cudaSuccess) return e;
       addr[dev] = a;
+      addr_ctx[dev] = current_context();   // current now: the lookup initialised it
     }
     scratch = addr[dev];
   }

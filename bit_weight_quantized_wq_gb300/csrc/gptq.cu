@@ -80,16 +80,13 @@ __global__ void __launch_bounds__(kGptqThreads, 1)
           hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
         if (lane == 0) {
-          const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-          __half s16 = __float2half_rn(s32);
-          if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
-          const float s = __half2float(s16);
-          const int z = __float2int_rn(__fdiv_rn(-lo, s));
+          float s, zf;
+          const __half s16 = int4_group_params(lo, hi, s, zf);
           s_scale[warp] = s;
-          s_zero[warp] = static_cast<float>(z);
+          s_zero[warp] = zf;
           const long long gi = static_cast<long long>(row0 + warp) * G + (i >> 7);
           scales[gi] = s16;
-          zeros[gi] = __int2half_rn(z);
+          zeros[gi] = __float2half_rn(zf);
         }
       }
       __syncthreads();
@@ -129,15 +126,6 @@ __global__ void __launch_bounds__(kGptqThreads, 1)
   }
 }
 
-// INT4 g128 group parameters from a group's range [lo, hi] (lo <= 0 <= hi), the rules of the
-// quantize kernel: s = fp16(rn((hi - lo) / 15)) (0 -> 1), z = rint(-lo / s).
-__device__ __forceinline__ void group_params(float lo, float hi, __half& s16, float& s, int& z) {
-  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-  s16 = __float2half_rn(s32);
-  if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
-  s = __half2float(s16);
-  z = __float2int_rn(__fdiv_rn(-lo, s));
-}
 
 template <int NJ>
 __device__ __forceinline__ float pick(const float (&a)[NJ], int k) {
@@ -226,16 +214,14 @@ __global__ void __launch_bounds__(kRegThreads, 1)
         const int r = lane;
         const float lo = fminf(fminf(s_lo[0][r], s_lo[1][r]), fminf(s_lo[2][r], s_lo[3][r]));
         const float hi = fmaxf(fmaxf(s_hi[0][r], s_hi[1][r]), fmaxf(s_hi[2][r], s_hi[3][r]));
-        __half s16;
-        float sc;
-        int z;
-        group_params(lo, hi, s16, sc, z);
+        float sc, zf;
+        const __half s16 = int4_group_params(lo, hi, sc, zf);
         s_scale[r] = sc;
-        s_zero[r] = static_cast<float>(z);
+        s_zero[r] = zf;
         if (r < rows) {
           const long long gi = static_cast<long long>(row0 + r) * G + (i >> 7);
           scales[gi] = s16;
-          zeros[gi] = __int2half_rn(z);
+          zeros[gi] = __float2half_rn(zf);
         }
       }
     }
@@ -307,15 +293,8 @@ cudaError_t launch_reg(const float* W, int64_t N, int64_t K, const float* U, int
   const size_t smem = static_cast<size_t>(D) * K * sizeof(float) + static_cast<size_t>(R) * K;
   const long long grid = (N + R - 1) / R;
   if (grid > 0x7fffffffLL || smem > static_cast<size_t>(kGptqSmem)) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gptq_int4_g128_reg<NJ, R, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGptqSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(k_gptq_int4_g128_reg<NJ, R, D>), kGptqSmem);
+  if (e != cudaSuccess) return e;
   k_gptq_int4_g128_reg<NJ, R, D><<<static_cast<unsigned>(grid), kRegThreads, smem, stream>>>(
       W, static_cast<int>(N), static_cast<int>(K), U, reinterpret_cast<uint32_t*>(Wq),
       reinterpret_cast<__half*>(scales), reinterpret_cast<__half*>(zeros));
@@ -344,14 +323,8 @@ cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const fl
   const int R = gptq_rows_per_cta(K);
   if (R < 1) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(R) * K * 5;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gptq_int4_g128, cudaFuncAttributeMaxDynamicSharedMemorySize, kGptqSmem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(k_gptq_int4_g128), kGptqSmem);
+  if (e != cudaSuccess) return e;
   const long long grid = (N + R - 1) / R;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   k_gptq_int4_g128<<<static_cast<unsigned>(grid), kGptqThreads, smem, stream>>>(

@@ -27,6 +27,14 @@ cudaError_t make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void
 
 int device_sm_count();
 
+// The calling thread's current CUDA context (driver entry point, no libcuda link), or
+// nullptr when none is current or the entry point is unavailable.
+CUcontext current_context();
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once per (kernel,
+// device); thread-safe.
+cudaError_t set_smem_attr_once(const void* kern, size_t smem_bytes);
+
 // Every workspace layout starts with this fixed header of split-K counters (the decode
 // kernel's bands, the tensor-core kernel's split last-wave tiles).  Every call that completes
 // leaves it at zero, so one workspace zeroed once can be shared by calls of any shape and by

@@ -39,12 +39,8 @@ __global__ void __launch_bounds__(256) k_quant_int4_g128(const float* __restrict
     lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
     hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
   }
-  const float s32 = __fdiv_rn(__fsub_rn(hi, lo), 15.0f);
-  __half s16 = __float2half_rn(s32);
-  if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
-  const float s = __half2float(s16);
-  const int z = __float2int_rn(__fdiv_rn(-lo, s));
-  const float zf = static_cast<float>(z);
+  float s, zf;
+  const __half s16 = int4_group_params(lo, hi, s, zf);
 
   uint32_t w0 = 0u, w1 = 0u;
 #pragma unroll
@@ -59,7 +55,7 @@ __global__ void __launch_bounds__(256) k_quant_int4_g128(const float* __restrict
     reinterpret_cast<uint2*>(Wq + g * 16)[sub] = make_uint2(w0, w1);
     if (sub == 0) {
       scales[g] = s16;
-      zeros[g] = __int2half_rn(z);
+      zeros[g] = __float2half_rn(zf);
     }
   }
   (void)groups_per_row;

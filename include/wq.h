@@ -56,8 +56,12 @@ typedef enum { WQ_FMT_INT4_G128_ASYM = 0, WQ_FMT_MXFP4 = 1 } wq_fmt;
  * 第 6 课：量化源码走读 (源码分层架构与生命周期: 8 INT4 codes in one int32 plus scale and zero
  * point tensors).  Per (row n, group g), float32 arithmetic:
  *   lo = min(min x, 0), hi = max(max x, 0); s32 = (hi - lo) / 15;
- *   s = fp16_rn(s32), and s = 1 if that is 0; z = rint(-lo / s);
+ *   s = fp16_rn(min(s32, 65504)), and s = 1 if that is 0; z = min(rint(-lo / s), 15);
  *   q = clamp(rint(x / s) + z, 0, 15).
+ *   (The min on s32 saturates the scale of a group whose range exceeds 15 * 65504 at the
+ *   largest finite fp16 value instead of +inf; its values beyond the range clip.  The min on
+ *   z keeps the zero point a code when the stored scale is far below s32, which happens only
+ *   for such groups and for fp16-subnormal scales, |x| below about 1e-6.)
  *   W       [N, K]    float32 input.
  *   Wq      [N, K/8]  int32 output; code k = 8j+i in bits 4i..4i+3 of word j.
  *   scales  [N, K/128] fp16 bits output.
@@ -201,7 +205,10 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * kernel accepts (M <= 16, N <= 2097152) on devices with up to 256 SMs, and a shape it cannot
  * hold is refused with WQ_ERR_SHAPE before anything is enqueued.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.  Each call
+ * with that device current); make that first call before any stream capture.  The address is
+ * looked up again when the device's current context has changed since (cudaDeviceReset
+ * unloads the module, and the array may come back elsewhere); after a reset, make one call
+ * outside any capture again before capturing.  Each call
  * clears the counters it needs on `stream` before the kernel.  All calls on a device share
  * the one array: calls that can overlap on the GPU (other streams, other threads) race and
  * corrupt each other's results -- serialise them.
@@ -212,7 +219,10 @@ wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_
 
 /*
  * The tensor-core (tcgen05, TMEM accumulator) kernel alone, for any M >= 1 (same arguments
- * and errors as wq_gemm_w4a16).
+ * and errors as wq_gemm_w4a16).  INT4: the dequantized weights (q - z) * s enter the tensor
+ * core as fp16, so they must lie inside the fp16 range (|w| <= 65504; beyond it the outputs
+ * are unspecified); activations of any finite bf16 magnitude are carried into fp16 exactly by
+ * a power-of-two scale per row.
  */
 wq_status wq_gemm_tc_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
                            const int32_t* Wq, const void* scales, const uint16_t* zeros,

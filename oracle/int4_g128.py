@@ -15,9 +15,12 @@ Steps for row n, group g, x = W[n, 128g : 128g + 128] (float32 arithmetic):
 1. ``x_min = min(min x, 0)``, ``x_max = max(max x, 0)``                (reading R1)
 2. ``s32 = (x_max - x_min) / 15``  (推理优化与量化算子深度技术调研 §1.2 with 2^4 - 1 levels;
    第 1 章：推理加速全景 §4.1)
-3. ``s = fp16(s32)`` rounded to nearest even and stored; if that is 0, ``s = 1``
-   (readings R3, R2)
-4. ``z = round(-x_min / s)`` with ``s`` the stored scale, round half to even (R4)
+3. ``s = fp16(min(s32, 65504))`` rounded to nearest even and stored; if that is 0,
+   ``s = 1`` (readings R3, R2; the ``min`` saturates a scale that would round past the
+   largest finite fp16 value to +inf at that value, reading R16)
+4. ``z = min(round(-x_min / s), 15)`` with ``s`` the stored scale, round half to even
+   (R4); the ``min`` keeps the zero point a code when the stored scale is far below
+   ``s32`` (fp16-subnormal or saturated scales, reading R16)
 5. ``q = clamp(round(x / s) + z, 0, 15)``
 6. pack: word ``j`` holds ``q[8j + i]`` in bits ``4i .. 4i+3`` (low nibble first, R5)
 
@@ -29,6 +32,7 @@ import numpy as np
 
 GROUP = 128
 LEVELS = 15
+FP16_MAX = 65504.0   # largest finite IEEE binary16 value, (2 - 2^-10) * 2^15
 
 
 def quantize(W: np.ndarray):
@@ -51,11 +55,12 @@ def group_params(x: np.ndarray):
     x_min = np.minimum(x.min(axis=-1), np.float32(0))
     x_max = np.maximum(x.max(axis=-1), np.float32(0))
     s32 = (x_max - x_min) / np.float32(LEVELS)                 # float32, round to nearest
+    s32 = np.minimum(s32, np.float32(FP16_MAX))                 # saturate (R16)
     s16 = np.asarray(s32.astype(np.float16))                    # stored scale
     s16[s16 == 0] = np.float16(1)
     s = s16.astype(np.float32)
-    z = np.rint((-x_min) / s).astype(np.int32)                  # non-negative integer
-    return s16, z
+    z = np.minimum(np.rint((-x_min) / s), np.float32(LEVELS))   # a code: 0 .. 15 (R16)
+    return s16, z.astype(np.int32)
 
 
 def codes(x: np.ndarray, s16: np.ndarray, z: np.ndarray) -> np.ndarray:

@@ -71,6 +71,42 @@ def test_gemm_tc_int4_large_activations(B):
     assert_close(y / scale, ref / scale, "int4 big X (scaled)")
 
 
+# Activation rows of very different magnitudes in one call: unit rows, rows of ~1e-6 (fp16
+# subnormals if converted unscaled), ~1e-20 and ~1e-30 (below fp16's range altogether).
+ROW_SCALES = (1.0, 1e-6, 1e-20, 1e-30)
+
+
+def _scaled_rows(seed, M, K):
+    xb, xf = inputs.activations(seed, M, K)
+    c = np.array([ROW_SCALES[m % len(ROW_SCALES)] for m in range(M)], np.float32)
+    xf = xf * c[:, None]
+    xb = inputs.bf16_bits_from_f32(xf)
+    return xb, inputs.f32_from_bf16_bits(xb), c.astype(np.float64)
+
+
+def check_small_rows(y, ref, c, what):
+    """Each row m scaled back by its magnitude c_m meets the unit-scale tolerance, and every
+    output with |ref| >= c_m is within 2 % of ref: relative accuracy independent of |x|."""
+    y = np.asarray(y, np.float64)
+    assert np.isfinite(y).all(), what + ": non-finite outputs"
+    assert_close(y / c[:, None], ref / c[:, None], what + " (rows / c_m)")
+    big = np.abs(ref) >= c[:, None]
+    rel = np.abs(y - ref)[big] / np.abs(ref)[big]
+    assert rel.size and rel.max() <= 2e-2, "%s: worst relative error %.3g" % (what, rel.max())
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_gemm_tc_small_magnitude_activations(B, fmt):
+    # The INT4 path converts X to fp16 with a per-row power of two; small rows must be scaled
+    # up (not only large rows down), else their values become fp16 subnormals or zeros.
+    M, N, K = 40, 384, 1024
+    W = inputs.weights(17, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf, c = _scaled_rows(18, M, K)
+    y = y_to_host(_run(B.gemm_tc_w4a16, fmt, xb, pk))
+    check_small_rows(y, linear.linear_w4a16(fmt, xf, *pk), c, "%s small |x|" % fmt)
+
+
 def test_dispatch_routes_by_m(B):
     M, N, K = 20, 256, 512
     W = inputs.weights(2, N, K, 0.05)

@@ -67,6 +67,20 @@ def test_gemv_mxfp4_large_activations(B):
     assert_close(y_to_host(Y), linear.linear_w4a16("mxfp4", xf, *pk), "mxfp4 big X")
 
 
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [4, 16])
+def test_gemv_small_magnitude_activations(B, fmt, M):
+    # Rows of ~1, 1e-6, 1e-20 and 1e-30 in one call (the MXFP4 decode path converts X to fp16
+    # with a power of two per 8-row tile and stage); accuracy relative to each row's magnitude.
+    from tests.test_gemm_tc_parity import _scaled_rows, check_small_rows
+    N, K = 512, 1024
+    W = inputs.weights(19, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf, c = _scaled_rows(20 + M, M, K)
+    y = y_to_host(_run(B, B.gemv_w4a16, fmt, xb, pk))
+    check_small_rows(y, linear.linear_w4a16(fmt, xf, *pk), c, "%s M=%d small |x|" % (fmt, M))
+
+
 def test_gemv_workspace_shared_across_shapes_and_kernels(B):
     # One workspace, zeroed once, serves calls of different shapes and both kernels.
     import torch

@@ -102,6 +102,48 @@ def test_int4_constant_positive_group_includes_zero_in_range():
     assert (int4_g128.unpack(Wq) == g["code"]).all()
 
 
+def test_int4_scale_saturates_at_fp16_max():
+    # Reading R16: a group range above 15 * 65504 stores the largest finite fp16 scale
+    # (not +inf), and the zero point stays a code; the dequantized group stays finite and
+    # 0 stays exact.
+    g = _golden("hand_derived_int4.json")["saturated_scale"]
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0] = -2e6
+    Wq, s, z = int4_g128.quantize(x)
+    assert s.view(np.uint16)[0, 0] == int(g["scale_fp16_hex"], 16)
+    assert float(z[0, 0]) == g["zero"]
+    q = int4_g128.unpack(Wq)[0]
+    assert q[0] == g["code_min"] and (q[1:] == g["code_zero"]).all()
+    deq = int4_g128.dequantize(Wq, s, z)[0]
+    assert deq[0] == g["deq_min"] and (deq[1:] == 0).all()
+    # just inside the fp16 range the rounding itself gives 65504: saturation changes nothing
+    g2 = _golden("hand_derived_int4.json")["scale_rounds_to_fp16_max"]
+    x[0, 0] = -982650.0
+    _, s, z = int4_g128.quantize(x)
+    assert s.view(np.uint16)[0, 0] == int(g2["scale_fp16_hex"], 16) and float(z[0, 0]) == g2["zero"]
+    # huge ranges (the 1e30 rows of the adversarial tests) give no overflow and finite values
+    with np.errstate(over="raise", invalid="raise"):
+        big = np.array([[-1e30, 3e38] + [0.0] * 126], np.float32)
+        Wq, s, z = int4_g128.quantize(big)
+        assert np.isfinite(int4_g128.dequantize(Wq, s, z)).all()
+    assert s.view(np.uint16)[0, 0] == 0x7BFF and 0 <= float(z[0, 0]) <= 15
+
+
+def test_int4_zero_point_clamped_to_code_range():
+    # Reading R16: an fp16-subnormal scale can sit far below s32; the zero point is then
+    # clamped to 15 so that 0.0 still dequantizes to exactly 0.
+    g = _golden("hand_derived_int4.json")["subnormal_scale_zero_clamp"]
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0] = np.float32(21 * 2.0 ** -24)
+    x[0, 0] = -x[0, 0]
+    Wq, s, z = int4_g128.quantize(x)
+    assert s.view(np.uint16)[0, 0] == int(g["scale_fp16_hex"], 16)
+    assert float(z[0, 0]) == g["zero"]
+    q = int4_g128.unpack(Wq)[0]
+    assert q[0] == g["code_min"] and (q[1:] == g["code_zero"]).all()
+    assert (int4_g128.dequantize(Wq, s, z)[0, 1:] == 0).all()
+
+
 def test_int4_packing_order():
     g = _golden("hand_derived_int4.json")["packing"]
     q = np.array([g["codes"]], dtype=np.uint32)

@@ -205,12 +205,20 @@ def test_swiglu_full_size_prefill_qwen25_72b(B):
 
 
 def test_swiglu_paths_agree_where_operands_are_exact(B):
-    # The K = 4096 case that needs the fp16-operand allowance on the INT4 tensor-core path
-    # passes the plain bound on the decode kernel (exact products) at M <= 16.
+    # The K = 4096 case, where the INT4 tensor-core path's fp16 operands matter: the decode
+    # kernel (exact products) meets the plain bound; the tensor-core kernel meets it plus the
+    # propagated fp16-operand allowance; the two kernels' outputs agree with each other within
+    # the same bound; and the allowance is needed only by a small fraction of the outputs
+    # (those near SiLU's steep region, g ~ 0 with large |u|).
     F, K, M = 1024, 4096, 16
     pk = _stacked("int4_g128", F, K, F * 5 + K + 1)
     xb, xf = inputs.activations(M * 3 + F, M, K)
     ref = _ref("int4_g128", xf, pk)
-    assert_close(y_to_host(_run(B.gemv_w4a16_swiglu, "int4_g128", xb, pk, F)), ref, "decode")
+    y_dec = y_to_host(_run(B.gemv_w4a16_swiglu, "int4_g128", xb, pk, F))
+    assert_close(y_dec, ref, "decode")
     y_tc = y_to_host(_run(B.gemm_tc_w4a16_swiglu, "int4_g128", xb, pk, F))
-    assert_close(y_tc, ref, "tc", _fp16_operand_allowance(xf, pk, F))
+    allow = _fp16_operand_allowance(xf, pk, F)
+    assert_close(y_tc, ref, "tc", allow)
+    assert_close(y_tc, y_dec, "tc vs decode", allow)
+    beyond_plain = np.abs(y_tc - ref) > 1e-2 * (1 + np.abs(ref))
+    assert beyond_plain.mean() <= 1e-3, "%d of %d outputs need the allowance" % (beyond_plain.sum(), ref.size)
