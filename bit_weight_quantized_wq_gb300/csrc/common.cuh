@@ -210,7 +210,9 @@ __device__ __forceinline__ __half int4_group_params(float lo, float hi, float& s
   __half s16 = __float2half_rn(fminf(s32, 65504.0f));
   if ((__half_as_ushort(s16) & 0x7fffu) == 0u) s16 = __ushort_as_half(0x3c00u);  // zero -> 1.0
   s = __half2float(s16);
-  zf = fminf(rintf(__fdiv_rn(-lo, s)), 15.0f);
+  // through an integer: -lo is -0.0 for a group without negative values, and the stored zero
+  // point must be +0 (an integer), not fp16 -0
+  zf = static_cast<float>(static_cast<int>(fminf(rintf(__fdiv_rn(-lo, s)), 15.0f)));
   return s16;
 }
 

@@ -116,7 +116,7 @@ struct Smem {
   // at byte 512 m -- the same size) land here by TMA and are converted in place.
   uint4 x[kXStages][NT][2][4][32];
   float xsum[kXStages][2][MT];               // INT4: sum of the group's activations per row m
-  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row (one per 8-row tile)
+  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row
   uint64_t full_w[WS];
   uint64_t empty_w[WS];
   uint64_t raw_x[kXStages];                  // the stage's raw activation rows landed (TMA)
@@ -486,26 +486,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < 8; ++r)
           cur[r] = (r < mlive) ? xs4[(8 * nt + r) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
-        // MXFP4: one power-of-two scale 2^-k per stage and 8-row tile carries every operand into
-        // fp16 exactly (bf16_to_f16_exponent: the largest in [2^14, 2^15), small tiles scaled up);
-        // only values more than 2^31 below the tile's largest lose bits, as fp16 subnormals.
-        // max |x| over the tile: bf16 magnitudes order like integers.
-        float inv = 1.f, xf = 1.f;
+        // MXFP4: one power-of-two scale 2^-k per stage and activation row carries every operand
+        // into fp16 exactly (bf16_to_f16_exponent: the row's largest in [2^14, 2^15), small
+        // rows scaled up); only values more than 2^31 below their row's largest lose bits, as
+        // fp16 subnormals.  max |x| per row: bf16 magnitudes order like integers; two rows'
+        // maxima share a word for the warp reduction.
+        float inv[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) inv[r] = 1.f;
         if constexpr (FMT != kInt4G128) {
-          uint32_t mx2 = 0u;   // per 16-bit half
+          uint32_t mxp[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t m2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const uint4 x = cur[2 * q + u];
+              const uint32_t v = __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                          __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
+              m2[u] = max(v & 0xffffu, v >> 16);
+            }
+            mxp[q] = m2[0] | (m2[1] << 16);
+          }
+#pragma unroll
+          for (int sh = 1; sh < 32; sh <<= 1)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mxp[q] = __vmaxu2(mxp[q], __shfl_xor_sync(0xffffffffu, mxp[q], sh));
 #pragma unroll
           for (int r = 0; r < 8; ++r) {
-            const uint4 x = cur[r];
-            mx2 = __vmaxu2(mx2, __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
-                                          __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu)));
+            const int kk = bf16_to_f16_exponent((mxp[r >> 1] >> (16 * (r & 1))) & 0xffffu);
+            inv[r] = pow2_normal(-kk);
+            if (lane == r) sm.xf[slot][8 * nt + r] = pow2_normal(kk);
           }
-          uint32_t mx = max(mx2 & 0xffffu, mx2 >> 16);
-#pragma unroll
-          for (int sh = 1; sh < 32; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-          const int kk = bf16_to_f16_exponent(mx);
-          inv = pow2_normal(-kk);
-          xf = pow2_normal(kk);
-          if (lane < 8) sm.xf[slot][8 * nt + lane] = xf;
         }
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
@@ -528,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv,
-                                             __uint_as_float(w4[q] & 0xffff0000u) * inv);
+              __half2 hh = __floats2half2_rn(__uint_as_float(w4[q] << 16) * inv[r],
+                                             __uint_as_float(w4[q] & 0xffff0000u) * inv[r]);
               o[q] = *reinterpret_cast<uint32_t*>(&hh);
             }
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
