@@ -32,6 +32,7 @@ EXPORTED = [
     "wq_status_str", "wq_read_error_flags", "wq_check_device", "wq_gemv_w4a16_noalloc",
     "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
     "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128", "wq_selftest_wait_timeout",
+    "wq_gemm_w4a16_qkv", "wq_gptq_workspace_bytes", "wq_gptq_factor", "wq_gptq_int4_g128_calib",
 ]
 
 _lib = None
@@ -68,6 +69,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_awq_workspace_bytes": (SZ, [I64, I64, I64]),
         "wq_awq_int4_g128": (I32, [P, I64, I64, P, I64, P, P, P, P, P, P, P, SZ, P]),
         "wq_selftest_wait_timeout": (I32, [U32, ctypes.POINTER(U32), P]),
+        "wq_gemm_w4a16_qkv": (I32, [I32, P, I64, I64, I64, I64, P, P, P, P, P, P, P, SZ, P]),
+        "wq_gptq_workspace_bytes": (SZ, [I64]),
+        "wq_gptq_factor": (I32, [P, I64, I64, P, P, SZ, P]),
+        "wq_gptq_int4_g128_calib": (I32, [P, I64, I64, P, I64, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -166,6 +171,46 @@ def gptq_int4_g128(W: torch.Tensor, U: torch.Tensor, stream=None):
     return Wq, scales, zeros
 
 
+def _gptq_workspace(K, dev, workspace):
+    need = int(load_library().wq_gptq_workspace_bytes(K))
+    if workspace is None:
+        return torch.empty((need,), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor on X's device")
+    return workspace
+
+
+def gptq_factor(X: torch.Tensor, workspace=None, stream=None):
+    """The upper factor U float32 [K, K] of H^-1 = U^T U, H = 2 X^T X + lambda I, from calibration
+    activations X float32 [n, K] (CUDA), computed on the device in float64."""
+    _need(X, torch.float32, "X")
+    n, K = X.shape
+    ws = _gptq_workspace(K, X.device, workspace)
+    U = torch.empty((K, K), dtype=torch.float32, device=X.device)
+    _check(load_library().wq_gptq_factor(_ptr(X), n, K, _ptr(U), _ptr(ws), ws.numel(), _stream(stream, X.device)),
+           "wq_gptq_factor")
+    return U
+
+
+def gptq_int4_g128_calib(W: torch.Tensor, X: torch.Tensor, workspace=None, stream=None):
+    """GPTQ of W float32 [N, K] from calibration activations X float32 [n, K] (both CUDA), the
+    factor and the sweep on the device -> (Wq int32 [N, K/8], scales fp16, zeros fp16)."""
+    _need(W, torch.float32, "W")
+    _need(X, torch.float32, "X")
+    N, K = W.shape
+    if X.dim() != 2 or X.shape[1] != K or X.device != W.device:
+        raise ValueError("X must be [n, K] on W's device")
+    n = X.shape[0]
+    ws = _gptq_workspace(K, W.device, workspace)
+    Wq = torch.empty((N, K // 8), dtype=torch.int32, device=W.device)
+    scales = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    zeros = torch.empty((N, K // 128), dtype=torch.float16, device=W.device)
+    _check(load_library().wq_gptq_int4_g128_calib(_ptr(W), N, K, _ptr(X), n, _ptr(Wq), _ptr(scales), _ptr(zeros),
+                                                  _ptr(ws), ws.numel(), _stream(stream, W.device)),
+           "wq_gptq_int4_g128_calib")
+    return Wq, scales, zeros
+
+
 def awq_int4_g128(W: torch.Tensor, X: torch.Tensor, workspace=None, stream=None):
     """AWQ of W float32 [N, K] with calibration activations X float32 [n, K] (both CUDA) ->
     (Wq, scales, zeros, s float32 [K], alpha_index int32 [1], losses float64 [21]); the layer's
@@ -235,10 +280,10 @@ def _fn(cname: str):
     return f
 
 
-def _prepare(f, X, Wq, scales, zeros, out, swiglu):
-    """The checks every layer call makes before its pointers reach the library, which sees
-    only raw addresses and sizes: dtypes, devices, contiguity, and the shapes of Wq, scales,
-    zeros and out against (M, K, N).  Returns (M, K, N, out), allocating out when None."""
+def _inputs(f, X, Wq, scales, zeros):
+    """The checks every layer call makes on its inputs before their pointers reach the library,
+    which sees only raw addresses and sizes: dtypes, devices, contiguity, and the shapes of Wq,
+    scales and zeros against X.  Returns (M, K, N)."""
     int4 = f == FMT_INT4_G128
     if (X.dtype is not _BF16 or Wq.dtype is not _I32 or scales.dtype is not (_F16 if int4 else _U8)
             or (zeros is not None and (not int4 or zeros.dtype is not _F16)) or (int4 and zeros is None)):
@@ -258,15 +303,23 @@ def _prepare(f, X, Wq, scales, zeros, out, swiglu):
     dev = X.device
     if Wq.device != dev or scales.device != dev or (zeros is not None and zeros.device != dev):
         raise ValueError("X, Wq, scales and zeros must be on the same device")
-    ncol = N // 2 if swiglu else N
+    return M, K, N
+
+
+def _output(out, M, ncol, dev, name="out"):
+    """A bf16 [M, ncol] output on ``dev``: ``out`` checked, or a new tensor when None."""
     if out is None:
-        out = torch.empty((M, ncol), dtype=_BF16, device=dev)
-    else:
-        if out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
-            _need(out, _BF16, "out")
-        if out.shape != (M, ncol) or out.device != dev:
-            raise ValueError("out must be [M, %s] on X's device" % ("N/2" if swiglu else "N"))
-    return M, K, N, out
+        return torch.empty((M, ncol), dtype=_BF16, device=dev)
+    if out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
+        _need(out, _BF16, name)
+    if out.shape != (M, ncol) or out.device != dev:
+        raise ValueError("%s must be [%d, %d] on X's device" % (name, M, ncol))
+    return out
+
+
+def _prepare(f, X, Wq, scales, zeros, out, swiglu):
+    M, K, N = _inputs(f, X, Wq, scales, zeros)
+    return M, K, N, _output(out, M, N // 2 if swiglu else N, X.device)
 
 
 def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
@@ -366,6 +419,32 @@ def gemv_w4a16_noalloc(fmt, X, Wq, scales, zeros=None, out=None, stream=None):
                                        _stream(stream, X.device))
     if st:
         _check(st, "wq_gemv_w4a16_noalloc")
+    return out
+
+
+def gemm_w4a16_qkv(fmt, X, Wq, scales, zeros=None, Nq=None, Nkv=None, out=None, workspace=None, stream=None):
+    """The fused QKV projection split in the epilogue: (Q [M, Nq], K [M, Nkv], V [M, Nkv]) from the
+    stacked packed weight [W_Q; W_K; W_V] of Nq + 2 Nkv rows; dispatches like ``gemm_w4a16``.
+    ``out`` may be a tuple of three preallocated bf16 tensors."""
+    f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
+    M, K, N = _inputs(f, X, Wq, scales, zeros)
+    if Nq is None or Nkv is None or Nq < 1 or Nkv < 1 or Nq + 2 * Nkv != N:
+        raise ValueError("Nq, Nkv >= 1 with Nq + 2 Nkv == Wq.shape[0] required")
+    dev = X.device
+    if out is not None and len(out) != 3:
+        raise ValueError("out must be three tensors (Q, K, V)")
+    out = tuple(_output(None if out is None else out[i], M, n, dev, "out " + nm)
+                for i, (n, nm) in enumerate(((Nq, "Q"), (Nkv, "K"), (Nkv, "V"))))
+    if workspace is not None and (not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on X's device")
+    ws = workspace if workspace is not None else _workspace_for(dev, gemm_workspace_bytes(f, M, K, N), None)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    st = _fn("wq_gemm_w4a16_qkv")(f, X.data_ptr(), M, K, Nq, Nkv, Wq.data_ptr(), scales.data_ptr(),
+                                   None if zeros is None else zeros.data_ptr(), out[0].data_ptr(), out[1].data_ptr(),
+                                   out[2].data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes,
+                                   _stream(stream, dev))
+    if st:
+        _check(st, "wq_gemm_w4a16_qkv")
     return out
 
 

@@ -181,6 +181,41 @@ wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U
   return from_cuda(wq::launch_gptq_int4_g128(W, N, K, U, Wq, scales, zeros, static_cast<cudaStream_t>(stream)));
 }
 
+size_t wq_gptq_workspace_bytes(int64_t K) {
+  if (K < 128 || K % 128 != 0 || K > 46208) return 0;
+  return wq::gptq_factor_workspace_bytes(K) + static_cast<size_t>(K) * static_cast<size_t>(K) * sizeof(float);
+}
+
+wq_status wq_gptq_factor(const float* X, int64_t n, int64_t K, float* U, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  if (!X || !U) return WQ_ERR_NULL;
+  if (n < 1 || n > (1LL << 30) || K < 128 || K % 128 != 0 || K > 46208) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(U)) return WQ_ERR_ALIGN;
+  if (!workspace || ws_bytes < wq::gptq_factor_workspace_bytes(K)) return WQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gptq_factor(X, n, K, U, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_gptq_int4_g128_calib(const float* W, int64_t N, int64_t K, const float* X, int64_t n, int32_t* Wq,
+                                  uint16_t* scales, uint16_t* zeros, void* workspace, size_t ws_bytes, void* stream) {
+  if (!W || !X || !Wq || !scales || !zeros) return WQ_ERR_NULL;
+  if (N < 1 || N > (1LL << 30) || n < 1 || n > (1LL << 30) || K < 128 || K % 128 != 0 || K > 46208 ||
+      wq::gptq_rows_per_cta(K) < 1)
+    return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(X) || !aligned16(Wq) || !aligned16(scales) || !aligned16(zeros)) return WQ_ERR_ALIGN;
+  if (!workspace || ws_bytes < wq_gptq_workspace_bytes(K)) return WQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* U = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + wq::gptq_factor_workspace_bytes(K));
+  st = from_cuda(wq::launch_gptq_factor(X, n, K, U, workspace, s));
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gptq_int4_g128(W, N, K, U, Wq, scales, zeros, s));
+}
+
 size_t wq_awq_workspace_bytes(int64_t N, int64_t K, int64_t n) {
   if (N < 1 || n < 1 || K < 128 || K % 128 != 0 || N > (1LL << 30) || K > (1LL << 30) || n > (1LL << 30)) return 0;
   return wq::awq_workspace_bytes(N, K, n);
@@ -339,6 +374,39 @@ wq_status wq_gemm_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t
   return wq_gemm_tc_w4a16_swiglu(fmt, X, M, K, F, Wq, scales, zeros, Y, workspace, ws_bytes, stream);
 }
 
+wq_status wq_gemm_w4a16_qkv(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t Nq, int64_t Nkv,
+                            const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Yq, uint16_t* Yk,
+                            uint16_t* Yv, void* workspace, size_t ws_bytes, void* stream) {
+  if (Nq < 1 || Nkv < 1 || Nq > (1LL << 29) || Nkv > (1LL << 28)) return WQ_ERR_SHAPE;
+  const int64_t N = Nq + 2 * Nkv;
+  wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Yq);
+  if (st != WQ_OK) return st;
+  if (!Yk || !Yv) return WQ_ERR_NULL;
+  if (!aligned16(Yk) || !aligned16(Yv)) return WQ_ERR_ALIGN;
+  wq::OutSplit split{};
+  split.y[0] = Yq;
+  split.y[1] = Yk;
+  split.y[2] = Yv;
+  split.ld[0] = Nq;
+  split.ld[1] = Nkv;
+  split.ld[2] = Nkv;
+  split.n1 = static_cast<int>(Nq);
+  split.n2 = static_cast<int>(Nq + Nkv);
+  const bool decode = M <= wq_dispatch_threshold(fmt, K, N);
+  if (decode && (N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
+  const size_t need = decode ? wq::gemv_workspace_bytes(fmt, M, K, N) : wq::gemm_tc_workspace_bytes(fmt, M, K, N);
+  if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (decode)
+    return from_cuda(wq::launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Yq, workspace, ws_bytes, s, wq::kEpiSplit3,
+                                     &split));
+  return from_cuda(wq::launch_gemm_tc(fmt, X, M, K, N, Wq, scales, zeros, Yq, workspace, ws_bytes, s, wq::kEpiSplit3,
+                                      &split));
+}
+
 wq_status wq_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t row_bytes, void* stream) {
   if (!src || !dst) return WQ_ERR_NULL;
   if (F < 8 || F % 8 != 0 || row_bytes < 1 || F > (1LL << 30) || row_bytes > (1LL << 40) / F) return WQ_ERR_SHAPE;
@@ -367,7 +435,8 @@ const char* wq_status_str(wq_status s) {
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
-  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() | wq::gptq_read_and_clear_error() |
+  *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() |
+         wq::gptq_read_and_clear_error() | wq::gptq_factor_read_and_clear_error() |
          wq::selftest_read_and_clear_error();
   return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }

@@ -19,6 +19,7 @@ enum : uint32_t {
   kErrWaitReduce = 1u << 3,   // split-K reduction gave up
   kErrDrain = 1u << 4,        // TMA drain at exit gave up
   kErrSelftestWait = 1u << 5, // the diagnostic wait of wq_selftest_wait_timeout ran out (expected)
+  kErrNotPositiveDefinite = 1u << 6,  // GPTQ factor: a Cholesky pivot of H was not positive
 };
 
 // About two seconds of polling, measured on the global nanosecond timer.

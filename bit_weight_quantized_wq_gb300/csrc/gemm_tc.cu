@@ -68,6 +68,7 @@ struct Params {
   const uint16_t* zeros;
   const float* xscale;   // INT4: 2^k_m per activation row (nullptr for MXFP4)
   uint16_t* Y;
+  OutSplit split;        // EPI == kEpiSplit3: three output tensors by column range
   int M, K, N;
   int KB;                // MXFP4 scale bytes per row (K / 32)
   int G;                 // INT4 groups per row (K / 128)
@@ -473,7 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (m < p.M) {
               float y = __uint_as_float(v[j]);
               if constexpr (FMT == kInt4G128) y *= __ldg(p.xscale + m);
-              p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+              const uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+              if constexpr (EPI == kEpiSplit3) store_split3(p.split, m, n, yb);
+              else p.Y[static_cast<long long>(m) * p.N + n] = yb;
             }
           }
         }
@@ -558,14 +561,16 @@ size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
 
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                           cudaStream_t stream, int epi) {
+                           cudaStream_t stream, int epi, const OutSplit* split) {
   using namespace tc;
   if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
+  if (epi == kEpiSplit3 && !split) return cudaErrorInvalidValue;
   if (ws_bytes < gemm_tc_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   Params p{};
   p.scales = scales;
   p.zeros = zeros;
   p.Y = Y;
+  if (split) p.split = *split;
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
@@ -610,8 +615,11 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   const size_t smem = sizeof(Smem) + 1024;
   const unsigned grid = static_cast<unsigned>(p.full_tiles + 2 * nsplit);
   void (*kern)(CUtensorMap, CUtensorMap, Params) =
-      fmt == kInt4G128 ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu> : k_gemm_tc<kInt4G128, kEpiNone>)
-                       : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu> : k_gemm_tc<kMxfp4, kEpiNone>);
+      fmt == kInt4G128
+          ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu>
+                               : (epi == kEpiSplit3 ? k_gemm_tc<kInt4G128, kEpiSplit3> : k_gemm_tc<kInt4G128, kEpiNone>))
+          : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu>
+                               : (epi == kEpiSplit3 ? k_gemm_tc<kMxfp4, kEpiSplit3> : k_gemm_tc<kMxfp4, kEpiNone>));
   e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, smem, stream>>>(tx, tw, p);

@@ -35,6 +35,7 @@
 // and resets the counter).
 #include <mutex>
 
+#include "decode_util.cuh"
 #include "internal.h"
 
 namespace wq {
@@ -49,6 +50,8 @@ uint32_t gemv_read_and_clear_error() {
 }
 
 namespace gemv {
+
+using namespace dec;
 
 constexpr int kConsumerWarps = 16;
 constexpr int kRowsPerWarp = 16;                     // one m16 row tile per consumer warp
@@ -82,6 +85,7 @@ struct Params {
   const void* scales;
   const uint16_t* zeros;
   uint16_t* Y;
+  OutSplit split;     // EPI == kEpiSplit3: three output tensors by column range
   float* part;        // [P][2][MT][kBand] fp32 partials
   uint32_t* cnt;      // [bands] counters
   int M, K, N;
@@ -99,10 +103,6 @@ struct Params {
 // started in an earlier band (lo_side).
 struct BandContrib { int c_lo, c_hi, lo_side; };
 
-// Fragment row f (0..15) of a 16-row tile -> row inside the tile.  Rows g and g+4 of a
-// smem swizzle atom then land in disjoint bank groups, so the consumer's 128-bit loads
-// are conflict-free.
-__device__ __forceinline__ int frag_row(int f) { return (f & 8) | ((f >> 1) & 3) | ((f & 1) << 2); }
 
 __device__ __forceinline__ long long unit_start(long long U, int P, int c) { return (U * c) / P; }
 
@@ -132,53 +132,6 @@ struct Smem {
   int ci_band[2];
   BandContrib ci[2];
 };
-
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
-  return d;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-  return d;
-}
-
-// Four E2M1 code pairs (one 32-bit word, byte b = elements 2b, 2b + 1) -> four f16x2, exact.
-// The word is split into bytes by register moves, with no shifts or masks.
-__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]) : "r"(w));
-}
-
-// Tensor-core MACs.  Not volatile: they are pure functions of their operands, so the
-// compiler may interleave independent accumulation chains.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 2^(byte - 127) as a float for an E8M0 byte (byte 0 -> 2^-127, subnormal).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
-  return byte ? __uint_as_float(byte << 23) : __uint_as_float(0x00400000u);
-}
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
@@ -272,7 +225,11 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, Ban
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int n = band * kBand + r4 + q;
-        if (n < p.N) p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o4[q]));
+        if (n < p.N) {
+          const uint16_t y = __bfloat16_as_ushort(__float2bfloat16_rn(o4[q]));
+          if constexpr (EPI == kEpiSplit3) store_split3(p.split, m, n, y);
+          else p.Y[static_cast<long long>(m) * p.N + n] = y;
+        }
       }
     }
   }
@@ -552,17 +509,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // times the just-written B fragments gives every column sum (exact products, fp32
           // accumulation).  Lane (g = 0, t) receives rows 2t, 2t + 1 of the tile.
           __syncwarp();
+          // (four independent accumulator chains per group: the MMA latency bounds this step)
           constexpr uint32_t kOnes = 0x3f803f80u;   // bf16 (1, 1)
 #pragma unroll
           for (int hg = 0; hg < 2; ++hg) {
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            float d[4][4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const uint4 b = sm.x[slot][nt][hg][v][lane];
-              mma_bf16(d, kOnes, kOnes, kOnes, kOnes, b.x, b.y);
-              mma_bf16(d, kOnes, kOnes, kOnes, kOnes, b.z, b.w);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) d[v][e] = 0.f;
+              mma_bf16(d[v], kOnes, kOnes, kOnes, kOnes, b.x, b.y);
+              mma_bf16(d[v], kOnes, kOnes, kOnes, kOnes, b.z, b.w);
             }
-            if (lane < 4) *reinterpret_cast<float2*>(&sm.xsum[slot][hg][8 * nt + 2 * lane]) = make_float2(d[0], d[1]);
+            const float s0 = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]);
+            const float s1 = (d[0][1] + d[1][1]) + (d[2][1] + d[3][1]);
+            if (lane < 4) *reinterpret_cast<float2*>(&sm.xsum[slot][hg][8 * nt + 2 * lane]) = make_float2(s0, s1);
           }
         }
       }
@@ -809,8 +771,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int e = 0; e < 4; ++e) {
                 const int m = 2 * t + (e & 1) + 8 * nt;
                 const int n = band * kBand + ((e >> 1) ? r1 : r0);
-                if (m < p.M && n < p.N)
-                  p.Y[static_cast<long long>(m) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
+                if (m < p.M && n < p.N) {
+                  const uint16_t y = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
+                  if constexpr (EPI == kEpiSplit3) store_split3(p.split, m, n, y);
+                  else p.Y[static_cast<long long>(m) * p.N + n] = y;
+                }
               }
           }
         } else {
@@ -897,13 +862,15 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
 
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                             const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                            cudaStream_t stream, int epi) {
+                            cudaStream_t stream, int epi, const OutSplit* split) {
   if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
+  if (epi == kEpiSplit3 && !split) return cudaErrorInvalidValue;
   gemv::Params p{};
   p.X = X;
   p.scales = scales;
   p.zeros = zeros;
   p.Y = Y;
+  if (split) p.split = *split;
   p.M = static_cast<int>(M);
   p.K = static_cast<int>(K);
   p.N = static_cast<int>(N);
@@ -950,18 +917,16 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
     }
   }
   const bool small = M <= 8;
-  if (epi == kEpiSwiglu) {
-    if (fmt == kInt4G128)
-      return small ? launch_gemv_t<kInt4G128, 8, kEpiSwiglu>(tw, ts, tz, p, stream)
-                   : launch_gemv_t<kInt4G128, 16, kEpiSwiglu>(tw, ts, tz, p, stream);
-    return small ? launch_gemv_t<kMxfp4, 8, kEpiSwiglu>(tw, ts, tz, p, stream)
-                 : launch_gemv_t<kMxfp4, 16, kEpiSwiglu>(tw, ts, tz, p, stream);
-  }
-  if (fmt == kInt4G128)
-    return small ? launch_gemv_t<kInt4G128, 8, kEpiNone>(tw, ts, tz, p, stream)
-                 : launch_gemv_t<kInt4G128, 16, kEpiNone>(tw, ts, tz, p, stream);
-  return small ? launch_gemv_t<kMxfp4, 8, kEpiNone>(tw, ts, tz, p, stream)
-               : launch_gemv_t<kMxfp4, 16, kEpiNone>(tw, ts, tz, p, stream);
+#define WQ_BAND_LAUNCH(EPIV)                                                                                   \
+  if (fmt == kInt4G128)                                                                                        \
+    return small ? launch_gemv_t<kInt4G128, 8, EPIV>(tw, ts, tz, p, stream)                                   \
+                 : launch_gemv_t<kInt4G128, 16, EPIV>(tw, ts, tz, p, stream);                                 \
+  return small ? launch_gemv_t<kMxfp4, 8, EPIV>(tw, ts, tz, p, stream)                                        \
+               : launch_gemv_t<kMxfp4, 16, EPIV>(tw, ts, tz, p, stream);
+  if (epi == kEpiSwiglu) { WQ_BAND_LAUNCH(kEpiSwiglu) }
+  if (epi == kEpiSplit3) { WQ_BAND_LAUNCH(kEpiSplit3) }
+  WQ_BAND_LAUNCH(kEpiNone)
+#undef WQ_BAND_LAUNCH
 }
 
 // The decode entry points run the mma.sync kernel above.  (A tcgen05 variant was measured
@@ -971,8 +936,8 @@ size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) { return g
 
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                         const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                        cudaStream_t stream, int epi) {
-  return launch_gemv_mma(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream, epi);
+                        cudaStream_t stream, int epi, const OutSplit* split) {
+  return launch_gemv_mma(fmt, X, M, K, N, Wq, scales, zeros, Y, ws, ws_bytes, stream, epi, split);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -16,8 +16,24 @@ enum Fmt : int { kInt4G128 = 0, kMxfp4 = 1 };
 // Epilogue of the linear layer.  kEpiSwiglu: the weight is the fused gate+up projection of
 // 2F rows with gate and up rows interleaved in blocks of 8 (row 16q + i is gate row 8q + i,
 // row 16q + 8 + i the matching up row), and the kernel writes Y[M, F] = SiLU(gate) * up,
-// applied to the fp32 accumulators before the one bf16 rounding.
-enum Epi : int { kEpiNone = 0, kEpiSwiglu = 1 };
+// applied to the fp32 accumulators before the one bf16 rounding.  kEpiSplit3: the output
+// columns go to three tensors by column range (OutSplit), e.g. the Q, K and V of a fused QKV
+// projection.
+enum Epi : int { kEpiNone = 0, kEpiSwiglu = 1, kEpiSplit3 = 2 };
+
+// Three row-major bf16 output tensors by column range: column n < n1 goes to
+// y[0][m * ld[0] + n], n1 <= n < n2 to y[1][m * ld[1] + n - n1], n >= n2 to y[2][m * ld[2] + n - n2].
+struct OutSplit {
+  uint16_t* y[3];
+  long long ld[3];
+  int n1, n2;
+};
+
+__device__ __forceinline__ void store_split3(const OutSplit& s, int m, int n, uint16_t v) {
+  if (n < s.n1) s.y[0][static_cast<long long>(m) * s.ld[0] + n] = v;
+  else if (n < s.n2) s.y[1][static_cast<long long>(m) * s.ld[1] + (n - s.n1)] = v;
+  else s.y[2][static_cast<long long>(m) * s.ld[2] + (n - s.n2)] = v;
+}
 
 // Encodes a 2-D tiled TMA descriptor through the driver entry point (no libcuda link).
 // dims/strides in elements/bytes, innermost first.
@@ -54,7 +70,7 @@ cudaError_t launch_quant_mxfp4(const float* W, int64_t N, int64_t K, int32_t* Wq
 size_t gemv_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                         const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                        cudaStream_t stream, int epi = kEpiNone);
+                        cudaStream_t stream, int epi = kEpiNone, const OutSplit* split = nullptr);
 uint32_t gemv_read_and_clear_error();
 size_t gemv_noalloc_scratch_bytes();
 cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -65,7 +81,7 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N);
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                            const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
-                           cudaStream_t stream, int epi = kEpiNone);
+                           cudaStream_t stream, int epi = kEpiNone, const OutSplit* split = nullptr);
 uint32_t gemm_tc_read_and_clear_error();
 
 // gptq.cu -- GPTQ sweep (INT4 g128) with a caller-provided inverse-Hessian Cholesky factor
@@ -73,6 +89,11 @@ int gptq_rows_per_cta(int64_t K);
 uint32_t gptq_read_and_clear_error();
 cudaError_t launch_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U, int32_t* Wq,
                                   uint16_t* scales, uint16_t* zeros, cudaStream_t stream);
+
+// gptq_factor.cu -- U (H^-1 = U^T U, H = 2 X^T X + lambda I) from calibration activations, float64
+size_t gptq_factor_workspace_bytes(int64_t K);
+cudaError_t launch_gptq_factor(const float* X, int64_t n, int64_t K, float* U, void* ws, cudaStream_t stream);
+uint32_t gptq_factor_read_and_clear_error();
 
 // awq.cu -- AWQ scale search + INT4 g128 quantize of the scaled weight
 size_t awq_workspace_bytes(int64_t N, int64_t K, int64_t n);

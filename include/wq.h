@@ -116,6 +116,40 @@ wq_status wq_gptq_int4_g128(const float* W, int64_t N, int64_t K, const float* U
                             uint16_t* scales, uint16_t* zeros, void* stream);
 
 /*
+ * GPTQ's inverse-Hessian factor from calibration activations, computed on the device:
+ *   H = 2 X^T X + lambda I,  lambda = 0.01 * mean(diag(2 X^T X)),  U upper triangular with
+ *   H^-1 = U^T U and a positive diagonal -- the factor wq_gptq_int4_g128 takes.
+ * Defined by: 第 1 章：推理加速全景 §4.2 (H = 2 X^T X + lambda I over the calibration set; H^-1
+ * through its Cholesky factor) and 推理优化与量化算子深度技术调研 §1.3 (a few hundred calibration
+ * samples, 128 typically).  The pages give no value for lambda; 1 % of the mean diagonal is
+ * used.  Computed in float64: a Cholesky factorisation of H with its row and column order
+ * reversed, J H J = L L^T, and U = J L^-1 J (the unique upper factor of H^-1), rounded to
+ * float32 once at the end.  Every sum runs in a fixed order (reproducible run to run).
+ *   X       [n, K] float32 calibration activations (n >= 1).
+ *   U       [K, K] float32 output, row-major, zero below the diagonal.
+ *   workspace / ws_bytes: device scratch of at least wq_gptq_workspace_bytes(K) bytes (about
+ *           16 K^2 bytes: float64 H and its inverse factor); no initialisation needed.
+ * A non-positive Cholesky pivot (H not positive definite, e.g. X all zero) records bit 1 << 6
+ * in the error word (wq_read_error_flags) and leaves NaN in U.
+ * Work: about K^3 float64 multiply-adds (the factorisation and the triangular inverse) plus
+ * n K^2 for H.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless n >= 1, K >= 128, K % 128 == 0, K <= 46208;
+ *         WQ_ERR_ALIGN; WQ_ERR_WORKSPACE; WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+size_t wq_gptq_workspace_bytes(int64_t K);
+wq_status wq_gptq_factor(const float* X, int64_t n, int64_t K, float* U, void* workspace, size_t ws_bytes,
+                         void* stream);
+
+/*
+ * GPTQ end to end from calibration activations: wq_gptq_factor into the workspace, then the
+ * wq_gptq_int4_g128 sweep with that factor.  Arguments, outputs and errors as those two calls;
+ * workspace / ws_bytes at least wq_gptq_workspace_bytes(K) (which includes room for U).
+ */
+wq_status wq_gptq_int4_g128_calib(const float* W, int64_t N, int64_t K, const float* X, int64_t n, int32_t* Wq,
+                                  uint16_t* scales, uint16_t* zeros, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
+/*
  * AWQ: scales the salient input channels of W before INT4 g128 quantization, the scale's
  * exponent chosen by a grid search on calibration activations.
  * Defined by: 第 1 章：推理加速全景 §4.4 (importance_j = mean |X_j| over the calibration set;
@@ -259,6 +293,27 @@ wq_status wq_gemv_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t
 wq_status wq_gemm_tc_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
                                   const int32_t* Wq, const void* scales, const uint16_t* zeros,
                                   uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * The fused QKV projection with its output split into Q, K and V:
+ *   [Q | K | V] = X * dequant([W_Q; W_K; W_V])^T,  Q [M, Nq], K [M, Nkv], V [M, Nkv].
+ * Defined by: 推理优化与量化算子深度技术调研 §4.2 (the fused QKV projection: one GEMM over the
+ * stacked W_Q, W_K, W_V, then the result split into Q, K and V).  The split is done by the
+ * kernels' epilogue, which writes each output column straight to its tensor, so the fused
+ * [M, Nq + 2 Nkv] result is never written.  With grouped-query attention (H_q query heads and
+ * H_kv key/value heads of d_head each) Nq = H_q d_head and Nkv = H_kv d_head.
+ *   X       [M, K] bf16 bits.
+ *   Wq, scales, zeros   the packed stacked weight of N = Nq + 2 Nkv rows (W_Q rows, then W_K,
+ *           then W_V), format fmt, the layouts of wq_gemm_w4a16.
+ *   Yq      [M, Nq], Yk [M, Nkv], Yv [M, Nkv] bf16 bits outputs, row-major, 16-byte aligned,
+ *           three distinct buffers.
+ *   workspace / ws_bytes: at least wq_gemm_workspace_bytes(fmt, M, K, Nq + 2 Nkv) bytes.
+ * Arithmetic, dispatch (T(fmt, K, Nq + 2 Nkv)), errors and workspace rules as wq_gemm_w4a16;
+ * WQ_ERR_SHAPE also unless Nq >= 1 and Nkv >= 1; WQ_ERR_NULL for a NULL output.
+ */
+wq_status wq_gemm_w4a16_qkv(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t Nq, int64_t Nkv,
+                            const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Yq,
+                            uint16_t* Yk, uint16_t* Yv, void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Row re-layout of a stacked [gate; up] array (2F rows of row_bytes bytes each: the packed

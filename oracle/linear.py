@@ -39,6 +39,16 @@ def linear_w4a16(fmt: str, X: np.ndarray, Wq, scales, zeros=None) -> np.ndarray:
     return linear(X, dequantize(fmt, Wq, scales, zeros))
 
 
+def qkv_split(Y: np.ndarray, Nq: int, Nkv: int):
+    """The fused QKV projection's output split into its three parts (推理优化与量化算子深度技术调研
+    §4.2: one GEMM over the stacked [W_Q; W_K; W_V], then the result split into Q, K and V):
+    ``(Y[:, :Nq], Y[:, Nq:Nq+Nkv], Y[:, Nq+Nkv:])`` for ``Y`` [M, Nq + 2 Nkv]."""
+    Y = np.asarray(Y)
+    if Nq < 1 or Nkv < 1 or Y.shape[1] != Nq + 2 * Nkv:
+        raise ValueError("Y must be [M, Nq + 2 Nkv] with Nq, Nkv >= 1")
+    return Y[:, :Nq], Y[:, Nq:Nq + Nkv], Y[:, Nq + Nkv:]
+
+
 def linear_rows(fmt: str, X: np.ndarray, Wq, scales, zeros, rows) -> np.ndarray:
     """Only the output columns ``rows`` (weight rows) of ``Y``: float64 [M, len(rows)].
 

@@ -80,3 +80,60 @@ def test_gptq_rejects_bad_shapes(B):
     W = torch.zeros((4, 256), dtype=torch.float32, device="cuda")
     with pytest.raises(ValueError):
         B.gptq_int4_g128(W, U)                  # U not [K, K]
+
+
+# ------------------------------------------------------------------ the factor on the device
+
+@pytest.mark.parametrize("n,K", [(128, 128), (64, 384), (128, 1024), (1, 512), (128, 2048)])
+def test_gptq_factor_matches_the_oracle(B, n, K):
+    # U with H^-1 = U^T U, H = 2 X^T X + lambda I: the device's float64 factorisation rounded to
+    # float32 once, against the oracle's float64 factor rounded to float32 (within one float32
+    # rounding of it plus float64 noise amplified by the conditioning of H).
+    X = inputs.calibration(K + n, n, K)
+    U = B.gptq_factor(to_dev(X)).cpu().numpy().astype(np.float64)
+    ref = gptq.inverse_cholesky_upper(gptq.hessian(X))
+    assert (np.tril(U, -1) == 0).all(), "U must be upper triangular"
+    assert (np.diag(U) > 0).all(), "U must have a positive diagonal"
+    err = np.abs(U - ref)
+    lim = 2.0 ** -23 * np.abs(ref) + 1e-6 * np.abs(ref).max()
+    assert (err <= lim).all(), "max |U - ref| = %g (%d entries outside)" % (err.max(), int((err > lim).sum()))
+    # and U is a factor of H^-1 in its own right: U^T U H = I
+    H = gptq.hessian(X)
+    R = (U.T @ U) @ H - np.eye(K)
+    assert np.abs(R).max() < 1e-3, "||U^T U H - I||_max = %g" % np.abs(R).max()
+    assert B.read_error_flags() == 0
+
+
+def test_gptq_factor_rejects_a_singular_hessian(B):
+    # All-zero calibration activations: H = 0 (lambda = 0), no Cholesky factor; the device
+    # reports it in the error word instead of faulting
+    import torch
+    X = torch.zeros((16, 256), dtype=torch.float32, device="cuda")
+    U = B.gptq_factor(X)
+    torch.cuda.synchronize()
+    assert B.read_error_flags() & (1 << 6)
+    assert not torch.isfinite(U).all()
+    assert B.read_error_flags() == 0
+
+
+@pytest.mark.parametrize("N,n,K", [(64, 128, 512), (40, 128, 2048)])
+def test_gptq_end_to_end_from_calibration(B, N, n, K):
+    # GPTQ with the factor computed on the device: the sweep is bit-exact against the oracle's
+    # sweep fed the same (device) factor, and the layer's calibration objective
+    # ||X (W_hat - W)^T||^2 is within 0.1 % of the oracle's end-to-end result.
+    W = inputs.weights(N + K, N, K, 0.05)
+    X = inputs.calibration(K + 7, n, K)
+    got = [t.cpu().numpy() for t in B.gptq_int4_g128_calib(to_dev(W), to_dev(X))]
+    U_dev = B.gptq_factor(to_dev(X)).cpu().numpy()
+    _same(got, gptq.sweep(W, U_dev), "sweep with the device factor")
+    ref = gptq.quantize(W, X)
+
+    def objective(pk):
+        W_hat = int4_g128.dequantize(*pk)
+        D = np.asarray(X, np.float64) @ (W_hat - W.astype(np.float64)).T
+        return float((D * D).sum())
+
+    assert objective(got) <= objective(ref) * (1 + 1e-3)
+    codes = int4_g128.unpack(got[0]) == int4_g128.unpack(ref[0])
+    assert codes.mean() > 0.99
+    assert B.read_error_flags() == 0

@@ -387,6 +387,19 @@ def test_linear_brute_force_fractions():
                 assert abs(Fraction(float(Y[m, n])) - exact) <= Fraction(1, 10 ** 12) * (1 + abs(exact))
 
 
+def test_qkv_split_definition():
+    # 推理优化与量化算子深度技术调研 §4.2: Q, K, V are the column blocks of the fused projection,
+    # W_Q rows first.  A hand-built weight whose rows are one-hot (row n selects input n) makes
+    # the fused output the input itself, so each part is a known slice of X.
+    X = np.arange(2 * 12, dtype=np.float64).reshape(2, 12)
+    Y = linear.linear(X, np.eye(12)[[3, 1, 4, 1, 5, 9, 2, 6]])          # Nq = 4, Nkv = 2
+    q, k, v = linear.qkv_split(Y, 4, 2)
+    assert q.tolist() == X[:, [3, 1, 4, 1]].tolist()
+    assert k.tolist() == X[:, [5, 9]].tolist() and v.tolist() == X[:, [2, 6]].tolist()
+    with pytest.raises(ValueError):
+        linear.qkv_split(Y, 4, 3)
+
+
 def test_linear_special_cases():
     M, K, N = 4, 256, 6
     _, X = inputs.activations(41, M, K)
