@@ -38,21 +38,25 @@ uint32_t gemm_tc_read_and_clear_error() {
 namespace tc {
 
 constexpr int BN = 128;          // weight rows per tile (MMA M)
-constexpr int BM = 256;          // activation rows per tile (MMA N)
 constexpr int BK = 64;           // k per stage (one 128-byte swizzle row of 16-bit X)
-constexpr int kStages = 6;
-constexpr int kXBytes = BM * BK * 2;        // 32 KB
 constexpr int kWBytes = BN * BK / 2;        // 4 KB packed weights
 constexpr int kDequantSets = 3;             // dequant warp sets, alternating stages
 constexpr int kThreads = 64 + 128 * kDequantSets;   // producer + MMA warp + 4 dequant warps per set
 constexpr int kTmemCols = 512;
-constexpr int kAccCol = 0;                  // D: columns [0, 256)
-constexpr int kACol = 256;                  // A stage s: columns [256 + 32 s, +32)
+constexpr int kAccCol = 0;                  // D: columns [0, BMT)
 constexpr int kGroupM = 8;                  // tile raster: 8 activation tiles per group
 
-static_assert(kACol + 32 * kStages <= kTmemCols, "the A stages must fit the tensor-memory allocation");
+// Activation rows per tile (MMA N) BMT: 256 for prefill, 128 or 64 when M is that small, so
+// that a stage's activation tile (BMT x 64 k, TMA with SWIZZLE_128B) carries no zero rows.
+// Smaller tiles leave room for more stages.
+__host__ __device__ constexpr int stages_for(int bmt) { return bmt == 256 ? 6 : (bmt == 128 ? 8 : 10); }
 
+template <int BMT>
 struct Smem {
+  static constexpr int kStages = stages_for(BMT);
+  static constexpr int kXBytes = BMT * BK * 2;
+  static constexpr int kACol = BMT;         // A stage s: columns [BMT + 32 s, +32)
+  static_assert(kACol + 32 * kStages <= kTmemCols, "the A stages must fit the tensor-memory allocation");
   uint8_t x[kStages][kXBytes];    // 1024-aligned (SWIZZLE_128B atoms)
   uint8_t w[kStages][kWBytes];
   uint64_t full[kStages];
@@ -60,7 +64,7 @@ struct Smem {
   uint64_t empty[kStages];
   uint64_t accum_full;
   uint32_t tmem_base;
-  int second;            // split tile: this CTA finished second and writes the outputs
+  int last;              // split tile: this CTA finished last and writes the outputs
 };
 
 struct Params {
@@ -73,11 +77,11 @@ struct Params {
   int KB;                // MXFP4 scale bytes per row (K / 32)
   int G;                 // INT4 groups per row (K / 128)
   int tiles_n, tiles_m;
-  int full_tiles;        // tiles [0, full_tiles) run whole; each later tile as two K halves
-  int split_stage;       // first stage of a split tile's second half
+  int full_tiles;        // tiles [0, full_tiles) run whole; each later tile as `splits` K parts
+  int splits;            // K parts per split tile (part q: stages [q KS / splits, (q + 1) KS / splits))
   int k_stages;          // ceil(K / BK)
   uint32_t* cnt;         // split tiles: one counter each (workspace header, left at zero)
-  float* part;           // split tiles: [tile][half][BN][BM] fp32 partial accumulators
+  float* part;           // split tiles: [tile][part][BN][BMT] fp32 partial accumulators
 };
 
 // ------------------------------------------------------------------------ tcgen05 helpers
@@ -148,9 +152,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulate, A/B K-major, M = 128, N = 256.
-// Instruction descriptor, kind::f16: fp32 accumulate, A/B both fp16 or both bf16, MMA N = n
-// (activation rows: BM for a whole tile, BM / 2 for a half tile), M = BN.
+// Instruction descriptor, kind::f16: fp32 accumulate, A/B K-major, A/B both fp16 or both bf16,
+// MMA N = n (the activation rows of a tile, BMT), M = BN.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt /*0 f16, 1 bf16*/, uint32_t n) {
   return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((n >> 3) << 17) | ((uint32_t(BN) >> 4) << 24);
 }
@@ -220,28 +223,33 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_n, int tiles_m, int
   tn = r / gsize;
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int BMT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
               const Params p) {
+  using S = Smem<BMT>;
+  constexpr int kStages = S::kStages;
+  constexpr int kXBytes = S::kXBytes;
+  constexpr int kACol = S::kACol;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + smem_align_pad(smem_raw));
+  S& sm = *reinterpret_cast<S*>(smem_raw + smem_align_pad(smem_raw));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Tiles past full_tiles (the last, partial wave) run split along K on two CTAs, stages
-  // [0, split_stage) and [split_stage, k_stages), so that wave ends in about half the time.
-  // Each half stores its fp32 accumulator; the second to finish adds the other's and writes Y.
-  int t = blockIdx.x, half = -1;
+  // Tiles past full_tiles run split along K on `splits` CTAs (the last, partial wave of a
+  // prefill layer in two; every tile of a layer with too few tiles for the SMs in up to
+  // eight), so that every SM has work.  Each part stores its fp32 accumulator; the last to
+  // finish adds all parts in part order (deterministic) and writes Y.
+  int t = blockIdx.x, part = -1;
   if (t >= p.full_tiles) {
     const int j = t - p.full_tiles;
-    t = p.full_tiles + (j >> 1);
-    half = j & 1;
+    t = p.full_tiles + j / p.splits;
+    part = j % p.splits;
   }
   int tn, tm;
   tile_coords(t, p.tiles_n, p.tiles_m, tn, tm);
-  const int n0 = tn * BN, m0 = tm * BM;
-  const int kb = half == 1 ? p.split_stage : 0;                     // first stage of this CTA
-  const int KS = (half == 0 ? p.split_stage : p.k_stages) - kb;      // stages this CTA runs
+  const int n0 = tn * BN, m0 = tm * BMT;
+  const int kb = part < 0 ? 0 : (part * p.k_stages) / p.splits;                      // first stage
+  const int KS = (part < 0 ? p.k_stages : ((part + 1) * p.k_stages) / p.splits) - kb;   // stages
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -260,6 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // Programmatic dependent launch: the set-up above overlaps the previous kernel's tail; every
+  // read of global memory comes after the wait (the MMA warp reads none).
+  pdl_launch_dependents();
+  if (warp != 1) pdl_wait();
 
   if (warp == 0) {
     // -------------------------------------------------------------- TMA producer
@@ -285,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u, static_cast<uint32_t>(BM));
+      const uint32_t idesc = idesc_f16(FMT == kInt4G128 ? 0u : 1u, static_cast<uint32_t>(BMT));
       bool ok = true;
       for (int i = 0; i < KS; ++i) {
         const int s = i % kStages;
@@ -395,15 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (epi_bar_and(ready)) {
       tc_fence_after();
       bool write_y = true;
-      const float* other = nullptr;
-      if (half >= 0) {
-        // this half's accumulator to its slot; then one GPU-scope counter update per CTA
-        // (release: after the barrier, covers every thread's stores) tells the second CTA to
+      const float* parts = nullptr;   // split tile, last CTA: this row's partial sums, part 0
+      if (part >= 0) {
+        // this part's accumulator to its slot; then one GPU-scope counter update per CTA
+        // (release: after the barrier, covers every thread's stores) tells the last CTA to
         // finish the tile
-        const long long slot = static_cast<long long>(t - p.full_tiles) * 2;
-        float* mine = p.part + (slot + half) * (BN * BM) + static_cast<long long>(r) * BM;
+        const long long slot = static_cast<long long>(t - p.full_tiles) * p.splits;
+        float* mine = p.part + (slot + part) * (BN * BMT) + static_cast<long long>(r) * BMT;
 #pragma unroll 1
-        for (int c = 32 * set; c < BM; c += 32 * kDequantSets) {
+        for (int c = 32 * set; c < BMT; c += 32 * kDequantSets) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + kAccCol + c, v);
           tc_wait_ld();
@@ -417,31 +429,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 64) {
           uint32_t* c = p.cnt + (t - p.full_tiles);
           const uint32_t old = atom_add_acq_rel_gpu(c, 1u);
-          sm.second = old == 1u ? 1 : 0;
-          if (old == 1u) atomicExch(c, 0u);   // ready for the next call
+          sm.last = old == static_cast<uint32_t>(p.splits - 1) ? 1 : 0;
+          if (sm.last) atomicExch(c, 0u);   // ready for the next call
         }
         epi_bar();
-        write_y = sm.second != 0;
+        write_y = sm.last != 0;
         if (write_y) {
           __threadfence();
-          other = p.part + (slot + (1 - half)) * (BN * BM) + static_cast<long long>(r) * BM;
+          parts = p.part + slot * (BN * BMT) + static_cast<long long>(r) * BMT;
         }
       }
 #pragma unroll 1
-      for (int c = 32 * set; c < BM && write_y; c += 32 * kDequantSets) {
+      for (int c = 32 * set; c < BMT && write_y; c += 32 * kDequantSets) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kAccCol + c, v);
         tc_wait_ld();
-        if (other) {
-          // the two halves' sum: a two-term fp32 sum, the same whichever half finished first
-          const float4* src = reinterpret_cast<const float4*>(other + c);
+        if (parts) {
+          if (p.splits == 2) {
+            // two parts: this CTA's accumulator plus the other's, a two-term fp32 sum that is
+            // the same whichever part finished last
+            const float4* src = reinterpret_cast<const float4*>(parts + static_cast<long long>(1 - part) * (BN * BMT) + c);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float4 o = __ldcg(src + u);
-            v[4 * u + 0] = __float_as_uint(__uint_as_float(v[4 * u + 0]) + o.x);
-            v[4 * u + 1] = __float_as_uint(__uint_as_float(v[4 * u + 1]) + o.y);
-            v[4 * u + 2] = __float_as_uint(__uint_as_float(v[4 * u + 2]) + o.z);
-            v[4 * u + 3] = __float_as_uint(__uint_as_float(v[4 * u + 3]) + o.w);
+            for (int u = 0; u < 8; ++u) {
+              const float4 o = __ldcg(src + u);
+              v[4 * u + 0] = __float_as_uint(__uint_as_float(v[4 * u + 0]) + o.x);
+              v[4 * u + 1] = __float_as_uint(__uint_as_float(v[4 * u + 1]) + o.y);
+              v[4 * u + 2] = __float_as_uint(__uint_as_float(v[4 * u + 2]) + o.z);
+              v[4 * u + 3] = __float_as_uint(__uint_as_float(v[4 * u + 3]) + o.w);
+            }
+          } else {
+            // more parts: all of them from the workspace, added in part order (the same bits
+            // whichever part finished last); each part's loads are issued before any addition
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 o[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (q < p.splits)
+                  o[q] = __ldcg(reinterpret_cast<const float4*>(parts + static_cast<long long>(q) * (BN * BMT) + c) + u);
+              float4 a = o[0];
+#pragma unroll
+              for (int q = 1; q < 8; ++q)
+                if (q < p.splits) {
+                  a.x += o[q].x;
+                  a.y += o[q].y;
+                  a.z += o[q].z;
+                  a.w += o[q].w;
+                }
+              v[4 * u + 0] = __float_as_uint(a.x);
+              v[4 * u + 1] = __float_as_uint(a.y);
+              v[4 * u + 2] = __float_as_uint(a.z);
+              v[4 * u + 3] = __float_as_uint(a.w);
+            }
           }
         }
         if constexpr (EPI == kEpiSwiglu) {
@@ -497,6 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // from L2.
 __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X, int K, uint16_t* __restrict__ Xh,
                                                   float* __restrict__ xs) {
+  pdl_launch_dependents();
+  pdl_wait();   // X may come from the previous kernel of the stream
   const int m = blockIdx.x;
   const uint4* row = reinterpret_cast<const uint4*>(X + static_cast<long long>(m) * K);
   uint4* out = reinterpret_cast<uint4*>(Xh + static_cast<long long>(m) * K);
@@ -536,24 +577,83 @@ __global__ void __launch_bounds__(256) k_x_to_f16(const uint16_t* __restrict__ X
 
 namespace {
 
-// Tiles of the last, partial wave that run split along K (0: none): when that wave fits in
-// half the SMs and a tile has at least two stages.
-long long split_tiles(int64_t M, int64_t K, int64_t N) {
+// The launch plan: the activation tile (MMA N) the rows of M need, and which tiles run split
+// along K on how many CTAs.  A layer with too few tiles for half the SMs (decode-sized to
+// mid-sized M) splits every tile, up to 8 ways with at least 8 stages each; otherwise the
+// tiles of a last, partial wave that fits in half the SMs split in two.
+struct TcPlan {
+  int bmt, tiles_n, tiles_m, k_stages, splits;
+  long long tiles, nsplit;
+};
+
+TcPlan plan_tc(int64_t M, int64_t K, int64_t N) {
   using namespace tc;
-  const long long tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+  TcPlan pl{};
+  pl.bmt = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  pl.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  pl.tiles_m = static_cast<int>((M + pl.bmt - 1) / pl.bmt);
+  pl.k_stages = static_cast<int>((K + BK - 1) / BK);
+  pl.tiles = static_cast<long long>(pl.tiles_n) * pl.tiles_m;
   const long long sms = device_sm_count();
-  const long long rem = tiles % sms;
-  const long long ks = (K + BK - 1) / BK;
-  return (rem > 0 && 2 * rem <= sms && ks >= 2) ? rem : 0;
+  pl.splits = 1;
+  pl.nsplit = 0;
+  if (2 * pl.tiles <= sms) {
+    long long s = sms / pl.tiles;
+    if (s > pl.k_stages / 8) s = pl.k_stages / 8;
+    if (s > 8) s = 8;
+    if (s >= 2) {
+      pl.splits = static_cast<int>(s);
+      pl.nsplit = pl.tiles;
+      return pl;
+    }
+  }
+  const long long rem = pl.tiles % sms;
+  if (rem > 0 && 2 * rem <= sms && pl.k_stages >= 2) {
+    pl.splits = 2;
+    pl.nsplit = rem;
+  }
+  return pl;
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+template <int FMT, int BMT>
+void (*pick_kernel(int epi))(CUtensorMap, CUtensorMap, tc::Params) {
+  return epi == kEpiSwiglu ? tc::k_gemm_tc<FMT, kEpiSwiglu, BMT>
+                           : (epi == kEpiSplit3 ? tc::k_gemm_tc<FMT, kEpiSplit3, BMT> : tc::k_gemm_tc<FMT, kEpiNone, BMT>);
+}
+
+template <int BMT>
+cudaError_t launch_tc_t(int fmt, int epi, const CUtensorMap& tx, const CUtensorMap& tw, const tc::Params& p,
+                        unsigned grid, cudaStream_t stream) {
+  static_assert(sizeof(tc::Smem<BMT>) + 1024 <= 227 * 1024, "tensor-core kernel shared memory over the per-CTA limit");
+  const size_t smem = sizeof(tc::Smem<BMT>) + 1024;
+  void (*kern)(CUtensorMap, CUtensorMap, tc::Params) =
+      fmt == kInt4G128 ? pick_kernel<kInt4G128, BMT>(epi) : pick_kernel<kMxfp4, BMT>(epi);
+  cudaError_t e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
+  if (e != cudaSuccess) return e;
+  // Programmatic stream serialization: the CTAs may start (barrier set-up, tensor-memory
+  // allocation) while the previous kernel of the stream is still running; every read of
+  // global memory comes after griddepcontrol.wait.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tx, tw, p);
+}
 
 }  // namespace
 
 size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   using namespace tc;
-  const size_t part = static_cast<size_t>(split_tiles(M, K, N)) * 2 * BN * BM * sizeof(float);
+  const TcPlan pl = plan_tc(M, K, N);
+  const size_t part = static_cast<size_t>(pl.nsplit) * pl.splits * BN * pl.bmt * sizeof(float);
   if (fmt != kInt4G128) return part ? kWsCounterBytes + part : 0;
   const size_t xh = round256(static_cast<size_t>(M) * K * 2);
   return kWsCounterBytes + xh + round256(static_cast<size_t>(M) * 4) + part;
@@ -566,6 +666,7 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
   if (epi == kEpiSplit3 && !split) return cudaErrorInvalidValue;
   if (ws_bytes < gemm_tc_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
+  const TcPlan pl = plan_tc(M, K, N);
   Params p{};
   p.scales = scales;
   p.zeros = zeros;
@@ -576,17 +677,14 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   p.N = static_cast<int>(N);
   p.KB = static_cast<int>(K / 32);
   p.G = static_cast<int>(K / 128);
-  p.tiles_n = static_cast<int>((N + BN - 1) / BN);
-  p.tiles_m = static_cast<int>((M + BM - 1) / BM);
-  p.k_stages = static_cast<int>((K + BK - 1) / BK);
-
-  const long long nsplit = split_tiles(M, K, N);
-  const long long tiles = static_cast<long long>(p.tiles_n) * p.tiles_m;
-  p.full_tiles = static_cast<int>(tiles - nsplit);
-  p.split_stage = p.k_stages / 2;
+  p.tiles_n = pl.tiles_n;
+  p.tiles_m = pl.tiles_m;
+  p.k_stages = pl.k_stages;
+  p.full_tiles = static_cast<int>(pl.tiles - pl.nsplit);
+  p.splits = pl.splits;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = nullptr;
-  if (nsplit) {
+  if (pl.nsplit) {
     size_t off = kWsCounterBytes;
     if (fmt == kInt4G128) off += round256(static_cast<size_t>(M) * K * 2) + round256(static_cast<size_t>(M) * 4);
     p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + off);
@@ -596,8 +694,16 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
     uint8_t* base = reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes;  // never touch the counter header
     uint16_t* Xh = reinterpret_cast<uint16_t*>(base);
     float* xs = reinterpret_cast<float*>(base + ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256);
-    k_x_to_f16<<<static_cast<unsigned>(M), 256, 0, stream>>>(X, static_cast<int>(K), Xh, xs);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(M));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_x_to_f16, X, static_cast<int>(K), Xh, xs);
     if (e != cudaSuccess) return e;
     xsrc = Xh;
     p.xscale = xs;
@@ -605,25 +711,17 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   CUtensorMap tx, tw;
   cudaError_t e = make_tmap_2d(&tx, fmt == kInt4G128 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                xsrc, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2,
-                               BK, BM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                               BK, static_cast<uint32_t>(pl.bmt), CU_TENSOR_MAP_SWIZZLE_128B,
+                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
   e = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(N),
                    static_cast<uint64_t>(K / 2), BK / 2, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e != cudaSuccess) return e;
-  static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "tensor-core kernel shared memory over the per-CTA limit");
-  const size_t smem = sizeof(Smem) + 1024;
-  const unsigned grid = static_cast<unsigned>(p.full_tiles + 2 * nsplit);
-  void (*kern)(CUtensorMap, CUtensorMap, Params) =
-      fmt == kInt4G128
-          ? (epi == kEpiSwiglu ? k_gemm_tc<kInt4G128, kEpiSwiglu>
-                               : (epi == kEpiSplit3 ? k_gemm_tc<kInt4G128, kEpiSplit3> : k_gemm_tc<kInt4G128, kEpiNone>))
-          : (epi == kEpiSwiglu ? k_gemm_tc<kMxfp4, kEpiSwiglu>
-                               : (epi == kEpiSplit3 ? k_gemm_tc<kMxfp4, kEpiSplit3> : k_gemm_tc<kMxfp4, kEpiNone>));
-  e = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(tx, tw, p);
-  return cudaGetLastError();
+  const unsigned grid = static_cast<unsigned>(p.full_tiles + pl.nsplit * pl.splits);
+  if (pl.bmt == 64) return launch_tc_t<64>(fmt, epi, tx, tw, p, grid, stream);
+  if (pl.bmt == 128) return launch_tc_t<128>(fmt, epi, tx, tw, p, grid, stream);
+  return launch_tc_t<256>(fmt, epi, tx, tw, p, grid, stream);
 }
 
 }  // namespace wq

@@ -45,6 +45,36 @@ def test_gemm_tc_small(B, fmt, M, N, K):
     assert_close(y_to_host(Y), linear.linear_w4a16(fmt, xf, *pk), "%s M=%d N=%d K=%d" % (fmt, M, N, K))
 
 
+# Mid-sized M: the activation tile is 64, 128 or 256 rows (M <= 64, <= 128, above), and
+# layers with few tiles split every tile along K over up to 8 CTAs; (M, N, K) straddle the
+# tile boundaries and give 2-, 4- and 8-way splits.
+MID = [(33, 1024, 2048), (64, 256, 4096), (65, 512, 4096), (128, 384, 1024), (129, 256, 2048), (200, 640, 8192)]
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M,N,K", MID)
+def test_gemm_tc_mid_m(B, fmt, M, N, K):
+    W = inputs.weights(N * 11 + K + M, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M * 7 + K, M, K)
+    Y = _run(B.gemm_tc_w4a16, fmt, xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16(fmt, xf, *pk), "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+    assert B.read_error_flags() == 0
+
+
+def test_gemm_tc_split_k_deterministic(B):
+    # every tile split 8 ways along K: the last CTA adds the parts in part order, so two calls
+    # give the same bits whichever part finishes last
+    M, N, K = 64, 256, 4096
+    W = inputs.weights(21, N, K, 0.05)
+    pk = int4_g128.quantize(W)
+    xb, xf = inputs.activations(22, M, K)
+    y1 = y_to_host(_run(B.gemm_tc_w4a16, "int4_g128", xb, pk))
+    y2 = y_to_host(_run(B.gemm_tc_w4a16, "int4_g128", xb, pk))
+    assert np.array_equal(y1, y2)
+    assert_close(y1, linear.linear_w4a16("int4_g128", xf, *pk), "split-K")
+
+
 @pytest.mark.parametrize("K", [32, 96, 160])
 def test_gemm_tc_mxfp4_k_tail(B, K):
     M, N = 100, 300
