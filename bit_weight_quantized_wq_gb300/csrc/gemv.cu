@@ -10,29 +10,39 @@
 //               groups of INT4 / 256 k of MXFP4), SWIZZLE_128B, into a 4- or 5-stage smem
 //               ring, with the matching scale / zero-point (INT4) or E8M0 (MXFP4) tiles.
 //   warps 1-3   prep (stage i by prep warp i % 3), on a separate 6-stage ring: the
-//               activations of the stage's k-range (from L2; they are small and shared by
-//               every CTA) in the exact order of the mma.sync B fragments, with their
-//               per-group sums (INT4) or converted to fp16 with a per-row power-of-two scale
-//               that keeps every value in fp16 range (MXFP4).  The activations do not depend
-//               on the weights, so this runs ahead of the weight stream.
+//               activations of the stage's k-range, loaded straight from global memory (L2;
+//               they are small and shared by every CTA) and written in the exact order of
+//               the mma.sync B fragments, with their per-group sums (INT4) or converted to
+//               fp16 with a per-row power-of-two scale that keeps every value in fp16 range
+//               (MXFP4).  The activations do not depend on the weights, so this runs ahead
+//               of the weight stream.
 //   warps 4-19  consumers: 16 weight rows each; per-row metadata straight from its tile,
 //               nibbles unpacked in registers, tensor-core mma.sync with fp32 accumulation,
 //               group scale applied in fp32 afterwards.
 //
-// Exactness: the tensor-core operands are exact small integers (INT4: 128 + q in bf16) or
-// exact E2M1 values (MXFP4, fp16); every product is exact and the per-group (INT4) or
-// per-32 (MXFP4) scale is applied to the fp32 partial sum.  No operand is rounded to 16
-// bits, which keeps the layer within 1e-2 (1 + |y|) of the float64 oracle at every K (a
-// bf16-rounded dequantised weight would not).  INT4 per group and output:
-//   sum_k (q - z) s x = s * sum_k (128 + q) x  -  s (128 + z) * sum_k x,
-// i.e. the zero-point cross term of 第 6 课：量化源码走读 §3 is compensated with the group sum of
-// the activations instead of subtracting z from every weight.
+// Exactness: the tensor-core operands are exact: the weights as small integers or E2M1
+// values, the activations as bf16 or as fp16 after a power-of-two scale per stage and row;
+// every product is exact and the per-group (INT4) or per-32 (MXFP4) scale is applied to the
+// fp32 partial sum.  No operand is rounded to 16 bits, which keeps the layer within
+// 1e-2 (1 + |y|) of the float64 oracle at every K (a bf16-rounded dequantised weight would
+// not).  INT4 per group and output, the zero-point cross term of 第 6 课：量化源码走读 §3
+// compensated with group sums of the activations instead of subtracting z from every weight:
+//   up to 8 activation rows, fp16 1024 + q (1024 + 16 q for the odd nibble of a byte, one
+//   shift saved per word; those activations carry 1/16), x' = x 2^-e, B' the B operand:
+//     sum_k (q - z) s x = 2^e s (sum_k A' B' - 1024 sum_k B' - z sum_k x')
+//   16 rows, bf16 128 + q and the raw activations:
+//     sum_k (q - z) s x = s sum_k (128 + q) x - s (128 + z) sum_k x
 //
 // Work split: the (256-row band, 256-k group pair) units -- one per pipeline stage -- are
-// split evenly over the CTAs in band-major order.  A band covered by one CTA is written directly as bf16; a band shared
-// by several CTAs is reduced through the workspace (fp32 partials + one counter per band,
-// deterministic order: the last CTA to finish sums the partials in CTA order, writes bf16
-// and resets the counter).
+// split evenly over the CTAs in band-major order (the host computes each CTA's range).  A
+// band covered by one CTA is written directly as bf16.  A band shared by several CTAs is
+// reduced by the CTA holding its first unit: that range ends inside the band, so it
+// finishes the band last, while every other contributor starts its range inside the band
+// and posts its fp32 partial sums early (one release-ordered counter increment per warp).
+// The reducer adds the partial sums to its own in CTA order (deterministic), writes bf16
+// and resets the band's counter for the next call.  A reducer only ever waits on CTAs of
+// higher index, which post before they wait themselves, so the wait always ends as long as
+// those CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is bounded).
 #include <mutex>
 
 #include "decode_util.cuh"
@@ -67,12 +77,13 @@ constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 640
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
 constexpr int kSmemLimit = 227 * 1024;               // dynamic shared memory per CTA
 constexpr int kSmemReserve = 1024 + 512;             // alignment pad + barriers and flags
+constexpr int kMaxCtas = 160;                        // CTAs per launch (one per SM, at most)
 
 // Raw metadata tile(s) per weight stage: INT4 scales + zeros boxes of 8 groups x 256 rows
 // (fp16); MXFP4 one box of 16 E8M0 bytes x 256 rows.
 __host__ __device__ constexpr int meta_raw_bytes(int fmt) { return fmt == kInt4G128 ? 2 * kBand * 16 : kBand * 16; }
 // One activation stage: B fragments + per-row group sums + per-row power-of-two factors.
-__host__ __device__ constexpr int x_stage_bytes(int mt) { return (mt / 8) * 2 * 4 * 32 * 16 + 2 * mt * 4 + mt * 4; }
+__host__ __device__ constexpr int x_stage_bytes(int mt) { return (mt / 8) * 2 * 4 * 32 * 16 + 4 * mt * 4 + mt * 4; }
 // Weight stages: as many as fit beside the activation ring (4 or 5).
 __host__ __device__ constexpr int w_stages(int fmt, int mt) {
   return (kSmemLimit - kSmemReserve - kXStages * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt)) > 6
@@ -86,25 +97,18 @@ struct Params {
   const uint16_t* zeros;
   uint16_t* Y;
   OutSplit split;     // EPI == kEpiSplit3: three output tensors by column range
-  float* part;        // [P][2][MT][kBand] fp32 partials
-  uint32_t* cnt;      // [bands] counters
+  float* part;        // [P][MT][kBand] fp32 partial sums of each CTA's first band
+  uint32_t* cnt;      // [bands] counters (warps of other CTAs that posted their partial sums)
   int M, K, N;
   int G;              // 128-k groups per row (ceil(K / 128))
   int GP;             // group pairs per row (ceil(G / 2)) -- one pair per stage
   int KB;             // MXFP4: scale bytes per row (K / 32)
   int bands;
-  long long U;        // bands * GP units (one unit = one stage)
+  int U;              // bands * GP units (one unit = one stage)
   int P;              // CTAs
   int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: consumers gather them
+  int ustart[kMaxCtas + 1];   // CTA c owns units [ustart[c], ustart[c + 1])
 };
-
-// The CTAs that share a band: [c_lo, c_hi].  CTA c_lo holds the band's first unit; every
-// later contributor starts inside the band (partial slot 0); c_lo uses slot 1 when its range
-// started in an earlier band (lo_side).
-struct BandContrib { int c_lo, c_hi, lo_side; };
-
-
-__device__ __forceinline__ long long unit_start(long long U, int P, int c) { return (U * c) / P; }
 
 template <int FMT, int MT>
 struct Smem {
@@ -112,25 +116,16 @@ struct Smem {
   static constexpr int WS = w_stages(FMT, MT);
   uint8_t w[WS][kTileBytes];                 // SWIZZLE_128B weight tiles (1024-aligned)
   uint8_t mraw[WS][meta_raw_bytes(FMT)];     // raw metadata tiles (TMA), 16 B per row per tensor
-  // B fragments [nt][group][vec][lane].  A stage's raw activations (MT rows x 256 k bf16, row m
-  // at byte 512 m -- the same size) land here by TMA and are converted in place.
+  // B fragments [nt][group][vec][lane]
   uint4 x[kXStages][NT][2][4][32];
-  float xsum[kXStages][2][MT];               // INT4: sum of the group's activations per row m
-  float xf[kXStages][MT];                    // MXFP4: power-of-two factor per activation row
+  float xsum[kXStages][2][MT];               // INT4: sum of the group's scaled activations per row m
+  float xoff[kXStages][2][MT];               // INT4: 1024 x the sum of the group's B operand per row m
+  float xf[kXStages][MT];                    // power-of-two factor per activation row
   uint64_t full_w[WS];
   uint64_t empty_w[WS];
-  uint64_t raw_x[kXStages];                  // the stage's raw activation rows landed (TMA)
   uint64_t full_x[kXStages];
   uint64_t empty_x[kXStages];
-  uint64_t prep_done;                        // every prep thread arrives once it has no tail left
-  // Split-K reductions this CTA must perform (a CTA has at most two partial bands): slot k
-  // holds band + 1 once posted (release), 0 before; slots are claimed in order via req_alloc.
-  int req_band[2];
-  int req_alloc;
-  // contributors of the CTA's first and last band (the only ones it can share), computed at
-  // start-up off the critical path
-  int ci_band[2];
-  BandContrib ci[2];
+  int reduce_ok;                             // the reducer's wait for the other CTAs ended
 };
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
@@ -139,45 +134,27 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
-// Counter update that publishes (release) this CTA's partial sums and, for the last
-// contributor, makes every other contributor's partial sums visible (acquire), at GPU scope.
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
+// Split-K publication: a contributor warp's partial sums are ordered before its counter
+// increment (release, GPU scope); the reducer reads the counter with acquire semantics before
+// it reads the partial sums.
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-
-__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
-
-__device__ __forceinline__ void st_release_cta(int* p, int v) {
-  asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_acquire_cta(const int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
-// Contributors to a band: the CTAs whose unit range meets it, [c_lo, c_hi] (see BandContrib).
-
-__device__ BandContrib band_contributors(const Params& p, int band) {
-  const long long bs = static_cast<long long>(band) * p.GP, be = bs + p.GP;
-  int c_lo = static_cast<int>((bs * p.P) / p.U);
-  while (c_lo > 0 && unit_start(p.U, p.P, c_lo) > bs) --c_lo;
-  while (unit_start(p.U, p.P, c_lo + 1) <= bs) ++c_lo;
-  int c_hi = static_cast<int>(((be - 1) * p.P) / p.U);
-  while (c_hi > c_lo && unit_start(p.U, p.P, c_hi) > be - 1) --c_hi;
-  while (c_hi + 1 < p.P && unit_start(p.U, p.P, c_hi + 1) <= be - 1) ++c_hi;
-  return BandContrib{c_lo, c_hi, unit_start(p.U, p.P, c_lo) < bs ? 1 : 0};
-}
-
-// One share of the deterministic split-K reduction of a band: the partial sums of every
-// contributing CTA, added in CTA order, for the float4 slots idx = first, first + step, ...
-// of the M x kBand outputs; bf16 results to Y.
+// One share of the reduction of a shared band by its reducer CTA: for the float4 slots idx =
+// first, first + step, ... of the M x kBand outputs, the reducer's own partial sums (`own`,
+// shared memory, [MT][kBand]) plus those of CTAs c_lo + 1 .. c_hi (global, in CTA order:
+// deterministic); bf16 results to the outputs.
 template <int MT, int EPI>
-__device__ __forceinline__ void reduce_band_share(const Params& p, int band, BandContrib bc, int first, int step) {
-  const long long cstride = 2LL * MT * kBand;   // floats between two CTAs' partial slots
-  [[maybe_unused]] const unsigned am = __activemask();   // the whole warp unless a wait timed out
+__device__ __forceinline__ void reduce_band_share(const Params& p, int band, const float* own, int c_lo, int c_hi,
+                                                  int first, int step) {
   for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
     int m, r4;
     if constexpr (EPI == kEpiSwiglu) {
@@ -190,17 +167,17 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, Ban
       m = idx / (kBand / 4);
       r4 = 4 * (idx % (kBand / 4));
     }
+    float4 acc4 = *reinterpret_cast<const float4*>(own + m * kBand + r4);
     const float* base = p.part + static_cast<long long>(m) * kBand + r4;
-    float4 acc4 = ld_cg_f32x4(base + (static_cast<long long>(bc.c_lo) * 2 + bc.lo_side) * MT * kBand);
-    for (int c = bc.c_lo + 1; c <= bc.c_hi; c += 8) {
+    for (int c = c_lo + 1; c <= c_hi; c += 8) {
       float4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        v[q] = (c + q <= bc.c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * cstride)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = (c + q <= c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * MT * kBand)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (c + q <= bc.c_hi) {
+        if (c + q <= c_hi) {
           acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
         }
     }
@@ -210,7 +187,7 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, Ban
       // warps run each iteration, so the shuffles below are converged
       float u4[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) u4[q] = __shfl_xor_sync(am, o4[q], 1);
+      for (int q = 0; q < 4; ++q) u4[q] = __shfl_xor_sync(0xffffffffu, o4[q], 1);
       if ((idx & 1) == 0) {
         const int F = p.N >> 1;
 #pragma unroll
@@ -235,21 +212,56 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, Ban
   }
 }
 
+// The bf16 outputs of one consumer lane: rows r0 / r1 of the band, activation rows
+// 2t + (e & 1) + 8 nt.  SwiGLU: r1 = r0 + 8 is the up row of the gate row r0 (the
+// interleaved layout), one output column per pair.
+template <int MT, int EPI>
+__device__ __forceinline__ void store_outputs(const Params& p, int band, int r0, int r1, int t,
+                                              const float (&acc)[MT / 8][4]) {
+  constexpr int NT = MT / 8;
+  if constexpr (EPI == kEpiSwiglu) {
+    const int n = band * kBand + r0;
+    const int F = p.N >> 1;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = 2 * t + e + 8 * nt;
+        if (m < p.M && n < p.N)
+          p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
+              __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(acc[nt][e]) * acc[nt][e + 2]));
+      }
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int m = 2 * t + (e & 1) + 8 * nt;
+        const int n = band * kBand + ((e >> 1) ? r1 : r0);
+        if (m < p.M && n < p.N) {
+          const uint16_t y = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
+          if constexpr (EPI == kEpiSplit3) store_split3(p.split, m, n, y);
+          else p.Y[static_cast<long long>(m) * p.N + n] = y;
+        }
+      }
+  }
+}
+
 // Stage i of a CTA = unit u0 + i = (band, group pair j).  Ranges are split at pair
 // boundaries, so a stage never straddles a band.  The cursor divides once at start-up and
-// then steps incrementally (64-bit division is a long software sequence on the GPU).
+// then steps incrementally.
 struct Cursor {
-  long long u, u0, u1, seg_start, seg_end;
-  int band, j, GP, G;
+  int u, u0, u1, seg_start, seg_end;
+  int band, j, GP;
   __device__ void set_seg() {
-    const long long bs = static_cast<long long>(band) * GP;
+    const int bs = band * GP;
     seg_start = bs > u0 ? bs : u0;
     seg_end = bs + GP < u1 ? bs + GP : u1;
   }
-  __device__ void init(long long a, long long b, int gp, int g) {
-    u = a; u0 = a; u1 = b; GP = gp; G = g;
-    band = static_cast<int>(a / gp);
-    j = static_cast<int>(a - static_cast<long long>(band) * gp);
+  __device__ void init(int a, int b, int gp) {
+    u = a; u0 = a; u1 = b; GP = gp;
+    band = a / gp;
+    j = a - band * gp;
     set_seg();
   }
   __device__ bool seg_last() const { return u + 1 == seg_end; }    // last stage of this band here
@@ -262,20 +274,23 @@ struct Cursor {
 template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemv(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
-           const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_x,
-           const Params p) {
+           const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ Params p) {
   using S = Smem<FMT, MT>;
   constexpr int NT = MT / 8;
   constexpr int WS = S::WS;
+  // INT4 operand form: fp16 (1024 + q | 1024 + 16 q, scaled activations) for 8-row activation
+  // tiles, where it saves unpack instructions; bf16 (128 + q, raw activations) for 16-row
+  // tiles, where each unpacked weight feeds two MMAs and the leaner activation prep wins.
+  constexpr bool kF16 = (FMT == kInt4G128) && (MT == 8);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>(smem_raw + smem_align_pad(smem_raw));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int cta = blockIdx.x;
-  const long long u0 = unit_start(p.U, p.P, cta);
-  const long long u1 = unit_start(p.U, p.P, cta + 1);
-  const int nstages = static_cast<int>(u1 - u0);
+  const int u0 = p.ustart[cta];
+  const int u1 = p.ustart[cta + 1];
+  const int nstages = u1 - u0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < WS; ++s) {
@@ -283,14 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.empty_w[s], 32 * kConsumerWarps);
     }
     for (int s = 0; s < kXStages; ++s) {
-      mbar_init(&sm.raw_x[s], 1);
       mbar_init(&sm.full_x[s], 32);
       mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
-    mbar_init(&sm.prep_done, 32 * kPrepWarps);
-    sm.req_band[0] = 0;
-    sm.req_band[1] = 0;
-    sm.req_alloc = 0;
+    sm.reduce_ok = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -307,7 +318,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
-      tma_prefetch_desc(&tmap_x);
       if (p.meta_tma) {
         tma_prefetch_desc(&tmap_s);
         if (FMT == kInt4G128) tma_prefetch_desc(&tmap_z);
@@ -315,37 +325,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_m = l2_policy_evict_last();
       Cursor st;
-      st.init(u0, u1, p.GP, p.G);
+      st.init(u0, u1, p.GP);
       {
         // While the previous kernel of the stream finishes: pull the first stages' weights
-        // into L2.  Every read that lands in shared memory comes after the wait below.
+        // into L2 (a hint only; every read that lands in shared memory follows the wait).
         Cursor pf = st;
-        for (int q = 0; q < WS && q < nstages; ++q, pf.next()) {
+        for (int q = 0; q < WS && q < nstages; ++q, pf.next())
           tma_prefetch_l2_2d(&tmap_w, pf.j * 128, pf.band * kBand);
-          if (p.meta_tma && (q == 0 || (FMT == kInt4G128 ? (pf.j & 3) == 0 : (pf.j & 1) == 0))) {
-            if constexpr (FMT == kInt4G128) {
-              tma_prefetch_l2_2d(&tmap_s, (2 * pf.j) & ~7, pf.band * kBand);
-              tma_prefetch_l2_2d(&tmap_z, (2 * pf.j) & ~7, pf.band * kBand);
-            } else {
-              tma_prefetch_l2_2d(&tmap_s, (8 * pf.j) & ~15, pf.band * kBand);
-            }
-          }
-        }
       }
       pdl_wait();
       int i = 0;
       for (; i < nstages; ++i, st.next()) {
         const int slot = i % WS;
         const uint32_t ph = (i / WS) & 1;
-        if (!mbar_wait(&sm.empty_w[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
+        if (i >= WS && !mbar_wait(&sm.empty_w[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
         mbar_arrive_expect_tx(&sm.full_w[slot], kTileBytes + (p.meta_tma ? kMetaBytes : 0));
         tma_load_2d(&sm.w[slot][0], &tmap_w, st.j * 128, st.band * kBand, &sm.full_w[slot], pol_w);
-        // the stage's activations into its fragment slot (free once stage i - kXStages is
-        // consumed; never the binding wait: that ring is deeper than the weight ring)
-        const int xs = i % kXStages;
-        if (!mbar_wait(&sm.empty_x[xs], ((i / kXStages) & 1) ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-        mbar_arrive_expect_tx(&sm.raw_x[xs], MT * 512);
-        tma_load_2d(&sm.x[xs][0][0][0][0], &tmap_x, st.j * 256, 0, &sm.raw_x[xs], pol_m);
         if (p.meta_tma) {
           if constexpr (FMT == kInt4G128) {
             const int gx = (2 * st.j) & ~7;
@@ -360,16 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj < 0) continue;
         mbar_wait(&sm.full_w[jj % WS], (jj / WS) & 1, &g_gemv_err, kErrDrain);
       }
-      for (int jj = i - kXStages; jj < i; ++jj) {
-        if (jj < 0) continue;
-        mbar_wait(&sm.raw_x[jj % kXStages], (jj / kXStages) & 1, &g_gemv_err, kErrDrain);
-      }
     }
   } else if (warp < kFirstConsumer) {
     // ------------------------------------------------------------------ prep
-    // Activations only.  The producer drops each stage's raw rows into the stage's fragment
-    // slot by TMA (rows >= M and columns >= K zero-filled); prep warp i % 3 converts them in
-    // place, off the weight ring's critical path and without global-memory latency.
+    // Activations only, read from global memory (they were written by the previous kernel of
+    // the stream: every read follows the dependency wait) and converted in registers.
     // Lane L owns the 16-byte chunk L (8 activations at k = 256 j + 8 L) of each row:
     //   INT4:  L = 16 h + 4 t + v  (group h, fragment lane t, vector v: k = 128 h + 32 t + 8 v)
     //   MXFP4: L = 16 h + 4 blk + t (group h, block blk, fragment lane t: k = 128 h + 32 blk + 8 t)
@@ -378,87 +368,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ft = (FMT == kInt4G128) ? ((lane >> 2) & 3) : (lane & 3);   // fragment lane t
     const int fv = (FMT == kInt4G128) ? (lane & 3) : ((lane >> 2) & 3);   // vector / block
     Cursor st;
-    st.init(u0, u1, p.GP, p.G);
-    for (int q = 0; q < pw; ++q) st.next();
-    // Split-K tails.  A band shared by several CTAs ends, in each of them, with fp32 partial
-    // sums that the consumers store before releasing the stage's activation slot.  The prep
-    // warp that next acquires that slot (the same warp: kXStages % kPrepWarps == 0) publishes
-    // the contribution with one GPU-scope acq_rel counter update.  The last contributor posts
-    // a reduction request; the 16 consumer warps sum every contributor's partials in CTA
-    // order (deterministic) and write the bf16 outputs.  Nobody waits on another CTA.
-    // Pending tails of this warp's last two stages (i - 3 and i - 6): band (-1: none), units.
-    int tb0 = -1, tu0 = 0, tb1 = -1, tu1 = 0;
-    auto split_tail = [&](int band, int units) {
-      if (lane == 0) {
-        const uint32_t old = atom_add_acq_rel_gpu(p.cnt + band, static_cast<uint32_t>(units));
-        if (old + static_cast<uint32_t>(units) == static_cast<uint32_t>(p.GP)) {
-          // last contributor: the consumers sum the band (acquire above, release below)
-          atomicExch(p.cnt + band, 0u);   // ready for the next launch
-          const int k = atomicAdd(&sm.req_alloc, 1);
-          st_release_cta(&sm.req_band[k], band + 1);
-        }
-      }
-      __syncwarp();
-    };
-    // (on the last prep warp: its first stage is the CTA's third, so short layers never wait for it)
-    if (pw == kPrepWarps - 1 && lane == 0 && nstages > 0) {
-#pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
-        const int band = static_cast<int>((q == 0 ? u0 : u1 - 1) / p.GP);
-        sm.ci_band[q] = band;
-        sm.ci[q] = band_contributors(p, band);
-      }
-    }
-    pdl_wait();   // the split-K counters may come from the previous kernel
-    // Stages i >= nstages are not prepared; their slot waits only deliver the last tails.
-    for (int i = pw; i < nstages + kXStages; i += kPrepWarps) {
+    st.init(u0, u1, p.GP);
+    for (int q = 0; q < pw && q < nstages; ++q) st.next();
+    pdl_wait();
+    for (int i = pw; i < nstages; i += kPrepWarps) {
       const int slot = i % kXStages;
       const uint32_t ph = (i / kXStages) & 1;
-      const bool hs = ((i / kPrepWarps) & 1) != 0;
-      const int pend_band = hs ? tb1 : tb0;          // tail of stage i - kXStages, -1 if none
-      const int pend_units = hs ? tu1 : tu0;
-      if (i >= nstages && pend_band < 0) continue;  // nothing left to publish
       if (!mbar_wait(&sm.empty_x[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
-      // the consumers are done with stage i - kXStages (same slot) and stored its partials
-      if (pend_band >= 0) split_tail(pend_band, pend_units);
-      int nb = -1, nu = 0;
-      if (i < nstages && st.seg_last()) {
-        const int band = st.band;
-        const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
-                          (st.seg_end == static_cast<long long>(band + 1) * p.GP);
-        if (!full) { nb = band; nu = static_cast<int>(st.seg_end - st.seg_start); }
-      }
-      if (hs) { tb1 = nb; tu1 = nu; } else { tb0 = nb; tu0 = nu; }
-      if (i >= nstages) continue;
-      for (int q = 0; q < kPrepWarps; ++q) st.next();
-      if (!mbar_wait(&sm.raw_x[slot], ph, &g_gemv_err, kErrWaitFull)) break;
-      uint4* xs4 = &sm.x[slot][0][0][0][0];
+      const int k0 = 256 * st.j + 8 * lane;   // this lane's 8 activations of each row
+      const bool kin = k0 < p.K;
+      uint4 cur[MT];
+#pragma unroll
+      for (int r = 0; r < MT; ++r)
+        cur[r] = (r < p.M && kin) ? __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(r) * p.K + k0))
+                                  : make_uint4(0u, 0u, 0u, 0u);
+      for (int q = 0; q < kPrepWarps && st.u < u1; ++q) st.next();
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        // 8 rows (one n-tile) in registers, then written back permuted: a row's fragment
-        // positions hold other rows' raw chunks, so every read of the tile precedes every write.
-        const int mlive = p.M - 8 * nt;   // rows of this tile below M
-        uint4 cur[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-          cur[r] = (r < mlive) ? xs4[(8 * nt + r) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
-        __syncwarp();
-        // MXFP4: one power-of-two scale 2^-k per stage and activation row carries every operand
-        // into fp16 exactly (bf16_to_f16_exponent: the row's largest in [2^14, 2^15), small
-        // rows scaled up); only values more than 2^31 below their row's largest lose bits, as
-        // fp16 subnormals.  max |x| per row: bf16 magnitudes order like integers; two rows'
-        // maxima share a word for the warp reduction.
+        // One power-of-two scale 2^-k per stage and activation row carries every operand into
+        // fp16 exactly (bf16_to_f16_exponent: the row's largest in [2^14, 2^15), small rows
+        // scaled up); only values more than 2^31 below their row's largest lose bits, as fp16
+        // subnormals.  max |x| per row: bf16 magnitudes order like integers; two rows' maxima
+        // share a word for the warp reduction.
         float inv[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) inv[r] = 1.f;
-        if constexpr (FMT != kInt4G128) {
+        if constexpr (FMT != kInt4G128 || kF16) {
           uint32_t mxp[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t m2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const uint4 x = cur[2 * q + u];
+              const uint4 x = cur[8 * nt + 2 * q + u];
               const uint32_t v = __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
                                           __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
               m2[u] = max(v & 0xffffu, v >> 16);
@@ -479,13 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           uint4* dst = &sm.x[slot][nt][h][fv][4 * r + ft];
-          if (r >= mlive) {   // zero-filled row: zero fragments (INT4: zero sums below)
-            *dst = make_uint4(0u, 0u, 0u, 0u);
-            continue;
-          }
-          const uint4 x = cur[r];
+          const uint4 x = cur[8 * nt + r];
           const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-          if constexpr (FMT == kInt4G128) {
+          if constexpr (FMT == kInt4G128 && !kF16) {
             // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
             uint4 o;
             o.x = prmt(x.x, x.z, 0x5410);
@@ -493,6 +431,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.z = prmt(x.y, x.w, 0x5410);
             o.w = prmt(x.y, x.w, 0x7632);
             *dst = o;
+          } else if constexpr (FMT == kInt4G128) {
+            // the same k order; the odd nibbles come out of the weights as 16 q, so their
+            // activations carry 1/16
+            const float f0 = inv[r], f1 = inv[r] * 0.0625f;
+            const uint32_t lo[4] = {w4[0] << 16, w4[0] & 0xffff0000u, w4[1] << 16, w4[1] & 0xffff0000u};
+            const uint32_t hi[4] = {w4[2] << 16, w4[2] & 0xffff0000u, w4[3] << 16, w4[3] & 0xffff0000u};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float f = (q & 1) ? f1 : f0;
+              __half2 hh = __floats2half2_rn(__uint_as_float(lo[q]) * f, __uint_as_float(hi[q]) * f);
+              o[q] = *reinterpret_cast<uint32_t*>(&hh);
+            }
+            *dst = make_uint4(o[0], o[1], o[2], o[3]);
           } else {
             uint32_t o[4];
 #pragma unroll
@@ -504,12 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
-        if constexpr (FMT == kInt4G128) {
+        if constexpr (FMT == kInt4G128 && !kF16) {
           // Per-group activation sums of the tile's 8 rows on the tensor core: an all-ones A
           // times the just-written B fragments gives every column sum (exact products, fp32
           // accumulation).  Lane (g = 0, t) receives rows 2t, 2t + 1 of the tile.
           __syncwarp();
-          // (four independent accumulator chains per group: the MMA latency bounds this step)
           constexpr uint32_t kOnes = 0x3f803f80u;   // bf16 (1, 1)
 #pragma unroll
           for (int hg = 0; hg < 2; ++hg) {
@@ -526,13 +477,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float s1 = (d[0][1] + d[1][1]) + (d[2][1] + d[3][1]);
             if (lane < 4) *reinterpret_cast<float2*>(&sm.xsum[slot][hg][8 * nt + 2 * lane]) = make_float2(s0, s1);
           }
+        } else if constexpr (FMT == kInt4G128) {
+          // Per-group sums of the tile's 8 rows on the tensor core (exact products, fp32
+          // accumulation): A = (1, 1 | 16, 16) times the B fragments just written gives the
+          // sum of the scaled activations; A = all ones gives the sum of the B operand itself,
+          // whose 1024-fold the weights' fp16 offset adds.  Lane (g = 0, t) receives rows
+          // 2t, 2t + 1 of the tile.
+          __syncwarp();
+          constexpr uint32_t kOne = 0x3c003c00u;      // fp16 (1, 1)
+          constexpr uint32_t kSixteen = 0x4c004c00u;  // fp16 (16, 16)
+#pragma unroll
+          for (int hg = 0; hg < 2; ++hg) {
+            float d[4][4], e[4][4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint4 b = sm.x[slot][nt][hg][v][lane];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) { d[v][q] = 0.f; e[v][q] = 0.f; }
+              mma_f16(d[v], kOne, kOne, kSixteen, kSixteen, b.x, b.y);
+              mma_f16(d[v], kOne, kOne, kSixteen, kSixteen, b.z, b.w);
+              mma_f16(e[v], kOne, kOne, kOne, kOne, b.x, b.y);
+              mma_f16(e[v], kOne, kOne, kOne, kOne, b.z, b.w);
+            }
+            const float s0 = (d[0][0] + d[1][0]) + (d[2][0] + d[3][0]);
+            const float s1 = (d[0][1] + d[1][1]) + (d[2][1] + d[3][1]);
+            const float o0 = 1024.f * ((e[0][0] + e[1][0]) + (e[2][0] + e[3][0]));
+            const float o1 = 1024.f * ((e[0][1] + e[1][1]) + (e[2][1] + e[3][1]));
+            if (lane < 4) {
+              *reinterpret_cast<float2*>(&sm.xsum[slot][hg][8 * nt + 2 * lane]) = make_float2(s0, s1);
+              *reinterpret_cast<float2*>(&sm.xoff[slot][hg][8 * nt + 2 * lane]) = make_float2(o0, o1);
+            }
+          }
         }
       }
-      // the slot is refilled by TMA (async proxy) once consumed: order these generic writes first
-      fence_proxy_async_smem();
       mbar_arrive(&sm.full_x[slot]);
     }
-    mbar_arrive(&sm.prep_done);
   } else {
     // ------------------------------------------------------------------ consumers
     const int cw = warp - kFirstConsumer;
@@ -548,7 +527,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
 
     Cursor st;
-    st.init(u0, u1, p.GP, p.G);
+    st.init(u0, u1, p.GP);
+    // The CTA's last band is reduced here when the range ends inside it and holds its first
+    // unit; the first band is published when the range starts inside it.
+    const int last_band = (u1 - 1) / p.GP;
+    const int red_band = (u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
+    float own_acc[NT][4] = {};   // the reducer's own partial sums of that band
+    float* own = reinterpret_cast<float*>(&sm.w[0][0]);
+    int pending = -1;       // band whose partial sums are stored but not yet published
+    auto publish = [&]() {
+      // the stores were issued a stage ago, so the release rarely waits
+      __syncwarp();
+      if (lane == 0) red_release_gpu_add(p.cnt + pending, 1u);
+      pending = -1;
+    };
+    pdl_wait();   // outputs, partial sums and counters may be in use by the previous kernel
     for (int i = 0; i < nstages; ++i, st.next()) {
       const int ws = i % WS;
       const uint32_t wph = (i / WS) & 1;
@@ -642,39 +635,96 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int jw = jh * PAR + q;
-                // nibble pairs (s, s+4) as bf16 128 + q (exact); the zero point is folded below
-                const uint32_t a0 = lop3_and_or(w0[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
-                const uint32_t a1 = lop3_and_or(w1[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
-                const uint32_t a2 = lop3_and_or(w0[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
-                const uint32_t a3 = lop3_and_or(w1[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                // nibble pairs (s, s+4) as fp16 1024 + q and (s+1, s+5) as 1024 + 16 q (exact;
+                // their activations carry 1/16); the offset and zero point are folded below
+                uint32_t a0, a1, a2, a3;
+                if constexpr (kF16) {
+                  const uint32_t u0 = hh ? (w0[h][jw] >> 8) : w0[h][jw];
+                  const uint32_t u1 = hh ? (w1[h][jw] >> 8) : w1[h][jw];
+                  a0 = lop3_and_or(u0, 0x000f000fu, 0x64006400u);
+                  a1 = lop3_and_or(u1, 0x000f000fu, 0x64006400u);
+                  a2 = lop3_and_or(u0, 0x00f000f0u, 0x64006400u);
+                  a3 = lop3_and_or(u1, 0x00f000f0u, 0x64006400u);
+                } else {
+                  // bf16 128 + q: every nibble shifted to bit 0 (a byte's high nibble would
+                  // reach bf16's exponent)
+                  a0 = lop3_and_or(w0[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                  a1 = lop3_and_or(w1[h][jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                  a2 = lop3_and_or(w0[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                  a3 = lop3_and_or(w1[h][jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                   const uint4 bv = bx[h][q][nt];
-                  mma_bf16(ga[h][q][nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
+                  if constexpr (kF16) mma_f16(ga[h][q][nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
+                  else mma_bf16(ga[h][q][nt], a0, a1, a2, a3, hh ? bv.z : bv.x, hh ? bv.w : bv.y);
                 }
               }
         }
-        // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)   (zero-point cross term)
+        if constexpr (kF16) {
+          // With x' = x 2^-e (per stage and activation row) and B' the B operand:
+          //   sum_k (q - z) s x = 2^e s (D - 1024 sum_k B' - z sum_k x'),  D = sum_k A' B'
+          // (offset and zero-point cross terms of 第 6 课：量化源码走读 §3, from the group sums).
+          float sacc[NT][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[0] >> (16 * h))));
-          const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[1] >> (16 * h))));
-          const float c0 = -s0 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[0] >> (16 * h)))));
-          const float c1 = -s1 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[1] >> (16 * h)))));
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[0] >> (16 * h))));
+            const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[1] >> (16 * h))));
+            const float z0 = __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[0] >> (16 * h))));
+            const float z1 = __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[1] >> (16 * h))));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float2 xs2 = *reinterpret_cast<const float2*>(&sm.xsum[xs][h][2 * t + 8 * nt]);
+              const float2 xo2 = *reinterpret_cast<const float2*>(&sm.xoff[xs][h][2 * t + 8 * nt]);
+              float gs[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                gs[e] = ga[h][0][nt][e];
+#pragma unroll
+                for (int q = 1; q < PAR; ++q) gs[e] += ga[h][q][nt][e];
+              }
+              sacc[nt][0] = fmaf(s0, gs[0] - fmaf(z0, xs2.x, xo2.x), sacc[nt][0]);
+              sacc[nt][1] = fmaf(s0, gs[1] - fmaf(z0, xs2.y, xo2.y), sacc[nt][1]);
+              sacc[nt][2] = fmaf(s1, gs[2] - fmaf(z1, xs2.x, xo2.x), sacc[nt][2]);
+              sacc[nt][3] = fmaf(s1, gs[3] - fmaf(z1, xs2.y, xo2.y), sacc[nt][3]);
+            }
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float2 xs2 = *reinterpret_cast<const float2*>(&sm.xsum[xs][h][2 * t + 8 * nt]);
-            float gs[4];
+            const float2 xf = *reinterpret_cast<const float2*>(&sm.xf[xs][2 * t + 8 * nt]);
+            acc[nt][0] = fmaf(xf.x, sacc[nt][0], acc[nt][0]);
+            acc[nt][1] = fmaf(xf.y, sacc[nt][1], acc[nt][1]);
+            acc[nt][2] = fmaf(xf.x, sacc[nt][2], acc[nt][2]);
+            acc[nt][3] = fmaf(xf.y, sacc[nt][3], acc[nt][3]);
+          }
+        } else {
+          // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)   (zero-point cross
+          // term of 第 6 课：量化源码走读 §3, from the group sum of the activations)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              gs[e] = ga[h][0][nt][e];
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[0] >> (16 * h))));
+            const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[1] >> (16 * h))));
+            const float c0 = -s0 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[0] >> (16 * h)))));
+            const float c1 = -s1 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[1] >> (16 * h)))));
 #pragma unroll
-              for (int q = 1; q < PAR; ++q) gs[e] += ga[h][q][nt][e];
+            for (int nt = 0; nt < NT; ++nt) {
+              const float2 xs2 = *reinterpret_cast<const float2*>(&sm.xsum[xs][h][2 * t + 8 * nt]);
+              float gs[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                gs[e] = ga[h][0][nt][e];
+#pragma unroll
+                for (int q = 1; q < PAR; ++q) gs[e] += ga[h][q][nt][e];
+              }
+              acc[nt][0] = fmaf(c0, xs2.x, fmaf(s0, gs[0], acc[nt][0]));
+              acc[nt][1] = fmaf(c0, xs2.y, fmaf(s0, gs[1], acc[nt][1]));
+              acc[nt][2] = fmaf(c1, xs2.x, fmaf(s1, gs[2], acc[nt][2]));
+              acc[nt][3] = fmaf(c1, xs2.y, fmaf(s1, gs[3], acc[nt][3]));
             }
-            acc[nt][0] = fmaf(c0, xs2.x, fmaf(s0, gs[0], acc[nt][0]));
-            acc[nt][1] = fmaf(c0, xs2.y, fmaf(s0, gs[1], acc[nt][1]));
-            acc[nt][2] = fmaf(c1, xs2.x, fmaf(s1, gs[2], acc[nt][2]));
-            acc[nt][3] = fmaf(c1, xs2.y, fmaf(s1, gs[3], acc[nt][3]));
           }
         }
       } else {
@@ -745,75 +795,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mbar_arrive(&sm.empty_w[ws]);   // weights consumed: the producer may refill the slot
+      if (pending >= 0) publish();
 
+      // Band end.  A band shared with other CTAs is either this CTA's first (its range
+      // started inside the band: publish the partial sums) or its last (this CTA holds the
+      // band's first unit: reduce after the loop, once the others have published).
       if (st.seg_last()) {
         const int band = st.band;
-        const bool full = (st.seg_start == static_cast<long long>(band) * p.GP) &&
-                          (st.seg_end == static_cast<long long>(band + 1) * p.GP);
-        if (full) {
-          if constexpr (EPI == kEpiSwiglu) {
-            // r1 = r0 + 8: this lane holds gate (e = 0, 1) and up (e = 2, 3) of one output
-            const int n = band * kBand + r0;
-            const int F = p.N >> 1;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int m = 2 * t + e + 8 * nt;
-                if (m < p.M && n < p.N)
-                  p.Y[static_cast<long long>(m) * F + swiglu_col(n)] =
-                      __bfloat16_as_ushort(__float2bfloat16_rn(silu_f32(acc[nt][e]) * acc[nt][e + 2]));
-              }
-          } else {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int m = 2 * t + (e & 1) + 8 * nt;
-                const int n = band * kBand + ((e >> 1) ? r1 : r0);
-                if (m < p.M && n < p.N) {
-                  const uint16_t y = __bfloat16_as_ushort(__float2bfloat16_rn(acc[nt][e]));
-                  if constexpr (EPI == kEpiSplit3) store_split3(p.split, m, n, y);
-                  else p.Y[static_cast<long long>(m) * p.N + n] = y;
-                }
-              }
-          }
+        const int bs = band * p.GP;
+        if (st.seg_start == bs && st.seg_end == bs + p.GP) {
+          store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
         } else {
-          // partial sums; the prep warp owning this activation slot publishes them
-          const int side = (u0 >= static_cast<long long>(band) * p.GP) ? 0 : 1;
-          float* slotp = p.part + (static_cast<long long>(cta) * 2 + side) * MT * kBand;
+          float* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int m = 2 * t + (e & 1) + 8 * nt;
-              __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
+              if (m < p.M) {
+                if (st.seg_start == bs) own_acc[nt][e] = acc[nt][e];
+                else __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
+              }
             }
+          if (st.seg_start != bs) pending = band;   // published after the next stage's math
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
       }
-      mbar_arrive(&sm.empty_x[xs]);   // release: orders the partial-sum stores before the tail
+      mbar_arrive(&sm.empty_x[xs]);   // activations consumed
     }
-    // Reductions posted by the prep warps (the last tails are published after the final
-    // stage): wait until the prep warps are done, then take this warp's share, 1/16 of the
-    // float4 slots of each band.
-    if (mbar_wait(&sm.prep_done, 0, &g_gemv_err, kErrWaitReduce)) {
-#pragma unroll 1
-      for (int k = 0; k < 2; ++k) {
-        const int b1 = ld_acquire_cta(&sm.req_band[k]);
-        if (b1 == 0) break;
-        const BandContrib bc = sm.ci[sm.ci_band[0] == b1 - 1 ? 0 : 1];
-        reduce_band_share<MT, EPI>(p, b1 - 1, bc, cw * 32 + lane, 32 * kConsumerWarps);
+    if (pending >= 0) publish();
+    // ---------------------------------------------------------------- shared last band
+    if (red_band >= 0) {
+      // every consumer warp is past its loop (those that gave up on a wait too): the weight
+      // ring is idle, and slot 0 holds this CTA's own partial sums for the coalesced pass
+      named_bar_sync(1, 32 * kConsumerWarps);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int m = 2 * t + (e & 1) + 8 * nt;
+          if (m < p.M) own[m * kBand + ((e >> 1) ? r1 : r0)] = own_acc[nt][e];
+        }
+      const int be = (red_band + 1) * p.GP;
+      int c_hi = cta;
+      while (c_hi + 1 < p.P && p.ustart[c_hi + 1] < be) ++c_hi;
+      if (cw == 0 && lane == 0) {
+        // each consumer warp of CTAs cta + 1 .. c_hi posts once
+        const uint32_t want = static_cast<uint32_t>(c_hi - cta) * kConsumerWarps;
+        int ok = 1;
+        if (ld_relaxed_gpu(p.cnt + red_band) < want) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_relaxed_gpu(p.cnt + red_band) < want) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              atomicOr(&g_gemv_err, kErrWaitReduce);
+              ok = 0;
+              break;
+            }
+          }
+        }
+        fence_acq_rel_gpu();             // the posted partial sums are visible from here on
+        if (ok) p.cnt[red_band] = 0u;    // ready for the next call (its contributors post after this grid ends)
+        sm.reduce_ok = ok;
       }
+      named_bar_sync(1, 32 * kConsumerWarps);
+      if (sm.reduce_ok)
+        reduce_band_share<MT, EPI>(p, red_band, own, cta, c_hi, cw * 32 + lane, 32 * kConsumerWarps);
     }
   }
 }
 
 int num_ctas(long long U) {
-  const long long sms = device_sm_count();
+  long long sms = device_sm_count();
+  if (sms > kMaxCtas) sms = kMaxCtas;
   return static_cast<int>(U < sms ? U : sms);
 }
 
@@ -826,18 +882,12 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   const long long bands = (N + gemv::kBand - 1) / gemv::kBand;
   const int P = gemv::num_ctas(bands * ((G + 1) / 2));
   (void)fmt;
-  return kWsCounterBytes + static_cast<size_t>(P) * 2 * MT * gemv::kBand * sizeof(float);
+  return kWsCounterBytes + static_cast<size_t>(P) * MT * gemv::kBand * sizeof(float);
 }
 
 template <int FMT, int MT, int EPI>
 static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, const CUtensorMap& tz,
                                  const gemv::Params& p, cudaStream_t stream) {
-  // activations: MT rows x 256 k per stage; rows >= M and columns >= K come back as zeros
-  CUtensorMap tx;
-  cudaError_t ex = make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.X, static_cast<uint64_t>(p.K),
-                                static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K) * 2, 256, MT,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (ex != cudaSuccess) return ex;
   using S = gemv::Smem<FMT, MT>;
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
   const size_t smem = sizeof(S) + 1024;
@@ -846,7 +896,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   if (ea != cudaSuccess) return ea;
   // Programmatic stream serialization: the CTAs may launch while the previous kernel of the
   // stream is still running; the kernel itself waits (griddepcontrol.wait) before it reads
-  // anything that kernel may have written.
+  // anything that kernel may have written or writes anything.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(p.P));
   cfg.blockDim = dim3(gemv::kThreads);
@@ -857,7 +907,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, tx, p);
+  return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, p);
 }
 
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -878,9 +928,11 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
   p.GP = (p.G + 1) / 2;
   p.KB = static_cast<int>(K / 32);
   p.bands = static_cast<int>((N + gemv::kBand - 1) / gemv::kBand);
-  p.U = static_cast<long long>(p.bands) * p.GP;
-  p.P = gemv::num_ctas(p.U);
-  if (p.bands > kWsMaxCounters) return cudaErrorInvalidValue;
+  const long long U = static_cast<long long>(p.bands) * p.GP;
+  if (p.bands > kWsMaxCounters || U > (1LL << 30)) return cudaErrorInvalidValue;
+  p.U = static_cast<int>(U);
+  p.P = gemv::num_ctas(U);
+  for (int c = 0; c <= p.P; ++c) p.ustart[c] = static_cast<int>((U * c) / p.P);   // P <= U: none empty
   if (ws_bytes < gemv_mma_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
@@ -946,12 +998,11 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
 // The split-K scratch of the decode kernel (reduction counters and fp32 partial sums) lives
 // here in one fixed, library-owned device array instead of a caller-provided workspace.  It
 // is sized for every decode shape the kernel accepts (M <= 16, N <= 2097152) on a device with
-// at most kNoAllocMaxCtas SMs: 64 KiB of counters + 8 MiB of partials.  Every GPU that loads
+// at most gemv::kMaxCtas CTAs: 64 KiB of counters + 2.5 MiB of partials.  Every GPU that loads
 // the library keeps this array until the process exits.
 // ---------------------------------------------------------------------------------------
-constexpr int kNoAllocMaxCtas = 256;
 constexpr size_t kNoAllocScratchBytes =
-    kWsCounterBytes + static_cast<size_t>(kNoAllocMaxCtas) * 2 * 16 * gemv::kBand * sizeof(float);
+    kWsCounterBytes + static_cast<size_t>(gemv::kMaxCtas) * 16 * gemv::kBand * sizeof(float);
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
