@@ -365,7 +365,7 @@ def gemm_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=
 
 
 def gemv_w4a16(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
-    """The decode kernel alone (M <= 16)."""
+    """The decode kernel alone (M <= 64)."""
     return _linear("wq_gemv_w4a16", fmt, X, Wq, scales, zeros, out, workspace, stream)
 
 
@@ -381,7 +381,7 @@ def gemm_w4a16_swiglu(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, 
 
 
 def gemv_w4a16_swiglu(fmt, X, Wq, scales, zeros=None, out=None, workspace=None, stream=None):
-    """The decode kernel alone with the SwiGLU epilogue (M <= 16)."""
+    """The decode kernel alone with the SwiGLU epilogue (M <= 64)."""
     return _linear("wq_gemv_w4a16_swiglu", fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=True)
 
 

@@ -110,7 +110,7 @@ struct ThresholdOverride {
 std::mutex g_thr_mu;
 ThresholdOverride g_thr[kMaxOverrides];
 int g_thr_n = 0;
-int64_t g_thr_default[2] = {16, 16};
+int64_t g_thr_default[2] = {32, 32};   // the K = N = 8192 sweep's crossover, both formats
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -250,7 +250,7 @@ int64_t wq_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N) {
 
 wq_status wq_set_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N, int64_t T) {
   if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return WQ_ERR_ARG;
-  if (T < 0 || T > 16 || K < 0 || N < 0) return WQ_ERR_SHAPE;
+  if (T < 0 || T > wq::kDecodeMaxM || K < 0 || N < 0) return WQ_ERR_SHAPE;
   std::lock_guard<std::mutex> lk(g_thr_mu);
   if (K == 0 && N == 0) {
     g_thr_default[fmt] = T;
@@ -269,7 +269,7 @@ wq_status wq_set_dispatch_threshold(wq_fmt fmt, int64_t K, int64_t N, int64_t T)
 size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N) {
   if (fmt != WQ_FMT_INT4_G128_ASYM && fmt != WQ_FMT_MXFP4) return 0;
   if (M < 1 || N < 1 || K < 1) return 0;
-  size_t a = M <= 16 ? wq::gemv_workspace_bytes(fmt, M, K, N) : 0;
+  size_t a = M <= wq::kDecodeMaxM ? wq::gemv_workspace_bytes(fmt, M, K, N) : 0;
   size_t b = wq::gemm_tc_workspace_bytes(fmt, M, K, N);
   return a > b ? a : b;
 }
@@ -279,7 +279,7 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
                         void* stream) {
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
-  if (M > 16) return WQ_ERR_SHAPE;
+  if (M > wq::kDecodeMaxM) return WQ_ERR_SHAPE;
   if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
   if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;
@@ -295,7 +295,7 @@ wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_
                                 void* stream) {
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
-  if (M > 16) return WQ_ERR_SHAPE;
+  if (M > 16) return WQ_ERR_SHAPE;   // the library's array holds 16-row partial sums
   if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   st = check_device_cached();
   if (st != WQ_OK) return st;
@@ -336,7 +336,7 @@ wq_status wq_gemv_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t
   const int64_t N = 2 * F;
   wq_status st = check_linear_args(fmt, X, M, K, N, Wq, scales, zeros, Y);
   if (st != WQ_OK) return st;
-  if (M > 16) return WQ_ERR_SHAPE;
+  if (M > wq::kDecodeMaxM) return WQ_ERR_SHAPE;
   if ((N + wq::kDecodeBand - 1) / wq::kDecodeBand > wq::kWsMaxCounters) return WQ_ERR_SHAPE;
   const size_t need = wq::gemv_workspace_bytes(fmt, M, K, N);
   if (need > 0 && (!workspace || ws_bytes < need)) return WQ_ERR_WORKSPACE;

@@ -68,10 +68,12 @@ constexpr int kRowsPerWarp = 16;                     // one m16 row tile per con
 constexpr int kBand = kRowsPerWarp * kConsumerWarps;  // 256 weight rows per CTA tile
 constexpr int kTileBytes = kBand * 128;              // 32 KB of packed weights per stage
 constexpr int kPrepWarps = 3;                        // stage i is prepared by prep warp i % 3
-constexpr int kXStages = 2 * kPrepWarps;             // activation-fragment ring depth
-// Each prep warp owns whole ring slots (kXStages % kPrepWarps == 0), so it waits on every phase
+// Activation-fragment ring depth: two slots per prep warp, one for 32- and 64-row tiles
+// (whose fragments fill 16 and 32 KB a stage).
+__host__ __device__ constexpr int x_stages(int mt) { return mt >= 32 ? kPrepWarps : 2 * kPrepWarps; }
+// Each prep warp owns whole ring slots (x_stages % kPrepWarps == 0), so it waits on every phase
 // of its slots' barriers in order; a parity wait two phases ahead would pass at once.
-static_assert(kXStages % kPrepWarps == 0, "prep warps must own whole ring slots");
+static_assert(x_stages(8) % kPrepWarps == 0 && x_stages(64) % kPrepWarps == 0, "prep warps must own whole ring slots");
 constexpr int kFirstConsumer = 1 + kPrepWarps;       // warp index of the first consumer
 constexpr int kThreads = 32 * (kFirstConsumer + kConsumerWarps);  // 640
 constexpr int kGroupK = 128;                         // k per group (INT4 group; 4 MXFP4 blocks)
@@ -86,9 +88,9 @@ __host__ __device__ constexpr int meta_raw_bytes(int fmt) { return fmt == kInt4G
 __host__ __device__ constexpr int x_stage_bytes(int mt) { return (mt / 8) * 2 * 4 * 32 * 16 + 4 * mt * 4 + mt * 4; }
 // Weight stages: as many as fit beside the activation ring (4 or 5).
 __host__ __device__ constexpr int w_stages(int fmt, int mt) {
-  return (kSmemLimit - kSmemReserve - kXStages * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt)) > 6
+  return (kSmemLimit - kSmemReserve - x_stages(mt) * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt)) > 6
              ? 6
-             : (kSmemLimit - kSmemReserve - kXStages * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt));
+             : (kSmemLimit - kSmemReserve - x_stages(mt) * x_stage_bytes(mt)) / (kTileBytes + meta_raw_bytes(fmt));
 }
 
 struct Params {
@@ -117,14 +119,15 @@ struct Smem {
   uint8_t w[WS][kTileBytes];                 // SWIZZLE_128B weight tiles (1024-aligned)
   uint8_t mraw[WS][meta_raw_bytes(FMT)];     // raw metadata tiles (TMA), 16 B per row per tensor
   // B fragments [nt][group][vec][lane]
-  uint4 x[kXStages][NT][2][4][32];
-  float xsum[kXStages][2][MT];               // INT4: sum of the group's scaled activations per row m
-  float xoff[kXStages][2][MT];               // INT4: 1024 x the sum of the group's B operand per row m
-  float xf[kXStages][MT];                    // power-of-two factor per activation row
+  static constexpr int XS = x_stages(MT);
+  uint4 x[XS][NT][2][4][32];
+  float xsum[XS][2][MT];                     // INT4: sum of the group's (scaled) activations per row m
+  float xoff[XS][2][MT];                     // INT4: 1024 x the sum of the group's B operand per row m
+  float xf[XS][MT];                          // power-of-two factor per activation row
   uint64_t full_w[WS];
   uint64_t empty_w[WS];
-  uint64_t full_x[kXStages];
-  uint64_t empty_x[kXStages];
+  uint64_t full_x[XS];
+  uint64_t empty_x[XS];
   int reduce_ok;                             // the reducer's wait for the other CTAs ended
 };
 
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.full_w[s], 1);
       mbar_init(&sm.empty_w[s], 32 * kConsumerWarps);
     }
-    for (int s = 0; s < kXStages; ++s) {
+    for (int s = 0; s < S::XS; ++s) {
       mbar_init(&sm.full_x[s], 32);
       mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
@@ -372,19 +375,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int q = 0; q < pw && q < nstages; ++q) st.next();
     pdl_wait();
     for (int i = pw; i < nstages; i += kPrepWarps) {
-      const int slot = i % kXStages;
-      const uint32_t ph = (i / kXStages) & 1;
+      const int slot = i % S::XS;
+      const uint32_t ph = (i / S::XS) & 1;
       if (!mbar_wait(&sm.empty_x[slot], ph ^ 1, &g_gemv_err, kErrWaitEmpty)) break;
       const int k0 = 256 * st.j + 8 * lane;   // this lane's 8 activations of each row
       const bool kin = k0 < p.K;
-      uint4 cur[MT];
+      // up to 16 rows are all in flight at once; larger tiles are loaded 8 rows at a time
+      constexpr int CR = MT <= 16 ? MT : 8;
+      uint4 cur[CR];
+      auto load_rows = [&](int r0) {
 #pragma unroll
-      for (int r = 0; r < MT; ++r)
-        cur[r] = (r < p.M && kin) ? __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(r) * p.K + k0))
-                                  : make_uint4(0u, 0u, 0u, 0u);
+        for (int r = 0; r < CR; ++r)
+          cur[r] = (r0 + r < p.M && kin)
+                       ? __ldcg(reinterpret_cast<const uint4*>(p.X + static_cast<long long>(r0 + r) * p.K + k0))
+                       : make_uint4(0u, 0u, 0u, 0u);
+      };
+      load_rows(0);
       for (int q = 0; q < kPrepWarps && st.u < u1; ++q) st.next();
-#pragma unroll
+      constexpr int kPrepUnroll = MT > 16 ? 1 : NT;   // wide tiles: one 8-row tile at a time
+#pragma unroll kPrepUnroll
       for (int nt = 0; nt < NT; ++nt) {
+        if constexpr (MT > 16) {
+          if (nt > 0) load_rows(8 * nt);
+        }
+        constexpr int kCurTile = MT <= 16 ? 8 : 0;   // row offset of tile nt inside cur
         // One power-of-two scale 2^-k per stage and activation row carries every operand into
         // fp16 exactly (bf16_to_f16_exponent: the row's largest in [2^14, 2^15), small rows
         // scaled up); only values more than 2^31 below their row's largest lose bits, as fp16
@@ -400,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t m2[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const uint4 x = cur[8 * nt + 2 * q + u];
+              const uint4 x = cur[kCurTile * nt + 2 * q + u];
               const uint32_t v = __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
                                           __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
               m2[u] = max(v & 0xffffu, v >> 16);
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
           uint4* dst = &sm.x[slot][nt][h][fv][4 * r + ft];
-          const uint4 x = cur[8 * nt + r];
+          const uint4 x = cur[kCurTile * nt + r];
           const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
           if constexpr (FMT == kInt4G128 && !kF16) {
             // (x0,x4) (x1,x5) (x2,x6) (x3,x7): the k order of the unpacked nibble pairs.
@@ -532,7 +546,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // unit; the first band is published when the range starts inside it.
     const int last_band = (u1 - 1) / p.GP;
     const int red_band = (u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
-    float own_acc[NT][4] = {};   // the reducer's own partial sums of that band
     float* own = reinterpret_cast<float*>(&sm.w[0][0]);
     int pending = -1;       // band whose partial sums are stored but not yet published
     auto publish = [&]() {
@@ -545,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nstages; ++i, st.next()) {
       const int ws = i % WS;
       const uint32_t wph = (i / WS) & 1;
-      const int xs = i % kXStages;
-      const uint32_t xph = (i / kXStages) & 1;
+      const int xs = i % S::XS;
+      const uint32_t xph = (i / S::XS) & 1;
 
       // Per-row metadata of the stage's two groups, rows r0 / r1 of this lane:
       //   INT4: sc[h][rr] = {s, c = -s (128 + z)}     MXFP4: eb[rr] = E8M0 bytes of the 8 blocks
@@ -597,7 +610,115 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       const uint8_t* wt = &sm.w[ws][0];
-      if constexpr (FMT == kInt4G128) {
+      if constexpr (NT >= 4) {
+        // 32 or 64 activation rows: the n-tiles in chunks of four, each chunk unpacking the
+        // weights again, so that one chunk's accumulators per group stay in registers.
+        constexpr int NC = (FMT == kInt4G128 || NT < 8) ? 4 : 2;
+#pragma unroll
+        for (int cb = 0; cb < NT; cb += NC) {
+          float sacc[NC][4];   // MXFP4: the stage's scaled block sums of this chunk
+#pragma unroll
+          for (int nc = 0; nc < NC; ++nc)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nc][e] = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // this group's words (INT4) or blocks (MXFP4), rows r0 / r1, read again per chunk
+            uint32_t w0[4], w1[4];
+            if constexpr (FMT == kInt4G128) {
+              const int c = 4 * h + t;
+              const uint4 a = *reinterpret_cast<const uint4*>(wt + r0 * 128 + ((c ^ (r0 & 7)) << 4));
+              const uint4 b = *reinterpret_cast<const uint4*>(wt + r1 * 128 + ((c ^ (r1 & 7)) << 4));
+              w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w;
+              w1[0] = b.x; w1[1] = b.y; w1[2] = b.z; w1[3] = b.w;
+            } else {
+#pragma unroll
+              for (int blk = 0; blk < 4; ++blk) {
+                const int cc = 4 * h + blk;
+                w0[blk] = *reinterpret_cast<const uint32_t*>(wt + r0 * 128 + ((cc ^ (r0 & 7)) << 4) + 4 * t);
+                w1[blk] = *reinterpret_cast<const uint32_t*>(wt + r1 * 128 + ((cc ^ (r1 & 7)) << 4) + 4 * t);
+              }
+            }
+            float ga[NC][4];
+#pragma unroll
+            for (int nc = 0; nc < NC; ++nc)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) ga[nc][e] = 0.f;
+#pragma unroll
+            for (int jw = 0; jw < 4; ++jw) {
+              uint32_t a[2][4];   // [hh] the A fragments of the two k16 steps
+              if constexpr (FMT == kInt4G128) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  a[hh][0] = lop3_and_or(w0[jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                  a[hh][1] = lop3_and_or(w1[jw] >> (8 * hh), 0x000f000fu, 0x43004300u);
+                  a[hh][2] = lop3_and_or(w0[jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                  a[hh][3] = lop3_and_or(w1[jw] >> (8 * hh + 4), 0x000f000fu, 0x43004300u);
+                }
+              } else {
+                uint32_t f0[4], f1[4];
+                e2m1x8_to_f16x2x4(w0[jw], f0);
+                e2m1x8_to_f16x2x4(w1[jw], f1);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  a[hh][0] = f0[2 * hh]; a[hh][1] = f1[2 * hh];
+                  a[hh][2] = f0[2 * hh + 1]; a[hh][3] = f1[2 * hh + 1];
+                }
+              }
+              float bacc[NC][4];   // MXFP4: this block's sums
+#pragma unroll
+              for (int nc = 0; nc < NC; ++nc) {
+                const uint4 bv = sm.x[xs][cb + nc][h][jw][lane];
+                if constexpr (FMT == kInt4G128) {
+                  mma_bf16(ga[nc], a[0][0], a[0][1], a[0][2], a[0][3], bv.x, bv.y);
+                  mma_bf16(ga[nc], a[1][0], a[1][1], a[1][2], a[1][3], bv.z, bv.w);
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) bacc[nc][e] = 0.f;
+                  mma_f16(bacc[nc], a[0][0], a[0][1], a[0][2], a[0][3], bv.x, bv.y);
+                  mma_f16(bacc[nc], a[1][0], a[1][1], a[1][2], a[1][3], bv.z, bv.w);
+                }
+              }
+              if constexpr (FMT != kInt4G128) {
+                const float e0 = e8m0_to_f32((eb[0][h] >> (8 * jw)) & 0xffu);
+                const float e1 = e8m0_to_f32((eb[1][h] >> (8 * jw)) & 0xffu);
+#pragma unroll
+                for (int nc = 0; nc < NC; ++nc) {
+                  sacc[nc][0] = fmaf(e0, bacc[nc][0], sacc[nc][0]);
+                  sacc[nc][1] = fmaf(e0, bacc[nc][1], sacc[nc][1]);
+                  sacc[nc][2] = fmaf(e1, bacc[nc][2], sacc[nc][2]);
+                  sacc[nc][3] = fmaf(e1, bacc[nc][3], sacc[nc][3]);
+                }
+              }
+            }
+            if constexpr (FMT == kInt4G128) {
+              // y += s * sum_k (128 + q) x + c * sum_k x,  c = -s (128 + z)
+              const float s0 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[0] >> (16 * h))));
+              const float s1 = __half2float(__ushort_as_half(static_cast<unsigned short>(sraw[1] >> (16 * h))));
+              const float c0 = -s0 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[0] >> (16 * h)))));
+              const float c1 = -s1 * (128.f + __half2float(__ushort_as_half(static_cast<unsigned short>(zraw[1] >> (16 * h)))));
+#pragma unroll
+              for (int nc = 0; nc < NC; ++nc) {
+                const float2 xs2 = *reinterpret_cast<const float2*>(&sm.xsum[xs][h][2 * t + 8 * (cb + nc)]);
+                acc[cb + nc][0] = fmaf(c0, xs2.x, fmaf(s0, ga[nc][0], acc[cb + nc][0]));
+                acc[cb + nc][1] = fmaf(c0, xs2.y, fmaf(s0, ga[nc][1], acc[cb + nc][1]));
+                acc[cb + nc][2] = fmaf(c1, xs2.x, fmaf(s1, ga[nc][2], acc[cb + nc][2]));
+                acc[cb + nc][3] = fmaf(c1, xs2.y, fmaf(s1, ga[nc][3], acc[cb + nc][3]));
+              }
+            }
+          }
+          if constexpr (FMT != kInt4G128) {
+#pragma unroll
+            for (int nc = 0; nc < NC; ++nc) {
+              const float2 xf = *reinterpret_cast<const float2*>(&sm.xf[xs][2 * t + 8 * (cb + nc)]);
+              acc[cb + nc][0] = fmaf(xf.x, sacc[nc][0], acc[cb + nc][0]);
+              acc[cb + nc][1] = fmaf(xf.y, sacc[nc][1], acc[cb + nc][1]);
+              acc[cb + nc][2] = fmaf(xf.x, sacc[nc][2], acc[cb + nc][2]);
+              acc[cb + nc][3] = fmaf(xf.y, sacc[nc][3], acc[cb + nc][3]);
+            }
+          }
+        }
+      } else if constexpr (FMT == kInt4G128) {
         // Both groups at once.  PAR words per step with their own accumulators keep four
         // independent MMA chains in flight per warp (groups x word parity x n-tiles).
         constexpr int PAR = (NT == 1) ? 2 : 1;
@@ -803,26 +924,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (st.seg_last()) {
         const int band = st.band;
         const int bs = band * p.GP;
-        if (st.seg_start == bs && st.seg_end == bs + p.GP) {
-          store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
-        } else {
-          float* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
+        // (the reducer's band is its range's last: acc keeps its partial sums past the loop)
+        if (st.seg_start != bs || st.seg_end == bs + p.GP) {
+          if (st.seg_start == bs) {
+            store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
+          } else {
+            float* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int m = 2 * t + (e & 1) + 8 * nt;
+                if (m < p.M) __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
+              }
+            pending = band;   // published after the next stage's math
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int m = 2 * t + (e & 1) + 8 * nt;
-              if (m < p.M) {
-                if (st.seg_start == bs) own_acc[nt][e] = acc[nt][e];
-                else __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
-              }
-            }
-          if (st.seg_start != bs) pending = band;   // published after the next stage's math
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
         }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
       }
       mbar_arrive(&sm.empty_x[xs]);   // activations consumed
     }
@@ -837,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int m = 2 * t + (e & 1) + 8 * nt;
-          if (m < p.M) own[m * kBand + ((e >> 1) ? r1 : r0)] = own_acc[nt][e];
+          if (m < p.M) own[m * kBand + ((e >> 1) ? r1 : r0)] = acc[nt][e];
         }
       const int be = (red_band + 1) * p.GP;
       int c_hi = cta;
@@ -875,9 +996,12 @@ int num_ctas(long long U) {
 
 }  // namespace gemv
 
+// Activation rows per launch: tiles of 8, 16 or 32; larger M runs as 32-row slices.
+static int tile_rows(int64_t M) { return M <= 8 ? 8 : M <= 16 ? 16 : 32; }
+
 size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
-  if (M < 1 || M > 16 || N < 1 || K < 1) return 0;
-  const int MT = M <= 8 ? 8 : 16;
+  if (M < 1 || M > kDecodeMaxM || N < 1 || K < 1) return 0;
+  const int MT = tile_rows(M);
   const long long G = (K + gemv::kGroupK - 1) / gemv::kGroupK;
   const long long bands = (N + gemv::kBand - 1) / gemv::kBand;
   const int P = gemv::num_ctas(bands * ((G + 1) / 2));
@@ -890,6 +1014,7 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
                                  const gemv::Params& p, cudaStream_t stream) {
   using S = gemv::Smem<FMT, MT>;
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
+  static_assert(MT * gemv::kBand * sizeof(float) <= sizeof(S::w), "reducer's partial sums must fit the weight ring");
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT, EPI>;
   cudaError_t ea = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
@@ -910,11 +1035,38 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
   return cudaLaunchKernelEx(&cfg, kern, tw, ts, tz, p);
 }
 
+static cudaError_t launch_gemv_slice(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                     const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Y,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream, int epi,
+                                     const OutSplit* split);
+
 cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
                             const void* scales, const uint16_t* zeros, uint16_t* Y, void* ws, size_t ws_bytes,
                             cudaStream_t stream, int epi, const OutSplit* split) {
   if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
   if (epi == kEpiSplit3 && !split) return cudaErrorInvalidValue;
+  // M > 32: consecutive 32-row slices of X and of the outputs, one launch each, in order on
+  // the stream (they share the workspace; each leaves its counters at zero).
+  constexpr int64_t kSlice = 32;
+  const int64_t ldy = epi == kEpiSwiglu ? N / 2 : N;
+  for (int64_t m0 = 0; m0 < M; m0 += kSlice) {
+    const int64_t ms = M - m0 < kSlice ? M - m0 : kSlice;
+    OutSplit sp{};
+    if (split) {
+      sp = *split;
+      for (int q = 0; q < 3; ++q) sp.y[q] = split->y[q] + m0 * split->ld[q];
+    }
+    const cudaError_t e = launch_gemv_slice(fmt, X + m0 * K, ms, K, N, Wq, scales, zeros, Y ? Y + m0 * ldy : Y,
+                                            ws, ws_bytes, stream, epi, split ? &sp : nullptr);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t launch_gemv_slice(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
+                                     const int32_t* Wq, const void* scales, const uint16_t* zeros, uint16_t* Y,
+                                     void* ws, size_t ws_bytes, cudaStream_t stream, int epi,
+                                     const OutSplit* split) {
   gemv::Params p{};
   p.X = X;
   p.scales = scales;
@@ -968,17 +1120,21 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
       if (e != cudaSuccess) return e;
     }
   }
-  const bool small = M <= 8;
+  const int mt = tile_rows(M);
+#define WQ_BAND_LAUNCH_F(F, EPIV)                                                                              \
+  switch (mt) {                                                                                                \
+    case 8: return launch_gemv_t<F, 8, EPIV>(tw, ts, tz, p, stream);                                           \
+    case 16: return launch_gemv_t<F, 16, EPIV>(tw, ts, tz, p, stream);                                         \
+    default: return launch_gemv_t<F, 32, EPIV>(tw, ts, tz, p, stream);                                         \
+  }
 #define WQ_BAND_LAUNCH(EPIV)                                                                                   \
-  if (fmt == kInt4G128)                                                                                        \
-    return small ? launch_gemv_t<kInt4G128, 8, EPIV>(tw, ts, tz, p, stream)                                   \
-                 : launch_gemv_t<kInt4G128, 16, EPIV>(tw, ts, tz, p, stream);                                 \
-  return small ? launch_gemv_t<kMxfp4, 8, EPIV>(tw, ts, tz, p, stream)                                        \
-               : launch_gemv_t<kMxfp4, 16, EPIV>(tw, ts, tz, p, stream);
+  if (fmt == kInt4G128) { WQ_BAND_LAUNCH_F(kInt4G128, EPIV) }                                                  \
+  WQ_BAND_LAUNCH_F(kMxfp4, EPIV)
   if (epi == kEpiSwiglu) { WQ_BAND_LAUNCH(kEpiSwiglu) }
   if (epi == kEpiSplit3) { WQ_BAND_LAUNCH(kEpiSplit3) }
   WQ_BAND_LAUNCH(kEpiNone)
 #undef WQ_BAND_LAUNCH
+#undef WQ_BAND_LAUNCH_F
 }
 
 // The decode entry points run the mma.sync kernel above.  (A tcgen05 variant was measured

@@ -59,6 +59,8 @@ constexpr size_t kWsCounterBytes = 64 * 1024;
 constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
 // Weight rows per split-K band of the decode kernel: N <= kWsMaxCounters * kDecodeBand.
 constexpr int64_t kDecodeBand = 128;
+// Activation rows the decode kernel accepts (tiles of 8, 16, 32 or 64 rows).
+constexpr int64_t kDecodeMaxM = 64;
 
 // quantize.cu
 cudaError_t launch_quant_int4_g128(const float* W, int64_t N, int64_t K, int32_t* Wq, uint16_t* scales,

@@ -198,7 +198,7 @@ size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N);
  * Defined by: 推理优化与量化算子深度技术调研 §1.2 (dequantization fused into the GEMM,
  * x_deq = (q - zp) * scale, before the multiply) and 第 6 课：量化源码走读 (W4A16 layer; the
  * "apply" step chooses a bandwidth kernel for small batch and a compute kernel for large
- * batch).  Dispatches on M: M <= T(fmt, K, N) runs the decode GEMV (T <= 16), otherwise the
+ * batch).  Dispatches on M: M <= T(fmt, K, N) runs the decode GEMV (T <= 64), otherwise the
  * tcgen05 tensor-core GEMM.
  *   X       [M, K] bf16 bits.
  *   Wq      [N, K/8] int32 (format fmt).
@@ -216,8 +216,8 @@ wq_status wq_gemm_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
                         uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
 /*
- * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 16
- * and N <= 2097152).
+ * The decode kernel alone (same arguments and errors as wq_gemm_w4a16; requires M <= 64
+ * and N <= 2097152; M > 32 runs as consecutive 32-row launches).
  * Streams the packed weights with TMA, unpacks in registers and applies the group scale in
  * fp32 after exact integer-valued tensor-core products; the zero point enters as (q - z),
  * the cross term of 第 6 课：量化源码走读 §3.
@@ -234,10 +234,10 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * this is a deployment convenience of this library, not part of the method.
  * Same arguments, results and errors as wq_gemv_w4a16 minus workspace/ws_bytes; allocates
  * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (split-K
- * counters + fp32 partials) is one library-owned device array of 64 KiB + 8 MiB, held by
- * every GPU that loads the library until the process exits; it covers every shape the decode
- * kernel accepts (M <= 16, N <= 2097152) on devices with up to 256 SMs, and a shape it cannot
- * hold is refused with WQ_ERR_SHAPE before anything is enqueued.
+ * counters + fp32 partials) is one library-owned device array of 64 KiB + 2.5 MiB, held by
+ * every GPU that loads the library until the process exits; it covers M <= 16 and
+ * N <= 2097152 (one CTA per SM, at most 160), and a shape it cannot hold (M > 16) is refused
+ * with WQ_ERR_SHAPE before anything is enqueued.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  * with that device current); make that first call before any stream capture.  The address is
  * looked up again when the device's current context has changed since (cudaDeviceReset
@@ -284,7 +284,7 @@ wq_status wq_gemm_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t
                                const int32_t* Wq, const void* scales, const uint16_t* zeros,
                                uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
-/* The decode kernel alone with the SwiGLU epilogue (M <= 16, 2F <= 2097152). */
+/* The decode kernel alone with the SwiGLU epilogue (M <= 64, 2F <= 2097152). */
 wq_status wq_gemv_w4a16_swiglu(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t F,
                                const int32_t* Wq, const void* scales, const uint16_t* zeros,
                                uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
@@ -333,7 +333,7 @@ wq_status wq_interleave_gate_up(const void* src, void* dst, int64_t F, int64_t r
 
 /*
  * Dispatch threshold T(fmt, K, N): wq_gemm_w4a16 uses the decode kernel when M <= T.
- * wq_set_dispatch_threshold overrides it for one (fmt, K, N) (T in [0, 16]; K = N = 0 sets
+ * wq_set_dispatch_threshold overrides it for one (fmt, K, N) (T in [0, 64]; K = N = 0 sets
  * the default for the format).  Returns WQ_ERR_ARG / WQ_ERR_SHAPE on bad input.  Host-side
  * state, process-wide, not thread-safe against concurrent calls.
  */

@@ -138,10 +138,11 @@ def test_gemm_tc_small_magnitude_activations(B, fmt):
 
 
 def test_dispatch_routes_by_m(B):
-    M, N, K = 20, 256, 512
+    # both sides of the default threshold (32): decode at M <= 32, tensor core above
+    N, K = 256, 512
     W = inputs.weights(2, N, K, 0.05)
     pk = int4_g128.quantize(W)
-    for m in (1, 16, 17, 20):
+    for m in (1, 16, 17, 20, 32, 33, 40):
         xb, xf = inputs.activations(m, m, K)
         Y = _run(B.gemm_w4a16, "int4_g128", xb, pk)
         assert_close(y_to_host(Y), linear.linear_w4a16("int4_g128", xf, *pk), "dispatch M=%d" % m)

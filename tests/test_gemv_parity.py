@@ -1,4 +1,4 @@
-"""Decode kernel (M <= 16) against the float64 oracle on the same dequantized weights."""
+"""Decode kernel (M <= 64) against the float64 oracle on the same dequantized weights."""
 import numpy as np
 import pytest
 
@@ -193,3 +193,29 @@ def test_gpu_quantize_then_decode_without_sync(B, fmt):
         Y = B.gemv_w4a16(fmt, X, Wq, s)
     ref = linear.linear_w4a16(fmt, xf, *_pack(fmt, W))
     assert_close(y_to_host(Y), ref, "%s quantize -> decode" % fmt)
+
+
+# 17..64 activation rows: 32-row tiles (n-tiles in chunks of four), and M > 32 as consecutive
+# 32-row launches on row slices of X and Y; bands shared by several CTAs and ragged tails.
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [17, 24, 32, 33, 40, 64])
+@pytest.mark.parametrize("N,K", [(300, 1152), (1000, 512), (2048, 4096)])
+def test_gemv_wide_tiles(B, fmt, M, N, K):
+    W = inputs.weights(N * 5 + K + M, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M * 3 + N, M, K)
+    Y = _run(B, B.gemv_w4a16, fmt, xb, pk)
+    assert_close(y_to_host(Y), linear.linear_w4a16(fmt, xf, *pk), "%s M=%d N=%d K=%d" % (fmt, M, N, K))
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_gemv_wide_tiles_full_size(B, fmt):
+    # a decode-shaped layer at M = 48 (two slices), sampled output columns
+    M, K, N = 48, 4096, 6144
+    W = inputs.weights(77, N, K, 0.02)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(78, M, K)
+    y = y_to_host(_run(B, B.gemv_w4a16, fmt, xb, pk))
+    rows = np.sort(np.random.default_rng(79).choice(N, 256, replace=False))
+    z = pk[2] if fmt == "int4_g128" else None
+    assert_close(y[:, rows], linear.linear_rows(fmt, xf, pk[0], pk[1], z, rows), "%s M=48 sampled" % fmt)

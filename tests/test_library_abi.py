@@ -73,7 +73,7 @@ def test_validation_errors(lib):
     assert _gemm(lib, fmt=1, z=None, K=48) == 2         # MXFP4: K % 32
     assert _gemm(lib, X=ODD) == 3                       # alignment
     assert _gemm(lib, Y=ODD) == 3
-    assert lib.wq_gemv_w4a16(0, FAKE, 17, 128, 8, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 2  # decode: M <= 16
+    assert lib.wq_gemv_w4a16(0, FAKE, 65, 128, 8, FAKE, FAKE, FAKE, FAKE, None, 0, None) == 2  # decode: M <= 64
     assert lib.wq_quantize_int4_g128(None, 4, 128, FAKE, FAKE, FAKE, None) == 1
     assert lib.wq_quantize_int4_g128(FAKE, 4, 96, FAKE, FAKE, FAKE, None) == 2
     assert lib.wq_quantize_mxfp4(FAKE, 4, 48, FAKE, FAKE, None) == 2
@@ -93,14 +93,14 @@ def test_workspace_checked_before_launch(lib):
 
 
 def test_dispatch_threshold_table(lib):
-    assert binding.dispatch_threshold("int4_g128", 4096, 4096) == 16
+    assert binding.dispatch_threshold("int4_g128", 4096, 4096) == 32
     binding.set_dispatch_threshold("int4_g128", 4096, 4096, 4)
     assert binding.dispatch_threshold("int4_g128", 4096, 4096) == 4
-    assert binding.dispatch_threshold("int4_g128", 4096, 8192) == 16
-    assert binding.dispatch_threshold("mxfp4", 4096, 4096) == 16
-    binding.set_dispatch_threshold("int4_g128", 4096, 4096, 16)
+    assert binding.dispatch_threshold("int4_g128", 4096, 8192) == 32
+    assert binding.dispatch_threshold("mxfp4", 4096, 4096) == 32
+    binding.set_dispatch_threshold("int4_g128", 4096, 4096, 32)
     with pytest.raises(ValueError):
-        binding.set_dispatch_threshold("int4_g128", 4096, 4096, 17)
+        binding.set_dispatch_threshold("int4_g128", 4096, 4096, 65)
     assert lib.wq_set_dispatch_threshold(3, 0, 0, 1) == 7
 
 
@@ -110,7 +110,7 @@ def test_validation_errors_swiglu_interleave_gptq_awq(lib):
                                                             kw.get("ws"), kw.get("wsb", 0), None)
     assert sw("wq_gemm_w4a16_swiglu", F=12) == 2
     assert sw("wq_gemm_w4a16_swiglu", F=0) == 2
-    assert sw("wq_gemv_w4a16_swiglu", M=17, F=16) == 2
+    assert sw("wq_gemv_w4a16_swiglu", M=65, F=16) == 2
     assert sw("wq_gemm_tc_w4a16_swiglu", K=64, F=16) == 2
     assert sw("wq_gemv_w4a16_swiglu", F=4096) == 4          # workspace missing
     # interleave: NULL, F, row bytes, overlap (src == dst)

@@ -24,11 +24,19 @@ def _pack(fmt, W):
     return int4_g128.quantize(W) if fmt == "int4_g128" else mxfp4.quantize(W)
 
 
-def _qkv(B, fmt, xb, pk, Nq, Nkv):
+def _qkv(B, fmt, xb, pk, Nq, Nkv, path=None):
+    """path: "decode" or "tc" pins the dispatch for this (fmt, K, N); None keeps the default."""
     d = [to_dev(a) for a in pk]
     X = x_to_dev(xb)
     z = d[2] if fmt == "int4_g128" else None
-    return [y_to_host(t) for t in B.gemm_w4a16_qkv(fmt, X, d[0], d[1], z, Nq=Nq, Nkv=Nkv)]
+    K, N = X.shape[1], Nq + 2 * Nkv
+    old = B.dispatch_threshold(fmt, K, N)
+    if path is not None:
+        B.set_dispatch_threshold(fmt, K, N, 64 if path == "decode" else 0)
+    try:
+        return [y_to_host(t) for t in B.gemm_w4a16_qkv(fmt, X, d[0], d[1], z, Nq=Nq, Nkv=Nkv)]
+    finally:
+        B.set_dispatch_threshold(fmt, K, N, old)
 
 
 def _check(got, ref_full, Nq, Nkv, what, rows=None):
@@ -52,13 +60,13 @@ SMALL = [(256, 64, 512), (200, 36, 384), (1024, 128, 1024)]
 
 
 @pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
-@pytest.mark.parametrize("M", [1, 5, 16])
+@pytest.mark.parametrize("M", [1, 5, 16, 40])
 @pytest.mark.parametrize("Nq,Nkv,K", SMALL)
 def test_qkv_decode(B, fmt, M, Nq, Nkv, K):
     N = Nq + 2 * Nkv
     pk = _pack(fmt, inputs.weights(Nq + K, N, K, 0.05))
     xb, xf = inputs.activations(M + Nq, M, K)
-    got = _qkv(B, fmt, xb, pk, Nq, Nkv)
+    got = _qkv(B, fmt, xb, pk, Nq, Nkv, path="decode")
     _check(got, linear.linear_w4a16(fmt, xf, *pk), Nq, Nkv, "%s M=%d" % (fmt, M))
 
 
@@ -69,7 +77,7 @@ def test_qkv_tensor_core(B, fmt, M, Nq, Nkv, K):
     N = Nq + 2 * Nkv
     pk = _pack(fmt, inputs.weights(Nq + K + 1, N, K, 0.05))
     xb, xf = inputs.activations(M + Nq + 1, M, K)
-    got = _qkv(B, fmt, xb, pk, Nq, Nkv)
+    got = _qkv(B, fmt, xb, pk, Nq, Nkv, path="tc")
     _check(got, linear.linear_w4a16(fmt, xf, *pk), Nq, Nkv, "%s M=%d" % (fmt, M))
 
 

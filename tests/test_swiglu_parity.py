@@ -107,7 +107,7 @@ DECODE_CASES = [(8, 128), (128, 4096), (2048, 256), (1000, 1152), (520, 512), (1
 
 
 @pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
-@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16, 24, 40])
 @pytest.mark.parametrize("F,K", DECODE_CASES)
 def test_swiglu_decode(B, fmt, M, F, K):
     pk = _stacked(fmt, F, K, F * 3 + K)
@@ -166,8 +166,8 @@ def test_swiglu_rejects_bad_shapes(B):
     with pytest.raises(ValueError):
         B.gemm_w4a16_swiglu("int4_g128", X, *pk)
     pk = [to_dev(a) for a in _stacked("int4_g128", 16, K, 2)]
-    X = torch.zeros((17, K), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError):     # the decode kernel takes M <= 16
+    X = torch.zeros((65, K), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):     # the decode kernel takes M <= 64
         B.gemv_w4a16_swiglu("int4_g128", X, *pk)
 
 
