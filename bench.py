@@ -11,11 +11,13 @@ and timed with CUDA events on its stream.
 
 Secondary measurements in the same run (same JSON line): prefill GEMM TFLOP/s on the
 Qwen2.5-72B shapes at M = 2048 and M = 8192, MXFP4 decode, the fused gate+up projection with
-its SwiGLU epilogue (decode and prefill, beside the plain projection), the quantize kernels,
-and the GEMV/GEMM crossover on K = N = 8192.
+its SwiGLU epilogue and the fused QKV projection with its Q/K/V split (decode and prefill,
+each beside the plain projection), the quantize kernels, GPTQ (sweep, on-device factor, end
+to end from calibration activations), AWQ, and the GEMV/GEMM crossover on K = N = 8192 plus
+the decode shapes, whose crossover points become the dispatch thresholds of the run.
 
 --impl reference times the CPU oracle (test infrastructure, float64) on a bounded sample
-of the same workload on the host cores.
+of the same workload on all host cores (the BLAS thread pool of the matmul).
 """
 from __future__ import annotations
 
@@ -37,7 +39,9 @@ DECODE_M = (1, 4, 16)
 PREFILL_SHAPES = [(8192, 10240), (8192, 8192), (8192, 59136), (29568, 8192)]
 PREFILL_M = 2048
 PREFILL_M_LARGE = 8192
-CROSS_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048)
+CROSS_M = (1, 2, 4, 8, 16, 24, 32, 48, 64, 128, 256, 512, 1024, 2048)
+DECODE_MAX_M = 64          # activation rows the decode kernel accepts
+THRESH_M = (16, 24, 32, 48, 64)   # the crossover points measured on each decode shape
 COPIES = 3
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 
@@ -149,8 +153,24 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------------- CPU oracle
+def host_threads():
+    """The host cores this process may run on, and the threads the BLAS pool of the oracle's
+    matmul uses (threadpoolctl where installed, else the OpenMP/BLAS environment)."""
+    cores = len(os.sched_getaffinity(0))
+    used = None
+    try:
+        from threadpoolctl import threadpool_info
+        used = max((d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"), default=None)
+    except Exception:
+        pass
+    if not used:
+        used = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or cores)
+    return cores, used
+
+
 def oracle_sample(seconds_budget, steps=1):
-    """Times the float64 oracle on a bounded sample of the decode workload (single-threaded).
+    """Times the float64 oracle on a bounded sample of the decode workload (all host cores:
+    the matmul runs on the BLAS thread pool; the dequantization is numpy elementwise code).
 
     Returns (algorithmic bytes processed, seconds, description).  The sample: for each of the
     12 layer calls, the first R weight rows (output columns) -- dequantize them and multiply."""
@@ -190,23 +210,31 @@ def oracle_sample(seconds_budget, steps=1):
     return total_b, t, desc
 
 
+def _all_core_env():
+    n = str(len(os.sched_getaffinity(0)))
+    return dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n)
+
+
 def cpu_baseline_subprocess(budget):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(budget)], env=env,
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-sample", str(budget)], env=_all_core_env(),
                        capture_output=True, text=True, timeout=600)
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+        return {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": d["desc"]}
+    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": d["threads"],
+            "host_cores": d["cores"], "kind": "oracle", "sample": d["desc"]}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ.setdefault(v, "1")
+    if os.environ.get("WQ_BENCH_CPU_CHILD") != "1":
+        # the BLAS pool sizes itself at import: run the timing in a child with all cores set
+        env = dict(_all_core_env(), WQ_BENCH_CPU_CHILD="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--impl", "reference", "--gpus", str(args.gpus),
+                            "--steps", str(args.steps), "--warmup", str(args.warmup)], env=env)
+        return r.returncode
     budget = 150.0 / max(1, args.steps + args.warmup)
     # warm-up passes (untimed), then K timed passes, each a bounded sample
     for _ in range(args.warmup):
@@ -218,13 +246,15 @@ def run_reference(args):
         tb += b
         tt += t
     v = tb / tt / 1e9
+    cores, threads = host_threads()
     out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / max(1, args.steps),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded normal weights with 1% x10 outlier input columns; N(0,1) bf16 activations)",
            "config": {"workload": "decode: LLaMA-3-8B projections (K,N) in {(4096,6144),(4096,4096),(4096,28672),"
                                   "(14336,4096)} x M in {1,4,16}, INT4 g128 asym (bounded row sample on CPU)"},
-           "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+           "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "host_cores": cores, "kind": "oracle",
+                            "sample": desc},
            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out))
     return 0
@@ -481,6 +511,20 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                                      "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12,
                                      "plain_gate_up_us": per_layer[gi]["us"]}
             del ysw
+            # QKV split on the fused QKV projection (GQA 64/8, d_head 128: Nq = 8192, Nkv = 1024)
+            qi = PREFILL_SHAPES.index((8192, 10240))
+            yq = (torch.empty((Mp, 8192), dtype=torch.bfloat16, device=dev),
+                  torch.empty((Mp, 1024), dtype=torch.bfloat16, device=dev),
+                  torch.empty((Mp, 1024), dtype=torch.bfloat16, device=dev))
+            fq = (lambda: binding.gemm_w4a16_qkv("int4_g128", Xp[8192], pre[qi][0], pre[qi][1], pre[qi][2],
+                                                 Nq=8192, Nkv=1024, out=yq, workspace=wsp))
+            ms = _graph_time(fq, stream, dev, max(3, reps // 5))
+            fl = 2.0 * Mp * 10240 * 8192
+            out["qkv_prefill"] = {"workload": "Qwen2.5-72B fused QKV (K=8192, Nq=8192, Nkv=1024) written as Q, K, V "
+                                              "by the epilogue, INT4 g128, M=%d" % Mp,
+                                  "us": ms * 1e3, "tflops": fl / (ms * 1e-3) / 1e12,
+                                  "plain_fused_us": per_layer[qi]["us"]}
+            del yq
         del Xp, Yp
         torch.cuda.empty_cache()
     del pre
@@ -548,6 +592,28 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
     out["swiglu_decode"] = {"workload": "LLaMA-3-8B fused gate+up (K=4096, 2F=28672) with SiLU(gate)*up "
                                         "in the epilogue, INT4 g128, Y [M, 14336]", "points": sw}
 
+    # QKV split on the fused QKV projection (LLaMA-3-8B: GQA 32/8, d_head 128: Nq = 4096,
+    # Nkv = 1024), beside the plain projection writing one [M, 6144] tensor.
+    qi = DECODE_SHAPES.index((4096, 6144))
+    qk = []
+    for M in DECODE_M:
+        yq = (torch.empty((M, 4096), dtype=torch.bfloat16, device=dev), torch.empty((M, 1024), dtype=torch.bfloat16, device=dev),
+              torch.empty((M, 1024), dtype=torch.bfloat16, device=dev))
+        wsq = binding.Workspace(dev).get(binding.gemm_workspace_bytes("int4_g128", M, 4096, 6144))
+
+        def fq(M=M, yq=yq, wsq=wsq):
+            for c in range(COPIES):
+                Wq, s, z = layers[qi][c]
+                binding.gemm_w4a16_qkv("int4_g128", X[(M, 4096)], Wq, s, z, Nq=4096, Nkv=1024, out=yq, workspace=wsq)
+
+        ms = _graph_time(fq, stream, dev, reps) / COPIES
+        b = decode_bytes(M, 4096, 6144)
+        plain = next(q["us"] for q in per if q["K"] == 4096 and q["N"] == 6144 and q["M"] == M)
+        qk.append({"M": M, "us": ms * 1e3, "GBps": b / (ms * 1e-3) / 1e9, "frac": b / (ms * 1e-3) / 1e9 / hbm_peak,
+                   "plain_fused_us": plain})
+    out["qkv_decode"] = {"workload": "LLaMA-3-8B fused QKV (K=4096, Nq=4096, Nkv=1024) written as Q, K, V by the "
+                                     "epilogue, INT4 g128", "points": qk}
+
     # GPTQ sweep (INT4 g128) on a LLaMA-3-8B projection (N = K = 4096).  The factor is the
     # seeded stand-in (the sweep's work does not depend on its values).  Bound: fp32 ALU, one
     # multiply and one subtract per update, N K^2 / 2 updates.
@@ -561,7 +627,22 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                              "roofline": {"bound": "alu", "achieved": upd / (ms * 1e-3) / 1e12, "peak": alu_peak,
                                           "unit": "T updates/s", "frac": upd / (ms * 1e-3) / 1e12 / alu_peak,
                                           "note": "peak = SMs x 128 fp32 lanes x max SM clock / 2 ops per update"}}
-    del Wg, Ug
+    del Ug
+    # GPTQ's inverse-Hessian factor on the device from 128 calibration samples (float64:
+    # H = 2 X^T X + lambda I, blocked Cholesky, blocked triangular inverse), and GPTQ end to end
+    # (factor + sweep).  Flop count 2 n K^2 + K^3 / 3 + K^3 / 3 against the nominal fp64 rate.
+    Xg = torch.from_numpy(inputs.calibration(5102, 128, 4096)).to(dev)
+    wsg = torch.empty(binding.load_library().wq_gptq_workspace_bytes(4096), dtype=torch.uint8, device=dev)
+    ms_f = _graph_time(lambda: binding.gptq_factor(Xg, workspace=wsg), stream, dev, 3, warm=1)
+    ms_e = _graph_time(lambda: binding.gptq_int4_g128_calib(Wg, Xg, workspace=wsg), stream, dev, 2, warm=1)
+    flf = 2.0 * 128 * 4096 ** 2 + 2.0 * 4096 ** 3 / 3
+    fp64_nominal = 1.25   # TFLOP/s, the part's nominal fp64 rate (no measured fp64 peak)
+    out["gptq_factor"] = {"workload": "H = 2 X^T X + lambda I and the upper factor of H^-1, K = 4096, n = 128",
+                          "ms": ms_f, "end_to_end_ms": ms_e,
+                          "roofline": {"bound": "fp64", "achieved": flf / (ms_f * 1e-3) / 1e12, "peak": fp64_nominal,
+                                       "unit": "TFLOP/s", "frac": flf / (ms_f * 1e-3) / 1e12 / fp64_nominal,
+                                       "note": "peak = nominal fp64 rate (fallback, not measured)"}}
+    del Wg, Xg, wsg
     torch.cuda.empty_cache()
 
     # AWQ search (21 exponents) + packing on the same projection, 128 calibration samples.
@@ -612,7 +693,7 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                 ys = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                 row = {"M": M}
                 for kname, kfn in (("gemv", binding.gemv_w4a16), ("tc", binding.gemm_tc_w4a16)):
-                    if kname == "gemv" and M > 16:
+                    if kname == "gemv" and M > DECODE_MAX_M:
                         continue
                     wsx = binding.Workspace(dev).get(binding.gemm_workspace_bytes(fmt, M, K, N))
 
@@ -627,13 +708,53 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
                         continue
                     row[kname] = {"us": ms * 1e3, "GBps": decode_bytes(M, K, N) / (ms * 1e-3) / 1e9,
                                   "TFLOPs": 2.0 * M * N * K / (ms * 1e-3) / 1e12}
-                if "gemv" in row and "tc" in row and "us" in row.get("gemv", {}) and "us" in row.get("tc", {}):
-                    if row["gemv"]["us"] <= row["tc"]["us"]:
-                        best_T = M
                 pts.append(row)
-            sweep[fmt] = {"points": pts, "threshold_T": best_T}
+            best_T = crossover_T(pts)
+            binding.set_dispatch_threshold(fmt, K, N, best_T)
+            sweep[fmt] = {"points": pts, "threshold_T": best_T, "applied": True}
         out["crossover_8192"] = sweep
+        # the decode shapes: the crossover around the decode kernel's limit, per format
+        th = {}
+        for fmt in ("int4_g128", "mxfp4"):
+            th[fmt] = {}
+            for i, (K, N) in enumerate(DECODE_SHAPES):
+                W = torch.from_numpy(inputs.weights(4100 + i, N, K, 0.02)).to(dev)
+                pk = binding.quantize_int4_g128(W) if fmt == "int4_g128" else binding.quantize_mxfp4(W)
+                cps = [pk] + [tuple(t.clone() for t in pk) for _ in range(COPIES - 1)]
+                del W
+                pts = []
+                for M in THRESH_M:
+                    Xs = torch.from_numpy(inputs.activations(4100 + M, M, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+                    ys = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                    wsx = binding.Workspace(dev).get(binding.gemm_workspace_bytes(fmt, M, K, N))
+                    row = {"M": M}
+                    for kname, kfn in (("gemv", binding.gemv_w4a16), ("tc", binding.gemm_tc_w4a16)):
+                        def f(kfn=kfn, Xs=Xs, ys=ys, wsx=wsx):
+                            for c in cps:
+                                kfn(fmt, Xs, c[0], c[1], c[2] if fmt == "int4_g128" else None, out=ys, workspace=wsx)
+                        row[kname] = {"us": _graph_time(f, stream, dev, max(3, reps // 5)) / COPIES * 1e3}
+                    pts.append(row)
+                T = crossover_T(pts, lower=16)
+                binding.set_dispatch_threshold(fmt, K, N, T)
+                th[fmt]["%dx%d" % (K, N)] = {"T": T, "points": pts}
+                del cps, pk
+            torch.cuda.empty_cache()
+        out["dispatch_thresholds"] = {"how": "per (fmt, K, N): the largest M of the measured points up to which the "
+                                             "decode kernel is at least as fast as the tensor-core kernel at every "
+                                             "point; applied with wq_set_dispatch_threshold", "table": th}
     return out
+
+
+def crossover_T(pts, lower=0):
+    """The largest M such that the decode kernel is no slower than the tensor-core kernel at
+    every measured M up to it (points without a decode time end the run)."""
+    T = lower
+    for r in pts:
+        g, c = r.get("gemv", {}), r.get("tc", {})
+        if "us" not in g or "us" not in c or g["us"] > c["us"]:
+            break
+        T = r["M"]
+    return T
 
 
 def run_ncu_case(args):
@@ -740,7 +861,8 @@ def main():
     args = ap.parse_args()
     if args.cpu_sample is not None:
         b, t, d = oracle_sample(args.cpu_sample, 1)
-        print(json.dumps({"bytes": b, "seconds": t, "desc": d}))
+        cores, threads = host_threads()
+        print(json.dumps({"bytes": b, "seconds": t, "desc": d, "cores": cores, "threads": threads}))
         return 0
     if args.warmup < 3:
         args.warmup = 3
