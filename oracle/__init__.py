@@ -23,6 +23,8 @@ section):
   inverse-Hessian error compensation of 第 1 章：推理加速全景 §4.2.
 * ``awq``       -- AWQ: per-channel scaling of the salient input channels, its exponent
   found by a grid search, before INT4 g128 quantization (第 1 章 §4.4).
+* ``fp8``       -- W8A8 in FP8 E4M3 (推理优化与量化算子深度技术调研 §1.4): per-output-channel
+  weight scales, per-token activation scales, the layer on the quantized operands.
 
 Quantization arithmetic runs in float32 (the precision the pages' torch code
 works in) so that integer decisions -- codes, zero points, exponents -- are
@@ -33,4 +35,4 @@ Pins (tests/test_oracle_pins.py, tests/golden/): the pages' worked example and
 asserts, closed forms, brute force on tiny inputs, invariants and special
 cases.  Every function here is pinned; none is "parity unpinned".
 """
-from . import uniform, int4_g128, mxfp4, linear, swiglu, gptq, awq  # noqa: F401
+from . import uniform, int4_g128, mxfp4, linear, swiglu, gptq, awq, fp8  # noqa: F401

@@ -11,7 +11,7 @@ import inspect
 import numpy as np
 import pytest
 
-from oracle import awq, gptq, int4_g128, linear, mxfp4, swiglu
+from oracle import awq, fp8, gptq, int4_g128, linear, mxfp4, swiglu
 from tests import test_oracle_pins as pins
 
 PINS = [f for n, f in inspect.getmembers(pins, inspect.isfunction)
@@ -187,6 +187,46 @@ def _awq_loss_multiplied(W, X, s):
     return float(np.sum(E * E))
 
 
+def _e4m3_round_variant(ties_even=True, saturate=True, keep_sign=True):
+    mag = fp8.e4m3_values()[:127]
+
+    def rnd(v):
+        v = np.asarray(v, dtype=np.float32)
+        a = np.abs(v).astype(np.float64)
+        hi = np.clip(np.searchsorted(mag, a, side="left"), 1, 126)
+        lo = hi - 1
+        dl, dh = a - mag[lo], mag[hi] - a
+        code = np.where(dl < dh, lo, hi)
+        if ties_even:
+            code = np.where(dl == dh, np.where(lo % 2 == 0, lo, hi), code)
+        else:
+            code = np.where(dl == dh, lo, code)
+        code = np.where(a >= 448.0, 126 if saturate else 127, code)
+        code = np.where(a == 0.0, 0, code)
+        sign = (v.view(np.uint32) >> np.uint32(31)).astype(np.uint8)
+        if not keep_sign:
+            sign = np.where(code == 0, 0, sign).astype(np.uint8)
+        return ((sign << np.uint8(7)) | code.astype(np.uint8)).astype(np.uint8)
+    return rnd
+
+
+def _fp8_quantize_rows(fmax=448.0, zero_rule=True):
+    def q(A):
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        amax = np.abs(A).max(axis=1)
+        s = (amax / np.float32(fmax)).astype(np.float32)
+        if zero_rule:
+            s[s == 0] = np.float32(1)
+        with np.errstate(all="ignore"):
+            return fp8.e4m3_round(A / s[:, None]), s
+    return q
+
+
+def _fp8_linear_one_scale(Xq, s_x, Wq, s_w):
+    v = fp8.e4m3_values()
+    return (v[np.asarray(Xq)] @ v[np.asarray(Wq)].T) * np.asarray(s_x, dtype=np.float64)[:, None]
+
+
 MUTATIONS = {
     "int4: zero not in the range": (int4_g128, "group_params", _group_params(zero_in_range=False)),
     "int4: sign of the zero point": (int4_g128, "group_params", _group_params(z_sign=-1.0)),
@@ -213,6 +253,12 @@ MUTATIONS = {
     "gptq: Hessian without the factor 2": (gptq, "hessian", _hessian_no_factor_two),
     "awq: exponent sign (activations scaled up)": (awq, "scales", _awq_scales_inverted),
     "awq: loss multiplies instead of dividing": (awq, "loss", _awq_loss_multiplied),
+    "fp8: ties to the lower code": (fp8, "e4m3_round", _e4m3_round_variant(ties_even=False)),
+    "fp8: no saturation (NaN code)": (fp8, "e4m3_round", _e4m3_round_variant(saturate=False)),
+    "fp8: sign of -0 dropped": (fp8, "e4m3_round", _e4m3_round_variant(keep_sign=False)),
+    "fp8: E4M3 maximum taken as 240": (fp8, "quantize_rows", _fp8_quantize_rows(fmax=240.0)),
+    "fp8: no zero-row scale rule": (fp8, "quantize_rows", _fp8_quantize_rows(zero_rule=False)),
+    "fp8: weight scale dropped in the layer": (fp8, "linear_w8a8", _fp8_linear_one_scale),
 }
 
 

@@ -662,3 +662,122 @@ def test_awq_search_protects_salient_channels():
     assert losses[a] == losses.min() and 0 < a < awq.GRID
     assert losses[a] < 0.8 * losses[0]
     assert (np.asarray(pk[0]) == np.asarray(awq.quantize_scaled(W, s)[0])).all()
+
+
+# ------------------------------------------------------------------ FP8 E4M3 W8A8 (oracle/fp8.py)
+# 推理优化与量化算子深度技术调研 §1.4 (E4M3 weights and activations with FP32 scales beside the
+# tensor) and 量化与加速's format table (E4M3: 4 exponent bits, 3 mantissa bits, +-448).
+
+def _e4m3_by_bits(c):
+    """E4M3 code -> value by moving its fields into a float32 bit pattern (an independent
+    formulation of the format: normal values are 1.m x 2^(e-7), subnormals m/8 x 2^-6)."""
+    import struct
+    s, e, m = c >> 7, (c >> 3) & 0xF, c & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        v = m * 2.0 ** -9
+    else:
+        v = struct.unpack("<f", struct.pack("<I", ((e - 7 + 127) << 23) | (m << 20)))[0]
+    return -v if s else v
+
+
+def test_e4m3_value_set():
+    from oracle import fp8
+    v = fp8.e4m3_values()
+    for c in range(256):
+        b = _e4m3_by_bits(c)
+        assert (np.isnan(b) and np.isnan(v[c])) or b == v[c], hex(c)
+    # named points of the format: 1.0, 1.5, 2.0, the largest finite value 448 and the next
+    # one down 416 / the value 240, the smallest normal 2^-6 and subnormal 2^-9
+    assert (v[0x38], v[0x3C], v[0x40], v[0x7E], v[0x7D], v[0x77]) == (1.0, 1.5, 2.0, 448.0, 416.0, 240.0)
+    assert (v[0x08], v[0x01], v[0x80]) == (2.0 ** -6, 2.0 ** -9, 0.0)
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and int(np.isfinite(v).sum()) == 254
+    assert np.nanmax(v) == fp8.E4M3_MAX == 448.0
+
+
+def test_e4m3_rounding_ties_saturation_and_signed_zero():
+    from oracle import fp8
+    cases = [  # (value, code): hand-derived from the value grid
+        (1.0625, 0x38),      # halfway 1 | 1.125 -> even code 0x38
+        (1.1875, 0x3A),      # halfway 1.125 | 1.25 -> even code 0x3A
+        (1.05, 0x38), (1.07, 0x39), (1.1, 0x39),
+        (15.5, 0x58),        # halfway 15 (0x57) | 16 (0x58) -> 0x58
+        (440.0, 0x7E), (420.0, 0x7D), (432.0, 0x7E),   # 432 halfway 416 | 448 -> even 0x7E
+        (464.0, 0x7E), (1.0e6, 0x7E),                   # saturation at 448
+        (2.0 ** -10, 0x00),  # halfway 0 | 2^-9 -> even code 0
+        (3 * 2.0 ** -10, 0x02),   # halfway 2^-9 | 2^-8 -> even 0x02
+        (2.0 ** -9, 0x01), (2.0 ** -6, 0x08), (0.0, 0x00),
+        (-1.0, 0xB8), (-448.0, 0xFE), (-1.0e9, 0xFE),
+    ]
+    for x, c in cases:
+        got = int(fp8.e4m3_round(np.float32(x)))
+        assert got == c, "%r -> %#x, expected %#x" % (x, got, c)
+    assert int(fp8.e4m3_round(np.float32(-0.0))) == 0x80                  # sign kept on zero
+    assert int(fp8.e4m3_round(np.float32(-2.0 ** -11))) == 0x80            # rounds to -0
+
+
+def test_e4m3_code_is_nearest_finite_value():
+    from oracle import fp8
+    rng = np.random.default_rng(811)
+    x = np.concatenate([rng.standard_normal(4000) * 50, rng.standard_normal(2000) * 0.01,
+                        rng.uniform(-470, 470, 2000)]).astype(np.float32)
+    codes = fp8.e4m3_round(x)
+    grid = np.array([_e4m3_by_bits(c) for c in range(256)])
+    fin = np.isfinite(grid)
+    for xi, ci in zip(x.astype(np.float64), codes):
+        d = np.abs(grid[fin] - min(max(xi, -448.0), 448.0))
+        assert abs(grid[ci] - min(max(xi, -448.0), 448.0)) == d.min()
+        if np.sum(d == d.min()) > 1 and grid[ci] != 0.0:                  # a tie: the even code
+            assert ci % 2 == 0
+
+
+def test_fp8_row_scales_closed_forms():
+    from oracle import fp8
+    # a row whose largest magnitude is 448 * 2^-3 has the scale 2^-3 exactly; values on the
+    # scaled grid come back exactly
+    grid = np.array([_e4m3_by_bits(c) for c in range(0x7F)])
+    W = (np.array([grid[[0x7E, 0x38, 0x3C, 0x01, 0x00, 0x55]], -grid[[0x40, 0x77, 0x08, 0x7D, 0x10, 0x20]]])
+         * 2.0 ** -3).astype(np.float32)
+    q, s = fp8.quantize_weights(W)
+    assert s[0] == np.float32(2.0 ** -3)
+    assert np.array_equal(fp8.dequantize_rows(q[:1], s[:1]), W[:1].astype(np.float64))
+    assert int(q[0, 0]) == 0x7E                          # the row's maximum maps to 448
+    # a zero row gets the scale 1 and the codes 0 (F3); -0.0 keeps its sign
+    q, s = fp8.quantize_activations(np.array([[0.0, -0.0, 0.0, 0.0]], np.float32))
+    assert s[0] == 1.0 and list(q[0]) == [0x00, 0x80, 0x00, 0x00]
+    # the scale is amax / 448 rounded to float32, and x / s rounds per element
+    x = np.array([[3.0, -1.0, 0.5, 0.0]], np.float32)
+    q, s = fp8.quantize_activations(x)
+    assert s[0] == np.float32(np.float32(3.0) / np.float32(448.0))
+    assert int(q[0, 0]) == 0x7E and int(q[0, 1]) & 0x80
+
+
+def test_fp8_error_bound():
+    from oracle import fp8
+    # inside the normal range the E4M3 spacing is 2^(e-3) on [2^e, 2^(e+1)): the error of a
+    # value is at most half of that, i.e. relative 2^-4, plus the subnormal floor 2^-10 s
+    rng = np.random.default_rng(813)
+    X = (rng.standard_normal((6, 512)) * np.array([1e-3, 0.1, 1, 10, 1e3, 1e5])[:, None]).astype(np.float32)
+    q, s = fp8.quantize_activations(X)
+    err = np.abs(fp8.dequantize_rows(q, s) - X.astype(np.float64))
+    bound = np.abs(X).astype(np.float64) * 2.0 ** -4 + s.astype(np.float64)[:, None] * 2.0 ** -10
+    assert (err <= bound * (1 + 1e-6)).all()
+
+
+def test_fp8_linear_brute_force_fractions():
+    from oracle import fp8
+    M, K, N = 3, 64, 4
+    rng = np.random.default_rng(817)
+    W = rng.standard_normal((N, K)).astype(np.float32) * 0.05
+    _, X = inputs.activations(819, M, K)
+    Wq, sw = fp8.quantize_weights(W)
+    Xq, sx = fp8.quantize_activations(X)
+    Y = fp8.linear_w8a8(Xq, sx, Wq, sw)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(_e4m3_by_bits(int(Xq[m, k]))) * Fraction(_e4m3_by_bits(int(Wq[n, k])))
+                        for k in range(K)) * Fraction(float(sx[m])) * Fraction(float(sw[n]))
+            assert abs(Fraction(float(Y[m, n])) - exact) <= Fraction(1, 10 ** 12) * (1 + abs(exact))
+    rows = np.array([2, 0])
+    assert np.array_equal(fp8.linear_w8a8_rows(Xq, sx, Wq, sw, rows), Y[:, rows])
