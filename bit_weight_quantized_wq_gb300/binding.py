@@ -33,6 +33,8 @@ EXPORTED = [
     "wq_gemm_w4a16_swiglu", "wq_gemv_w4a16_swiglu", "wq_gemm_tc_w4a16_swiglu", "wq_interleave_gate_up",
     "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128", "wq_selftest_wait_timeout",
     "wq_gemm_w4a16_qkv", "wq_gptq_workspace_bytes", "wq_gptq_factor", "wq_gptq_int4_g128_calib",
+    "wq_quantize_fp8_weights", "wq_quantize_fp8_activations", "wq_gemm_fp8", "wq_gemm_w8a8_fp8_workspace_bytes",
+    "wq_gemm_w8a8_fp8",
 ]
 
 _lib = None
@@ -73,6 +75,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_gptq_workspace_bytes": (SZ, [I64]),
         "wq_gptq_factor": (I32, [P, I64, I64, P, P, SZ, P]),
         "wq_gptq_int4_g128_calib": (I32, [P, I64, I64, P, I64, P, P, P, P, SZ, P]),
+        "wq_quantize_fp8_weights": (I32, [P, I64, I64, P, P, P]),
+        "wq_quantize_fp8_activations": (I32, [P, I64, I64, P, P, P]),
+        "wq_gemm_fp8": (I32, [P, P, I64, I64, I64, P, P, P, P]),
+        "wq_gemm_w8a8_fp8_workspace_bytes": (SZ, [I64, I64]),
+        "wq_gemm_w8a8_fp8": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -468,3 +475,69 @@ def read_error_flags() -> int:
     v = ctypes.c_uint32(0)
     _check(load_library().wq_read_error_flags(ctypes.byref(v)), "wq_read_error_flags")
     return int(v.value)
+
+
+# ------------------------------------------------------------------ FP8 E4M3 W8A8
+def quantize_fp8_weights(W: torch.Tensor, stream=None):
+    """W float32 [N, K] (CUDA) -> (Wq uint8 [N, K] E4M3 codes, s_w float32 [N]), one scale per
+    output channel."""
+    _need(W, torch.float32, "W")
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    Wq = torch.empty((N, K), dtype=torch.uint8, device=W.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _check(load_library().wq_quantize_fp8_weights(_ptr(W), N, K, _ptr(Wq), _ptr(sw), _stream(stream, W.device)),
+           "wq_quantize_fp8_weights")
+    return Wq, sw
+
+
+def quantize_fp8_activations(X: torch.Tensor, stream=None):
+    """X bf16 [M, K] (CUDA) -> (Xq uint8 [M, K] E4M3 codes, s_x float32 [M]), one scale per token."""
+    _need(X, _BF16, "X")
+    if X.dim() != 2:
+        raise ValueError("X must be [M, K]")
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(load_library().wq_quantize_fp8_activations(_ptr(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream, X.device)),
+           "wq_quantize_fp8_activations")
+    return Xq, sx
+
+
+def _fp8_operands(Wq, sw, K, dev):
+    _need(Wq, torch.uint8, "Wq")
+    _need(sw, torch.float32, "s_w")
+    if Wq.dim() != 2 or Wq.shape[1] != K or Wq.device != dev:
+        raise ValueError("Wq must be [N, K] on the activations' device")
+    if sw.shape != (Wq.shape[0],) or sw.device != dev:
+        raise ValueError("s_w must be [N] on the activations' device")
+    return Wq.shape[0]
+
+
+def gemm_fp8(Xq, sx, Wq, sw, out=None, stream=None):
+    """Y bf16 [M, N] = s_x s_w^T * (E4M3(Xq) E4M3(Wq)^T) on the tensor cores."""
+    _need(Xq, torch.uint8, "Xq")
+    _need(sx, torch.float32, "s_x")
+    M, K = Xq.shape
+    if sx.shape != (M,) or sx.device != Xq.device:
+        raise ValueError("s_x must be [M] on Xq's device")
+    N = _fp8_operands(Wq, sw, K, Xq.device)
+    Y = _output(out, M, N, Xq.device, "out")
+    _check(load_library().wq_gemm_fp8(_ptr(Xq), _ptr(sx), M, K, N, _ptr(Wq), _ptr(sw), _ptr(Y), _stream(stream, Xq.device)),
+           "wq_gemm_fp8")
+    return Y
+
+
+def gemm_w8a8_fp8(X, Wq, sw, out=None, workspace=None, stream=None):
+    """The W8A8 FP8 layer from bf16 activations: per-token quantization of X, then the GEMM."""
+    _need(X, _BF16, "X")
+    M, K = X.shape
+    N = _fp8_operands(Wq, sw, K, X.device)
+    Y = _output(out, M, N, X.device, "out")
+    lib = load_library()
+    need = lib.wq_gemm_w8a8_fp8_workspace_bytes(M, K)
+    ws = workspace if workspace is not None else Workspace(X.device).get(need)
+    _check(lib.wq_gemm_w8a8_fp8(_ptr(X), M, K, N, _ptr(Wq), _ptr(sw), _ptr(Y), _ptr(ws), ws.numel(),
+                                _stream(stream, X.device)), "wq_gemm_w8a8_fp8")
+    return Y

@@ -148,6 +148,8 @@ wq_status check_linear_args(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K,
 
 wq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? WQ_OK : WQ_ERR_CUDA; }
 
+size_t round_up256(size_t b) { return (b + 255) / 256 * 256; }
+
 }  // namespace
 
 extern "C" {
@@ -432,12 +434,74 @@ const char* wq_status_str(wq_status s) {
   return "unknown wq_status";
 }
 
+// ------------------------------------------------------------------ FP8 E4M3 W8A8
+wq_status wq_quantize_fp8_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* scales, void* stream) {
+  if (!W || !Wq || !scales) return WQ_ERR_NULL;
+  if (N < 1 || K < 16 || K % 16 != 0 || N > (1LL << 30) || K > (1LL << 30)) return WQ_ERR_SHAPE;
+  if (!aligned16(W) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_quant_fp8_rows(false, W, N, K, Wq, scales, static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_quantize_fp8_activations(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* scales,
+                                      void* stream) {
+  if (!X || !Xq || !scales) return WQ_ERR_NULL;
+  if (M < 1 || K < 16 || K % 16 != 0 || M > (1LL << 30) || K > (1LL << 30)) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(Xq) || (reinterpret_cast<uintptr_t>(scales) & 3u)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_quant_fp8_rows(true, X, M, K, Xq, scales, static_cast<cudaStream_t>(stream)));
+}
+
+static wq_status check_fp8_gemm(int64_t M, int64_t K, int64_t N, const void* Wq, const float* s_w, uint16_t* Y) {
+  if (!Wq || !s_w || !Y) return WQ_ERR_NULL;
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30))
+    return WQ_ERR_SHAPE;
+  if (!aligned16(Wq) || !aligned16(Y) || (reinterpret_cast<uintptr_t>(s_w) & 3u)) return WQ_ERR_ALIGN;
+  return WQ_OK;
+}
+
+wq_status wq_gemm_fp8(const uint8_t* Xq, const float* s_x, int64_t M, int64_t K, int64_t N, const uint8_t* Wq,
+                      const float* s_w, uint16_t* Y, void* stream) {
+  if (!Xq || !s_x) return WQ_ERR_NULL;
+  wq_status st = check_fp8_gemm(M, K, N, Wq, s_w, Y);
+  if (st != WQ_OK) return st;
+  if (!aligned16(Xq) || (reinterpret_cast<uintptr_t>(s_x) & 3u)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_gemm_fp8(Xq, s_x, M, K, N, Wq, s_w, Y, static_cast<cudaStream_t>(stream)));
+}
+
+size_t wq_gemm_w8a8_fp8_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 1 || K < 1) return 0;
+  return round_up256(static_cast<size_t>(M) * static_cast<size_t>(K)) + round_up256(static_cast<size_t>(M) * 4);
+}
+
+wq_status wq_gemm_w8a8_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t N, const uint8_t* Wq, const float* s_w,
+                           uint16_t* Y, void* workspace, size_t ws_bytes, void* stream) {
+  if (!X) return WQ_ERR_NULL;
+  wq_status st = check_fp8_gemm(M, K, N, Wq, s_w, Y);
+  if (st != WQ_OK) return st;
+  if (!aligned16(X)) return WQ_ERR_ALIGN;
+  if (!workspace || ws_bytes < wq_gemm_w8a8_fp8_workspace_bytes(M, K)) return WQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  uint8_t* Xq = static_cast<uint8_t*>(workspace);
+  float* s_x = reinterpret_cast<float*>(Xq + round_up256(static_cast<size_t>(M) * static_cast<size_t>(K)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wq::launch_quant_fp8_rows(true, X, M, K, Xq, s_x, s);
+  if (e != cudaSuccess) return WQ_ERR_CUDA;
+  return from_cuda(wq::launch_gemm_fp8(Xq, s_x, M, K, N, Wq, s_w, Y, s));
+}
+
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;
   *out = wq::gemv_read_and_clear_error() | wq::gemm_tc_read_and_clear_error() |
          wq::gptq_read_and_clear_error() | wq::gptq_factor_read_and_clear_error() |
-         wq::selftest_read_and_clear_error();
+         wq::selftest_read_and_clear_error() | wq::fp8_read_and_clear_error();
   return cudaGetLastError() == cudaSuccess ? WQ_OK : WQ_ERR_CUDA;
 }
 

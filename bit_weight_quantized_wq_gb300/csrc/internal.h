@@ -105,6 +105,14 @@ cudaError_t launch_awq_int4_g128(const float* W, int64_t N, int64_t K, const flo
 
 // selftest.cu -- the bounded-wait path, exercised on demand
 uint32_t selftest_read_and_clear_error();
+
+// FP8 E4M3 W8A8 (gemm_fp8.cu): per-row quantization (fp32 weights or bf16 activations) and
+// the GEMM with per-token and per-channel scales in the epilogue.
+cudaError_t launch_quant_fp8_rows(bool bf16_in, const void* in, int64_t R, int64_t K, uint8_t* Q, float* scales,
+                                  cudaStream_t stream);
+cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* sx, int64_t M, int64_t K, int64_t N, const uint8_t* Wq,
+                            const float* sw, uint16_t* Y, cudaStream_t stream);
+uint32_t fp8_read_and_clear_error();
 cudaError_t run_selftest_wait(uint64_t limit_ns, uint32_t* timed_out_host, cudaStream_t stream);
 
 // layout.cu -- row re-layout of the stacked gate+up weight

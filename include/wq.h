@@ -359,6 +359,51 @@ wq_status wq_read_error_flags(uint32_t* out);
  */
 wq_status wq_selftest_wait_timeout(uint32_t limit_us, uint32_t* timed_out, void* stream);
 
+/*
+ * W8A8 in FP8 E4M3 -- the large-batch prefill format of 第 6 课：量化源码走读 §4 (W4A16 for
+ * small-batch decode, FP8 for large-batch prefill); the format of 推理优化与量化算子深度技术调研
+ * §1.4 (E4M3 tensors stored as torch.float8_e4m3fn with their FP32 scales beside them) and
+ * 量化与加速's format table (E4M3, +-448).
+ *
+ * Row quantization (both operands): per row r, s[r] = fp32(max_k |A[r, k]| / 448) (a zero
+ * row gets 1), and code[r, k] = E4M3(fp32(A[r, k] / s[r])), round to nearest with ties to the
+ * even code, saturating at +-448, the sign kept on a zero.  Codes and scales are bit-exact
+ * run to run and against the library's CPU reference.
+ *   wq_quantize_fp8_weights:     W [N, K] float32 -> Wq [N, K] uint8, scales [N] float32 (one
+ *                                per output channel; offline).
+ *   wq_quantize_fp8_activations: X [M, K] bf16 bits -> Xq [M, K] uint8, scales [M] float32
+ *                                (one per token, computed from the token's own values).
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless rows >= 1 and K % 16 == 0 (K >= 16);
+ *         WQ_ERR_ALIGN (arrays 16-byte aligned, scales 4-byte); WQ_ERR_UNSUPPORTED_ARCH;
+ *         WQ_ERR_CUDA.
+ */
+wq_status wq_quantize_fp8_weights(const float* W, int64_t N, int64_t K, uint8_t* Wq, float* scales, void* stream);
+wq_status wq_quantize_fp8_activations(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq, float* scales,
+                                      void* stream);
+
+/*
+ * Y[m, n] = bf16( s_x[m] * s_w[n] * sum_k E4M3(Xq[m, k]) * E4M3(Wq[n, k]) ): exact products,
+ * fp32 accumulation on the tensor cores (tcgen05.mma kind::f8f6f4), the two scales applied
+ * to the fp32 accumulator in the epilogue.
+ *   Xq [M, K] uint8, s_x [M] float32 (wq_quantize_fp8_activations); Wq [N, K] uint8, s_w [N]
+ *   float32 (wq_quantize_fp8_weights); Y [M, N] bf16 bits output.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless M, N >= 1 and K % 16 == 0 (K >= 16); WQ_ERR_ALIGN;
+ *         WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+wq_status wq_gemm_fp8(const uint8_t* Xq, const float* s_x, int64_t M, int64_t K, int64_t N, const uint8_t* Wq,
+                      const float* s_w, uint16_t* Y, void* stream);
+
+/*
+ * The W8A8 layer from bf16 activations: quantizes X per token into the workspace
+ * (wq_quantize_fp8_activations), then wq_gemm_fp8; both launches on `stream`.
+ *   workspace / ws_bytes: at least wq_gemm_w8a8_fp8_workspace_bytes(M, K) bytes (M K bytes of
+ *   codes and M scales), 16-byte aligned; its content on entry is irrelevant.
+ * Errors as wq_gemm_fp8, plus WQ_ERR_WORKSPACE.
+ */
+size_t wq_gemm_w8a8_fp8_workspace_bytes(int64_t M, int64_t K);
+wq_status wq_gemm_w8a8_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t N, const uint8_t* Wq, const float* s_w,
+                           uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
 /* WQ_OK when the current device is a GB300-class part (compute capability 10.3). */
 wq_status wq_check_device(void);
 

@@ -143,3 +143,23 @@ def test_selftest_argument_checks(lib):
     assert lib.wq_selftest_wait_timeout(1000, None, None) == 1
     assert lib.wq_selftest_wait_timeout(0, ctypes.byref(v), None) == 7
     assert lib.wq_selftest_wait_timeout(2000001, ctypes.byref(v), None) == 7
+
+
+def test_validation_errors_fp8(lib):
+    # quantizers: NULLs, K % 16, rows, alignment (arrays 16-byte, scales 4-byte)
+    assert lib.wq_quantize_fp8_weights(None, 4, 64, FAKE, FAKE, None) == 1
+    assert lib.wq_quantize_fp8_weights(FAKE, 4, 24, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_fp8_weights(FAKE, 0, 64, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_fp8_weights(ODD, 4, 64, FAKE, FAKE, None) == 3
+    assert lib.wq_quantize_fp8_activations(FAKE, 4, 64, FAKE, ctypes.c_void_p(0x10002), None) == 3
+    assert lib.wq_quantize_fp8_activations(FAKE, 4, 8, FAKE, FAKE, None) == 2
+    # GEMM: NULLs, shapes, alignment
+    g = lambda Xq=FAKE, sx=FAKE, M=4, K=64, N=8, Wq=FAKE, sw=FAKE, Y=FAKE: lib.wq_gemm_fp8(Xq, sx, M, K, N, Wq, sw, Y, None)
+    assert g(Xq=None) == 1 and g(sw=None) == 1 and g(Y=None) == 1
+    assert g(K=40) == 2 and g(M=0) == 2 and g(N=0) == 2
+    assert g(Wq=ODD) == 3 and g(Xq=ODD) == 3
+    # fused entry: workspace size and presence
+    assert lib.wq_gemm_w8a8_fp8_workspace_bytes(300, 1024) >= 300 * 1024 + 300 * 4
+    assert lib.wq_gemm_w8a8_fp8_workspace_bytes(0, 1024) == 0
+    f = lambda ws=FAKE, wsb=1 << 30, K=64: lib.wq_gemm_w8a8_fp8(FAKE, 4, K, 8, FAKE, FAKE, FAKE, ws, wsb, None)
+    assert f(ws=None) == 4 and f(wsb=16) == 4 and f(K=40) == 2
