@@ -25,6 +25,8 @@ section):
   found by a grid search, before INT4 g128 quantization (第 1 章 §4.4).
 * ``fp8``       -- W8A8 in FP8 E4M3 (推理优化与量化算子深度技术调研 §1.4): per-output-channel
   weight scales, per-token activation scales, the layer on the quantized operands.
+* ``w4a4``      -- W4A4 in MXFP4 (第 6 课：量化源码走读, micro-scaling formats): the activations
+  quantized by the weights' MXFP4 rules, the layer on both dequantized operands.
 
 Quantization arithmetic runs in float32 (the precision the pages' torch code
 works in) so that integer decisions -- codes, zero points, exponents -- are
@@ -35,4 +37,4 @@ Pins (tests/test_oracle_pins.py, tests/golden/): the pages' worked example and
 asserts, closed forms, brute force on tiny inputs, invariants and special
 cases.  Every function here is pinned; none is "parity unpinned".
 """
-from . import uniform, int4_g128, mxfp4, linear, swiglu, gptq, awq, fp8  # noqa: F401
+from . import uniform, int4_g128, mxfp4, linear, swiglu, gptq, awq, fp8, w4a4  # noqa: F401

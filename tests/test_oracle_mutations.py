@@ -11,7 +11,7 @@ import inspect
 import numpy as np
 import pytest
 
-from oracle import awq, fp8, gptq, int4_g128, linear, mxfp4, swiglu
+from oracle import awq, fp8, gptq, int4_g128, linear, mxfp4, swiglu, w4a4
 from tests import test_oracle_pins as pins
 
 PINS = [f for n, f in inspect.getmembers(pins, inspect.isfunction)
@@ -227,6 +227,10 @@ def _fp8_linear_one_scale(Xq, s_x, Wq, s_w):
     return (v[np.asarray(Xq)] @ v[np.asarray(Wq)].T) * np.asarray(s_x, dtype=np.float64)[:, None]
 
 
+def _w4a4_activation_scales_dropped(Xq, xs, Wq, ws):
+    return mxfp4.decode_e2m1(mxfp4.unpack(Xq)) @ mxfp4.dequantize(Wq, ws).T
+
+
 MUTATIONS = {
     "int4: zero not in the range": (int4_g128, "group_params", _group_params(zero_in_range=False)),
     "int4: sign of the zero point": (int4_g128, "group_params", _group_params(z_sign=-1.0)),
@@ -259,6 +263,7 @@ MUTATIONS = {
     "fp8: E4M3 maximum taken as 240": (fp8, "quantize_rows", _fp8_quantize_rows(fmax=240.0)),
     "fp8: no zero-row scale rule": (fp8, "quantize_rows", _fp8_quantize_rows(zero_rule=False)),
     "fp8: weight scale dropped in the layer": (fp8, "linear_w8a8", _fp8_linear_one_scale),
+    "w4a4: activation block scales dropped": (w4a4, "linear_w4a4", _w4a4_activation_scales_dropped),
 }
 
 

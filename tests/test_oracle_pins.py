@@ -781,3 +781,33 @@ def test_fp8_linear_brute_force_fractions():
             assert abs(Fraction(float(Y[m, n])) - exact) <= Fraction(1, 10 ** 12) * (1 + abs(exact))
     rows = np.array([2, 0])
     assert np.array_equal(fp8.linear_w8a8_rows(Xq, sx, Wq, sw, rows), Y[:, rows])
+
+
+# ------------------------------------------------------------------ W4A4 MXFP4 (oracle/w4a4.py)
+
+def test_w4a4_brute_force_fractions_and_grid_activations():
+    from oracle import w4a4
+    M, K, N = 2, 64, 3
+    W = inputs.weights(821, N, K, 0.05)
+    _, X = inputs.activations(823, M, K)
+    Xq, xs = w4a4.quantize_activations(X)
+    Wq, ws = mxfp4.quantize(W)
+    Y = w4a4.linear_w4a4(Xq, xs, Wq, ws)
+    # the layer is the exact sum of products of the two dequantized operands
+    xv = mxfp4.dequantize(Xq, xs)
+    wv = mxfp4.dequantize(Wq, ws)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(Fraction(float(xv[m, k])) * Fraction(float(wv[n, k])) for k in range(K))
+            assert abs(Fraction(float(Y[m, n])) - exact) <= Fraction(1, 10 ** 12) * (1 + abs(exact))
+    # activations already on the MXFP4 grid are quantized exactly, so the W4A4 layer then equals
+    # the W4A16 MXFP4 layer on the same activations
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    rng = np.random.default_rng(827)
+    Xg = (rng.choice(grid, (M, K)) * rng.choice([-1.0, 1.0], (M, K))).astype(np.float32)
+    Xg[:, ::32] = 6.0                                   # every block's max: scale 2^0
+    Xq, xs = w4a4.quantize_activations(Xg)
+    assert np.array_equal(mxfp4.dequantize(Xq, xs), Xg.astype(np.float64))
+    assert np.array_equal(w4a4.linear_w4a4(Xq, xs, Wq, ws), linear.linear_w4a16("mxfp4", Xg, Wq, ws))
+    rows = np.array([2, 0])
+    assert np.array_equal(w4a4.linear_w4a4_rows(Xq, xs, Wq, ws, rows), w4a4.linear_w4a4(Xq, xs, Wq, ws)[:, rows])
