@@ -34,7 +34,7 @@ EXPORTED = [
     "wq_gptq_int4_g128", "wq_awq_workspace_bytes", "wq_awq_int4_g128", "wq_selftest_wait_timeout",
     "wq_gemm_w4a16_qkv", "wq_gptq_workspace_bytes", "wq_gptq_factor", "wq_gptq_int4_g128_calib",
     "wq_quantize_fp8_weights", "wq_quantize_fp8_activations", "wq_gemm_fp8", "wq_gemm_w8a8_fp8_workspace_bytes",
-    "wq_gemm_w8a8_fp8",
+    "wq_gemm_w8a8_fp8", "wq_mxfp4_weights_to_e4m3", "wq_quantize_w4a4_activations", "wq_gemm_w4a4_mxfp4",
 ]
 
 _lib = None
@@ -80,6 +80,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "wq_gemm_fp8": (I32, [P, P, I64, I64, I64, P, P, P, P]),
         "wq_gemm_w8a8_fp8_workspace_bytes": (SZ, [I64, I64]),
         "wq_gemm_w8a8_fp8": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
+        "wq_mxfp4_weights_to_e4m3": (I32, [P, P, I64, I64, P, P, P]),
+        "wq_quantize_w4a4_activations": (I32, [P, I64, I64, P, P, P]),
+        "wq_gemm_w4a4_mxfp4": (I32, [P, I64, I64, I64, P, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -540,4 +543,48 @@ def gemm_w8a8_fp8(X, Wq, sw, out=None, workspace=None, stream=None):
     ws = workspace if workspace is not None else Workspace(X.device).get(need)
     _check(lib.wq_gemm_w8a8_fp8(_ptr(X), M, K, N, _ptr(Wq), _ptr(sw), _ptr(Y), _ptr(ws), ws.numel(),
                                 _stream(stream, X.device)), "wq_gemm_w8a8_fp8")
+    return Y
+
+
+# ------------------------------------------------------------------ W4A4 MXFP4 (FP8 tensor-core path)
+def mxfp4_weights_to_e4m3(Wq: torch.Tensor, scales: torch.Tensor, stream=None):
+    """MXFP4-packed weights (Wq int32 [N, K/8], E8M0 scales uint8 [N, K/32]) -> (Wq8 uint8 [N, K]
+    E4M3 codes, s_w float32 [N] powers of two): E4M3(Wq8) * s_w equals the dequantized MXFP4
+    weight exactly for every block within 14 binades of its row's largest."""
+    _need(Wq, _I32, "Wq")
+    _need(scales, _U8, "scales")
+    N, K8 = Wq.shape
+    K = 8 * K8
+    if scales.shape != (N, K // 32) or scales.device != Wq.device:
+        raise ValueError("scales must be [N, K/32] on Wq's device")
+    W8 = torch.empty((N, K), dtype=torch.uint8, device=Wq.device)
+    sw = torch.empty((N,), dtype=torch.float32, device=Wq.device)
+    _check(load_library().wq_mxfp4_weights_to_e4m3(_ptr(Wq), _ptr(scales), N, K, _ptr(W8), _ptr(sw),
+                                                    _stream(stream, Wq.device)), "wq_mxfp4_weights_to_e4m3")
+    return W8, sw
+
+
+def quantize_w4a4_activations(X: torch.Tensor, stream=None):
+    """bf16 X [M, K] -> MXFP4 per token (the weights' rules), re-encoded: (Xq8 uint8 [M, K] E4M3,
+    s_x float32 [M] powers of two)."""
+    _need(X, _BF16, "X")
+    M, K = X.shape
+    Xq = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+    sx = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(load_library().wq_quantize_w4a4_activations(_ptr(X), M, K, _ptr(Xq), _ptr(sx), _stream(stream, X.device)),
+           "wq_quantize_w4a4_activations")
+    return Xq, sx
+
+
+def gemm_w4a4_mxfp4(X, Wq8, sw, out=None, workspace=None, stream=None):
+    """The W4A4 MXFP4 layer from bf16 activations (weights from ``mxfp4_weights_to_e4m3``)."""
+    _need(X, _BF16, "X")
+    M, K = X.shape
+    N = _fp8_operands(Wq8, sw, K, X.device)
+    Y = _output(out, M, N, X.device, "out")
+    lib = load_library()
+    need = lib.wq_gemm_w8a8_fp8_workspace_bytes(M, K)
+    ws = workspace if workspace is not None else Workspace(X.device).get(need)
+    _check(lib.wq_gemm_w4a4_mxfp4(_ptr(X), M, K, N, _ptr(Wq8), _ptr(sw), _ptr(Y), _ptr(ws), ws.numel(),
+                                  _stream(stream, X.device)), "wq_gemm_w4a4_mxfp4")
     return Y

@@ -496,6 +496,46 @@ wq_status wq_gemm_w8a8_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t N, c
   return from_cuda(wq::launch_gemm_fp8(Xq, s_x, M, K, N, Wq, s_w, Y, s));
 }
 
+// ------------------------------------------------------------------ W4A4 MXFP4
+wq_status wq_mxfp4_weights_to_e4m3(const int32_t* Wq, const uint8_t* scales, int64_t N, int64_t K, uint8_t* Wq8,
+                                   float* s_w, void* stream) {
+  if (!Wq || !scales || !Wq8 || !s_w) return WQ_ERR_NULL;
+  if (N < 1 || K < 32 || K % 32 != 0 || N > (1LL << 30) || K > (1LL << 30)) return WQ_ERR_SHAPE;
+  if (!aligned16(Wq) || !aligned16(Wq8) || (reinterpret_cast<uintptr_t>(s_w) & 3u)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_mx_weights_to_e4m3(Wq, scales, N, K, Wq8, s_w, static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_quantize_w4a4_activations(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq8, float* s_x,
+                                       void* stream) {
+  if (!X || !Xq8 || !s_x) return WQ_ERR_NULL;
+  if (M < 1 || K < 32 || K % 32 != 0 || K > 131072 || M > (1LL << 30)) return WQ_ERR_SHAPE;
+  if (!aligned16(X) || !aligned16(Xq8) || (reinterpret_cast<uintptr_t>(s_x) & 3u)) return WQ_ERR_ALIGN;
+  wq_status st = check_device_cached();
+  if (st != WQ_OK) return st;
+  return from_cuda(wq::launch_quant_w4a4_act(X, M, K, Xq8, s_x, static_cast<cudaStream_t>(stream)));
+}
+
+wq_status wq_gemm_w4a4_mxfp4(const uint16_t* X, int64_t M, int64_t K, int64_t N, const uint8_t* Wq8, const float* s_w,
+                             uint16_t* Y, void* workspace, size_t ws_bytes, void* stream) {
+  if (!X) return WQ_ERR_NULL;
+  wq_status st = check_fp8_gemm(M, K, N, Wq8, s_w, Y);
+  if (st != WQ_OK) return st;
+  if (K % 32 != 0 || K > 131072) return WQ_ERR_SHAPE;
+  if (!aligned16(X)) return WQ_ERR_ALIGN;
+  if (!workspace || ws_bytes < wq_gemm_w8a8_fp8_workspace_bytes(M, K)) return WQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return WQ_ERR_ALIGN;
+  st = check_device_cached();
+  if (st != WQ_OK) return st;
+  uint8_t* Xq8 = static_cast<uint8_t*>(workspace);
+  float* s_x = reinterpret_cast<float*>(Xq8 + round_up256(static_cast<size_t>(M) * static_cast<size_t>(K)));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wq::launch_quant_w4a4_act(X, M, K, Xq8, s_x, s);
+  if (e != cudaSuccess) return WQ_ERR_CUDA;
+  return from_cuda(wq::launch_gemm_fp8(Xq8, s_x, M, K, N, Wq8, s_w, Y, s));
+}
+
 wq_status wq_read_error_flags(uint32_t* out) {
   if (!out) return WQ_ERR_NULL;
   if (cudaDeviceSynchronize() != cudaSuccess) return WQ_ERR_CUDA;

@@ -113,6 +113,13 @@ cudaError_t launch_quant_fp8_rows(bool bf16_in, const void* in, int64_t R, int64
 cudaError_t launch_gemm_fp8(const uint8_t* Xq, const float* sx, int64_t M, int64_t K, int64_t N, const uint8_t* Wq,
                             const float* sw, uint16_t* Y, cudaStream_t stream);
 uint32_t fp8_read_and_clear_error();
+
+// W4A4 MXFP4 on the FP8 path (w4a4.cu): MXFP4 weights re-encoded as E4M3 against a per-row
+// power of two; bf16 activations quantized to MXFP4 and re-encoded the same way.
+cudaError_t launch_mx_weights_to_e4m3(const int32_t* Wq, const uint8_t* scales, int64_t N, int64_t K, uint8_t* W8,
+                                      float* sw, cudaStream_t stream);
+cudaError_t launch_quant_w4a4_act(const uint16_t* X, int64_t M, int64_t K, uint8_t* X8, float* sx,
+                                  cudaStream_t stream);
 cudaError_t run_selftest_wait(uint64_t limit_ns, uint32_t* timed_out_host, cudaStream_t stream);
 
 // layout.cu -- row re-layout of the stacked gate+up weight

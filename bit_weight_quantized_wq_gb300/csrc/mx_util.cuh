@@ -1,0 +1,36 @@
+// MXFP4 quantization helpers shared by the weight quantizer (quantize.cu) and the W4A4
+// activation quantizer (w4a4.cu): the block's E8M0 exponent from the IEEE fields of
+// amax / 6 and the E2M1 magnitude code by the grid's decision boundaries.
+#pragma once
+
+#include "common.cuh"
+
+namespace wq {
+
+// ceil(log2 r) for a positive finite float, exact, from the IEEE fields.
+__device__ __forceinline__ int ceil_log2_pos(float r) {
+  const uint32_t b = __float_as_uint(r);
+  const int ex = static_cast<int>((b >> 23) & 0xffu);
+  const uint32_t man = b & 0x7fffffu;
+  if (ex != 0) return (ex - 127) + (man != 0u ? 1 : 0);
+  // subnormal: r = man * 2^-149
+  const int p = 31 - __clz(static_cast<int>(man));       // highest set bit
+  return (p - 149) + ((man & (man - 1u)) != 0u ? 1 : 0);
+}
+
+// 2^f for f in [-127, 127] as a float (2^-127 is subnormal).
+__device__ __forceinline__ float exp2_int(int f) {
+  return f >= -126 ? __uint_as_float(static_cast<uint32_t>(f + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// Magnitude code of |v|: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
+// saturating at 6.  Each comparison is one decision boundary (midpoint) of the grid; the
+// strict/non-strict choice at a midpoint sends the tie to the even code.
+__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
+  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
+         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
+         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
+         static_cast<uint32_t>(a > 5.0f);
+}
+
+}  // namespace wq

@@ -6,6 +6,7 @@
 // division/subtraction, no contraction) so that every code, scale and zero point is
 // reproducible bit for bit.
 #include "internal.h"
+#include "mx_util.cuh"
 
 namespace wq {
 
@@ -64,32 +65,6 @@ __global__ void __launch_bounds__(256) k_quant_int4_g128(const float* __restrict
 // ---------------------------------------------------------------------------------------
 // MXFP4, block of 32 along K.  4 lanes per block, 8 consecutive floats per lane.
 // ---------------------------------------------------------------------------------------
-
-// ceil(log2 r) for a positive finite float, exact, from the IEEE fields.
-__device__ __forceinline__ int ceil_log2_pos(float r) {
-  const uint32_t b = __float_as_uint(r);
-  const int ex = static_cast<int>((b >> 23) & 0xffu);
-  const uint32_t man = b & 0x7fffffu;
-  if (ex != 0) return (ex - 127) + (man != 0u ? 1 : 0);
-  // subnormal: r = man * 2^-149
-  const int p = 31 - __clz(static_cast<int>(man));       // highest set bit
-  return (p - 149) + ((man & (man - 1u)) != 0u ? 1 : 0);
-}
-
-// 2^f for f in [-127, 127] as a float (2^-127 is subnormal).
-__device__ __forceinline__ float exp2_int(int f) {
-  return f >= -126 ? __uint_as_float(static_cast<uint32_t>(f + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
-// Magnitude code of |v|: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
-// saturating at 6.  Each comparison is one decision boundary (midpoint) of the grid; the
-// strict/non-strict choice at a midpoint sends the tie to the even code.
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
-         static_cast<uint32_t>(a > 5.0f);
-}
 
 __global__ void __launch_bounds__(256) k_quant_mxfp4(const float* __restrict__ W, int64_t blocks,
                                                      uint32_t* __restrict__ Wq,

@@ -404,6 +404,33 @@ size_t wq_gemm_w8a8_fp8_workspace_bytes(int64_t M, int64_t K);
 wq_status wq_gemm_w8a8_fp8(const uint16_t* X, int64_t M, int64_t K, int64_t N, const uint8_t* Wq, const float* s_w,
                            uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * W4A4 in MXFP4 -- 第 6 课：量化源码走读 (量化范式与精度矩阵: NVFP4/MXFP4 micro-scaling quantizes
+ * weights and activations to 4 bits with one shared scale per small block, the activations on
+ * the fly); the block format of 大模型量化推理引擎全景大复盘 (里程碑六 / 方程 3).  Executed on the
+ * FP8 tensor-core path (wq_gemm_fp8): every MXFP4 value E2M1(c) 2^e is the E4M3 value
+ * E2M1(c) 2^(e - E) times the row's power of two 2^E, exactly for every block within 14
+ * binades of the row's largest block (E = that block's exponent - 6); a block further below
+ * is rounded to E4M3 (zero beyond 2^-13 of the largest).
+ *   wq_mxfp4_weights_to_e4m3:     MXFP4 weights as wq_quantize_mxfp4 writes them (Wq [N, K/8]
+ *                                 int32, scales [N, K/32] E8M0) -> Wq8 [N, K] E4M3 codes and
+ *                                 s_w [N] float32 powers of two (once per layer).
+ *   wq_quantize_w4a4_activations: X [M, K] bf16 bits quantized per token row by exactly the
+ *                                 rules of wq_quantize_mxfp4, then re-encoded the same way ->
+ *                                 Xq8 [M, K], s_x [M].
+ *   wq_gemm_w4a4_mxfp4:           the layer from bf16 activations: the activation quantizer into
+ *                                 the workspace (wq_gemm_w8a8_fp8_workspace_bytes(M, K) bytes),
+ *                                 then wq_gemm_fp8 with the powers of two as the row scales.
+ * Errors: WQ_ERR_NULL; WQ_ERR_SHAPE unless K % 32 == 0 (activations: K <= 131072); WQ_ERR_ALIGN;
+ *         WQ_ERR_WORKSPACE; WQ_ERR_UNSUPPORTED_ARCH; WQ_ERR_CUDA.
+ */
+wq_status wq_mxfp4_weights_to_e4m3(const int32_t* Wq, const uint8_t* scales, int64_t N, int64_t K, uint8_t* Wq8,
+                                   float* s_w, void* stream);
+wq_status wq_quantize_w4a4_activations(const uint16_t* X, int64_t M, int64_t K, uint8_t* Xq8, float* s_x,
+                                       void* stream);
+wq_status wq_gemm_w4a4_mxfp4(const uint16_t* X, int64_t M, int64_t K, int64_t N, const uint8_t* Wq8, const float* s_w,
+                             uint16_t* Y, void* workspace, size_t ws_bytes, void* stream);
+
 /* WQ_OK when the current device is a GB300-class part (compute capability 10.3). */
 wq_status wq_check_device(void);
 

@@ -163,3 +163,13 @@ def test_validation_errors_fp8(lib):
     assert lib.wq_gemm_w8a8_fp8_workspace_bytes(0, 1024) == 0
     f = lambda ws=FAKE, wsb=1 << 30, K=64: lib.wq_gemm_w8a8_fp8(FAKE, 4, K, 8, FAKE, FAKE, FAKE, ws, wsb, None)
     assert f(ws=None) == 4 and f(wsb=16) == 4 and f(K=40) == 2
+
+
+def test_validation_errors_w4a4(lib):
+    assert lib.wq_mxfp4_weights_to_e4m3(None, FAKE, 4, 64, FAKE, FAKE, None) == 1
+    assert lib.wq_mxfp4_weights_to_e4m3(FAKE, FAKE, 4, 48, FAKE, FAKE, None) == 2
+    assert lib.wq_mxfp4_weights_to_e4m3(ODD, FAKE, 4, 64, FAKE, FAKE, None) == 3
+    assert lib.wq_quantize_w4a4_activations(FAKE, 4, 48, FAKE, FAKE, None) == 2
+    assert lib.wq_quantize_w4a4_activations(FAKE, 4, 131104, FAKE, FAKE, None) == 2
+    f = lambda ws=FAKE, wsb=1 << 30, K=64: lib.wq_gemm_w4a4_mxfp4(FAKE, 4, K, 8, FAKE, FAKE, FAKE, ws, wsb, None)
+    assert f(ws=None) == 4 and f(K=48) == 2
