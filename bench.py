@@ -530,6 +530,48 @@ def secondary(args, dev, stream, layers, X, hbm_peak, bf16_peak, bf16_sus):
     del pre
     torch.cuda.empty_cache()
 
+    # W8A8 FP8 E4M3 and W4A4 MXFP4 (on the FP8 tensor-core path) on the same Qwen2.5-72B
+    # shapes, M = 2048 and 8192: the GEMM alone and the layer from bf16 activations
+    # (per-token quantization + GEMM).  Peak: the FP8 dense rate, 2x the measured bf16 burst
+    # (the nominal fp8/bf16 ratio 4.5 / 2.25).
+    fp8_peak = 2.0 * bf16_peak
+    for key, wfmt in (("fp8_prefill", "fp8"), ("w4a4_prefill", "w4a4")):
+        res = {}
+        for Mp in (PREFILL_M, PREFILL_M_LARGE):
+            per_layer = []
+            for i, (K, N) in enumerate(PREFILL_SHAPES):
+                W = torch.from_numpy(inputs.weights(3000 + i, N, K, 0.015)).to(dev)
+                if wfmt == "fp8":
+                    Wq8, sw = binding.quantize_fp8_weights(W)
+                else:
+                    Wq8, sw = binding.mxfp4_weights_to_e4m3(*binding.quantize_mxfp4(W))
+                del W
+                Xp = torch.from_numpy(inputs.activations(3100 + K, Mp, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+                Yp = torch.empty((Mp, N), dtype=torch.bfloat16, device=dev)
+                wsf = binding.Workspace(dev).get(binding.load_library().wq_gemm_w8a8_fp8_workspace_bytes(Mp, K))
+                qfn = binding.quantize_fp8_activations if wfmt == "fp8" else binding.quantize_w4a4_activations
+                Xq, sx = qfn(Xp)
+                lay = binding.gemm_w8a8_fp8 if wfmt == "fp8" else binding.gemm_w4a4_mxfp4
+                nrep = max(3, reps // (5 if Mp == PREFILL_M else 20))
+                ms_g = _graph_time(lambda: binding.gemm_fp8(Xq, sx, Wq8, sw, out=Yp), stream, dev, nrep)
+                ms_l = _graph_time(lambda: lay(Xp, Wq8, sw, out=Yp, workspace=wsf), stream, dev, nrep)
+                fl = 2.0 * Mp * N * K
+                per_layer.append({"K": K, "N": N, "M": Mp, "gemm_us": ms_g * 1e3, "gemm_tflops": fl / (ms_g * 1e-3) / 1e12,
+                                  "layer_us": ms_l * 1e3, "layer_tflops": fl / (ms_l * 1e-3) / 1e12})
+                del Wq8, sw, Xp, Yp, Xq, sx
+                torch.cuda.empty_cache()
+            tot_fl = sum(2.0 * Mp * N * K for K, N in PREFILL_SHAPES)
+            tg = tot_fl / (sum(q["gemm_us"] for q in per_layer) * 1e-6) / 1e12
+            tl = tot_fl / (sum(q["layer_us"] for q in per_layer) * 1e-6) / 1e12
+            res["m%d" % Mp] = {"gemm_tflops": tg, "layer_tflops": tl, "layers": per_layer,
+                               "roofline": {"bound": "tensor", "achieved": tg, "peak": fp8_peak, "unit": "TFLOP/s",
+                                            "frac": tg / fp8_peak,
+                                            "note": "tcgen05 kind::f8f6f4 GEMM; peak = 2 x measured bf16 burst"}}
+        res["workload"] = ("W8A8 FP8 E4M3 (per-channel weight, per-token activation scales)" if wfmt == "fp8" else
+                           "W4A4 MXFP4 (weights and per-token activations in MXFP4, re-encoded exactly to E4M3)") + \
+            ", Qwen2.5-72B shapes, M = 2048 and 8192"
+        out[key] = res
+
     # MXFP4 decode (same four shapes, M in {1, 16})
     mx_layers = []
     for i, (K, N) in enumerate(DECODE_SHAPES):
@@ -769,6 +811,7 @@ def run_ncu_case(args):
              SwiGLU epilogue, M = 1, INT4.
     quant:   INT4 quantize of the (4096, 28672) weights (470 MB fp32).
     gptq:    the GPTQ sweep, N = K = 4096, seeded stand-in inverse-Hessian factor.
+    fp8:     the FP8 E4M3 GEMM alone on the (8192, 8192) prefill layer, M = 2048.
     awq:     the AWQ search + packing, N = K = 4096, 128 calibration samples.
     """
     import numpy as np
@@ -800,6 +843,20 @@ def run_ncu_case(args):
                     n += 1
         torch.cuda.synchronize()
         print(json.dumps({"ncu_case": case, "launches": n, "launches_per_step": len(DECODE_M) * len(DECODE_SHAPES)}))
+        return 0
+    if case == "fp8":
+        # the FP8 GEMM alone on the (8192, 8192) prefill layer at M = 2048
+        K, N, M = 8192, 8192, 2048
+        W = torch.from_numpy(inputs.weights(1002, N, K, 0.015)).to(dev)
+        Wq8, sw = binding.quantize_fp8_weights(W)
+        del W
+        X = torch.from_numpy(inputs.activations(7, M, K)[0].view(np.int16)).to(dev).view(torch.bfloat16)
+        Xq, sx = binding.quantize_fp8_activations(X)
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup + args.steps):
+            binding.gemm_fp8(Xq, sx, Wq8, sw, out=Y)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_case": case, "launches": args.warmup + args.steps, "K": K, "N": N, "M": M}))
         return 0
     if case in ("gptq", "awq"):
         W = torch.from_numpy(inputs.weights(5100, 4096, 4096, 0.02)).to(dev)
@@ -856,7 +913,7 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-sample", type=float, default=None, help=argparse.SUPPRESS)
-    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "swiglu_decode", "quant", "gptq", "awq"],
+    ap.add_argument("--ncu-case", default=None, choices=["decode", "decode_step", "prefill", "mxfp4", "swiglu_decode", "quant", "gptq", "awq", "fp8"],
                     help="run a few plain launches of one kernel (for ncu captures) instead of the bench")
     args = ap.parse_args()
     if args.cpu_sample is not None:
