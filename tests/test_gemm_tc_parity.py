@@ -186,3 +186,21 @@ def test_gemm_tc_mxfp4_crossover_shape(B, M):
     Y = y_to_host(_run(B.gemm_tc_w4a16, "mxfp4", xb, pk))
     ref = linear.linear_rows("mxfp4", xf, pk[0], pk[1], None, rows)
     assert_close(Y[:, rows], ref, "mxfp4 M=%d" % M)
+
+
+# Wide layers with short K: more tiles than SMs (a partial last wave), ragged M, N and K
+# tails, and an odd number of weight tiles; the result is also the same on a second run.
+WIDE_CASES = [("int4_g128", 256, 256, 10240), ("int4_g128", 300, 384, 10152), ("mxfp4", 256, 352, 10240),
+            ("mxfp4", 1000, 224, 3968)]
+
+
+@pytest.mark.parametrize("fmt,M,K,N", WIDE_CASES)
+def test_gemm_tc_wide_short_k(B, fmt, M, K, N):
+    W = inputs.weights(M + K + N, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M * 5 + K, M, K)
+    y1 = y_to_host(_run(B.gemm_tc_w4a16, fmt, xb, pk))
+    assert_close(y1, linear.linear_w4a16(fmt, xf, *pk), "wide %s M=%d K=%d N=%d" % (fmt, M, K, N))
+    y2 = y_to_host(_run(B.gemm_tc_w4a16, fmt, xb, pk))
+    assert np.array_equal(y1, y2), "result differs between runs"
+    assert B.read_error_flags() == 0

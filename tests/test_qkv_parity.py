@@ -115,3 +115,14 @@ def test_qkv_rejects_bad_arguments(B):
     with pytest.raises(ValueError):
         B.gemm_w4a16_qkv("int4_g128", X, *pk, Nq=256, Nkv=64,
                          out=(torch.empty((2, 256), dtype=torch.bfloat16, device="cuda"),) * 2)
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_qkv_tensor_core_wide_short_k(B, fmt):
+    # M = 256, Nq + 2 Nkv = 10240 rows (more tiles than SMs), short K = 256
+    M, Nq, Nkv, K = 256, 8192, 1024, 256
+    N = Nq + 2 * Nkv
+    pk = _pack(fmt, inputs.weights(777, N, K, 0.05))
+    xb, xf = inputs.activations(778, M, K)
+    got = _qkv(B, fmt, xb, pk, Nq, Nkv, path="tc")
+    _check(got, linear.linear_w4a16(fmt, xf, *pk), Nq, Nkv, "wide QKV %s" % fmt)

@@ -222,3 +222,15 @@ def test_swiglu_paths_agree_where_operands_are_exact(B):
     assert_close(y_tc, y_dec, "tc vs decode", allow)
     beyond_plain = np.abs(y_tc - ref) > 1e-2 * (1 + np.abs(ref))
     assert beyond_plain.mean() <= 1e-3, "%d of %d outputs need the allowance" % (beyond_plain.sum(), ref.size)
+
+
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+def test_swiglu_tc_wide_short_k(B, fmt):
+    # M = 256 with 2F = 10240 fused gate + up rows (more tiles than SMs), short K = 256
+    M, F, K = 256, 5120, 256
+    pk = _stacked(fmt, F, K, 4242)
+    xb, xf = inputs.activations(4243, M, K)
+    Y = _run(B.gemm_tc_w4a16_swiglu, fmt, xb, pk, F)
+    extra = _fp16_operand_allowance(xf, pk, F) if fmt == "int4_g128" else None
+    assert_close(y_to_host(Y), _ref(fmt, xf, pk), "wide SwiGLU %s" % fmt, extra)
+    assert B.read_error_flags() == 0
