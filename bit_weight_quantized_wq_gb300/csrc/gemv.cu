@@ -148,7 +148,11 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 ld_cg_f32x4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
 // One share of the reduction of a shared band by its reducer CTA: for the float4 slots idx =
@@ -977,7 +981,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        fence_acq_rel_gpu();             // the posted partial sums are visible from here on
+        // One acquire load of the final count (it reads the last of the contributors' release
+        // increments, so it synchronizes with all of them): the posted partial sums are
+        // visible from here on, at the cost of a load rather than a GPU-scope fence.
+        (void)ld_acquire_gpu(p.cnt + red_band);
         if (ok) p.cnt[red_band] = 0u;    // ready for the next call (its contributors post after this grid ends)
         sm.reduce_ok = ok;
       }
