@@ -366,11 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sm.last) atomicExch(c, 0u);   // ready for the next call
         }
         epi_bar();
+        // The counter update's acquire (thread 64) and the barrier after it order the other
+        // parts' stores before this CTA's loads of them; no further fence is needed.
         write_y = sm.last != 0;
-        if (write_y) {
-          __threadfence();
-          parts = p.part + slot * (BN * BMT) + static_cast<long long>(r) * BMT;
-        }
+        if (write_y) parts = p.part + slot * (BN * BMT) + static_cast<long long>(r) * BMT;
       }
 #pragma unroll 1
       for (int c = 32 * set; c < BMT && write_y; c += 32 * kDequantSets) {
