@@ -33,4 +33,14 @@ __device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
          static_cast<uint32_t>(a > 5.0f);
 }
 
+// Two floats to a byte of E2M1 codes (hi in bits 4-7, lo in bits 0-3): round to nearest, ties
+// to the even code, saturating at +-6 (cvt.rn.satfinite.e2m1x2.f32).
+__device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
+  uint16_t d;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(d)
+      : "f"(hi), "f"(lo));
+  return d;
+}
+
 }  // namespace wq

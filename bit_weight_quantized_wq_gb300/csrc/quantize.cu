@@ -43,10 +43,18 @@ __global__ void __launch_bounds__(256) k_quant_int4_g128(const float* __restrict
   float s, zf;
   const __half s16 = int4_group_params(lo, hi, s, zf);
 
+  // rint(x / s) with the IEEE quotient's rounding, from x times the correctly rounded 1/s:
+  // that product is within 1.5 ulp of the quotient (|x / s| <= 16, ulp <= 2^-20), so both
+  // round to the same integer unless the quotient is within 2^-17 of a rounding boundary
+  // n + 1/2; there (rarely) the exact division decides.
+  const float rs = __frcp_rn(s);
   uint32_t w0 = 0u, w1 = 0u;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float q = __fadd_rn(rintf(__fdiv_rn(x[i], s)), zf);
+    const float qa = __fmul_rn(x[i], rs);
+    const float fr = qa - floorf(qa);
+    const float qi = fabsf(fr - 0.5f) < 0x1p-17f ? rintf(__fdiv_rn(x[i], s)) : rintf(qa);
+    float q = __fadd_rn(qi, zf);
     q = fminf(fmaxf(q, 0.f), 15.f);
     const uint32_t c = static_cast<uint32_t>(q);
     if (i < 8) w0 |= c << (4 * i);
@@ -92,14 +100,14 @@ __global__ void __launch_bounds__(256) k_quant_mxfp4(const float* __restrict__ W
   e = max(-127, min(127, e));
   const float inv = exp2_int(-e);
 
+  // E2M1 by the hardware conversion: round to nearest, ties to the even code, saturating at
+  // +-6, the sign kept (also on a zero) -- the grid rule of e2m1_mag_code, two values per
+  // instruction.
   uint32_t word = 0u;
   if (amax != 0.f) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float v = __fmul_rn(x[i], inv);
-      const uint32_t sign = __float_as_uint(x[i]) >> 31;
-      word |= ((sign << 3) | e2m1_mag_code(fabsf(v))) << (4 * i);
-    }
+    for (int i = 0; i < 8; i += 2)
+      word |= e2m1x2_rn(__fmul_rn(x[i + 1], inv), __fmul_rn(x[i], inv)) << (4 * i);
   }
   if (active) {
     Wq[b * 4 + sub] = word;
