@@ -46,6 +46,24 @@ __device__ __forceinline__ float pow2_any(int e) {
   return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(1u << (e + 149));
 }
 
+// E2M1 code pair -> fp16 pair (exact), fp16 pair times fp16 pair, fp16 pair -> E4M3 codes.
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
+  uint32_t d;
+  const unsigned short h = static_cast<unsigned short>(byte);
+  asm("{\n\t.reg .b8 t, u;\n\tmov.b16 {t, u}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(d) : "h"(h));
+  return d;
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2_e4m3x2(uint32_t h2) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(h2));
+  return d;
+}
+
 __device__ __forceinline__ int block_max_int(int v, int* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -134,21 +152,29 @@ __global__ void __launch_bounds__(kThreads) k_quant_w4a4_act(const uint16_t* __r
     const int e = be[b];
     const uint4* src = reinterpret_cast<const uint4*>(xrow + 32 * b);
     const float inv = exp2_int(-(e == -128 ? 0 : e));
+    // 2^(e - E) as an fp16 pair (d >= kMinShift = -20: at least 2^-20, an exact fp16); an
+    // E2M1 value times it has at most two significant bits and stays >= 2^-21, so the fp16
+    // product is exact and its E4M3 rounding is that of the value itself
+    int d = e - E;
+    if (d < kMinShift) d = kMinShift;
+    const uint32_t f1 = __half_as_ushort(__float2half_rn(pow2_small(d)));
+    const uint32_t f2 = f1 | (f1 << 16);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {               // 8 elements per 16-byte load
       const uint4 v = __ldg(src + i);
       const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      uint32_t word = 0u;
+      uint32_t c[4] = {0u, 0u, 0u, 0u};         // a zero block (e = -128) is all +0 codes
       if (e != -128) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float x0 = __uint_as_float(w4[q] << 16), x1 = __uint_as_float(w4[q] & 0xffff0000u);
-          const uint32_t c0 = ((__float_as_uint(x0) >> 31) << 3) | e2m1_mag_code(fabsf(__fmul_rn(x0, inv)));
-          const uint32_t c1 = ((__float_as_uint(x1) >> 31) << 3) | e2m1_mag_code(fabsf(__fmul_rn(x1, inv)));
-          word |= (c0 | (c1 << 4)) << (8 * q);
+          // E2M1 of x 2^-e: round to nearest, ties to the even code, saturating at +-6 (the
+          // rule of e2m1_mag_code), sign kept; then re-encoded against the row's 2^E
+          const uint32_t codes = e2m1x2_rn(__fmul_rn(x1, inv), __fmul_rn(x0, inv));
+          c[q] = f16x2_e4m3x2(hmul2_bits(e2m1x2_f16x2(codes), f2));
         }
       }
-      *reinterpret_cast<uint2*>(orow + 32 * b + 8 * i) = reencode8(word, e, E, e == -128);
+      *reinterpret_cast<uint2*>(orow + 32 * b + 8 * i) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
     }
   }
   if (threadIdx.x == 0) sx[m] = pow2_any(E);
