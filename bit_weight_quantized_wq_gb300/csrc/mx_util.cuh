@@ -1,6 +1,6 @@
 // MXFP4 quantization helpers shared by the weight quantizer (quantize.cu) and the W4A4
 // activation quantizer (w4a4.cu): the block's E8M0 exponent from the IEEE fields of
-// amax / 6 and the E2M1 magnitude code by the grid's decision boundaries.
+// amax / 6 and the E2M1 codes by round-to-nearest-even onto the grid.
 #pragma once
 
 #include "common.cuh"
@@ -23,18 +23,9 @@ __device__ __forceinline__ float exp2_int(int f) {
   return f >= -126 ? __uint_as_float(static_cast<uint32_t>(f + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// Magnitude code of |v|: nearest of {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
-// saturating at 6.  Each comparison is one decision boundary (midpoint) of the grid; the
-// strict/non-strict choice at a midpoint sends the tie to the even code.
-__device__ __forceinline__ uint32_t e2m1_mag_code(float a) {
-  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) +
-         static_cast<uint32_t>(a > 5.0f);
-}
-
-// Two floats to a byte of E2M1 codes (hi in bits 4-7, lo in bits 0-3): round to nearest, ties
-// to the even code, saturating at +-6 (cvt.rn.satfinite.e2m1x2.f32).
+// Two floats to a byte of E2M1 codes (hi in bits 4-7, lo in bits 0-3), sign kept (also on a
+// zero): the nearest of the grid {0, .5, 1, 1.5, 2, 3, 4, 6} in magnitude, a tie (0.25, 0.75,
+// 1.25, 1.75, 2.5, 3.5, 5) to the even code, saturating at +-6 (cvt.rn.satfinite.e2m1x2.f32).
 __device__ __forceinline__ uint32_t e2m1x2_rn(float hi, float lo) {
   uint16_t d;
   asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"

@@ -100,9 +100,8 @@ __global__ void __launch_bounds__(256) k_quant_mxfp4(const float* __restrict__ W
   e = max(-127, min(127, e));
   const float inv = exp2_int(-e);
 
-  // E2M1 by the hardware conversion: round to nearest, ties to the even code, saturating at
-  // +-6, the sign kept (also on a zero) -- the grid rule of e2m1_mag_code, two values per
-  // instruction.
+  // E2M1 by the hardware conversion (e2m1x2_rn): round to nearest, ties to the even code,
+  // saturating at +-6, the sign kept (also on a zero); two values per instruction.
   uint32_t word = 0u;
   if (amax != 0.f) {
 #pragma unroll

@@ -168,8 +168,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_w4a4_act(const uint16_t* __r
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float x0 = __uint_as_float(w4[q] << 16), x1 = __uint_as_float(w4[q] & 0xffff0000u);
-          // E2M1 of x 2^-e: round to nearest, ties to the even code, saturating at +-6 (the
-          // rule of e2m1_mag_code), sign kept; then re-encoded against the row's 2^E
+          // E2M1 of x 2^-e: round to nearest, ties to the even code, saturating at +-6, sign
+          // kept; then re-encoded against the row's 2^E
           const uint32_t codes = e2m1x2_rn(__fmul_rn(x1, inv), __fmul_rn(x0, inv));
           c[q] = f16x2_e4m3x2(hmul2_bits(e2m1x2_f16x2(codes), f2));
         }
