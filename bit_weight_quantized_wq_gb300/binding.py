@@ -293,13 +293,15 @@ def _fn(cname: str):
 def _inputs(f, X, Wq, scales, zeros):
     """The checks every layer call makes on its inputs before their pointers reach the library,
     which sees only raw addresses and sizes: dtypes, devices, contiguity, and the shapes of Wq,
-    scales and zeros against X.  Returns (M, K, N)."""
+    scales and zeros against X.  Returns (M, K, N, CUDA device index).  Device checks use
+    ``get_device()`` (an int, -1 on the CPU), cheaper per call than comparing device objects."""
     int4 = f == FMT_INT4_G128
     if (X.dtype is not _BF16 or Wq.dtype is not _I32 or scales.dtype is not (_F16 if int4 else _U8)
             or (zeros is not None and (not int4 or zeros.dtype is not _F16)) or (int4 and zeros is None)):
         _linear_explain(f, X, Wq, scales, zeros)
-    if not (X.is_cuda and Wq.is_cuda and scales.is_cuda and X.is_contiguous() and Wq.is_contiguous()
-            and scales.is_contiguous() and (zeros is None or (zeros.is_cuda and zeros.is_contiguous()))):
+    d = X.get_device()
+    if d < 0 or not (X.is_contiguous() and Wq.is_contiguous() and scales.is_contiguous()
+                     and (zeros is None or zeros.is_contiguous())):
         _linear_explain(f, X, Wq, scales, zeros)
     if X.dim() != 2 or Wq.dim() != 2:
         raise ValueError("X must be [M, K] and Wq [N, K/8]")
@@ -310,26 +312,27 @@ def _inputs(f, X, Wq, scales, zeros):
     meta = (N, K // 128) if int4 else (N, K // 32)
     if scales.shape != meta or (zeros is not None and zeros.shape != meta):
         raise ValueError("scales%s must be [N, K/%d]" % (" and zeros" if int4 else "", 128 if int4 else 32))
-    dev = X.device
-    if Wq.device != dev or scales.device != dev or (zeros is not None and zeros.device != dev):
+    if Wq.get_device() != d or scales.get_device() != d or (zeros is not None and zeros.get_device() != d):
+        if not (Wq.is_cuda and scales.is_cuda and (zeros is None or zeros.is_cuda)):
+            _linear_explain(f, X, Wq, scales, zeros)
         raise ValueError("X, Wq, scales and zeros must be on the same device")
-    return M, K, N
+    return M, K, N, d
 
 
-def _output(out, M, ncol, dev, name="out"):
-    """A bf16 [M, ncol] output on ``dev``: ``out`` checked, or a new tensor when None."""
+def _output(out, M, ncol, d, name="out"):
+    """A bf16 [M, ncol] output on CUDA device ``d``: ``out`` checked, or a new tensor when None."""
     if out is None:
-        return torch.empty((M, ncol), dtype=_BF16, device=dev)
-    if out.dtype is not _BF16 or not out.is_cuda or not out.is_contiguous():
+        return torch.empty((M, ncol), dtype=_BF16, device=torch.device("cuda", d))
+    if out.dtype is not _BF16 or not out.is_contiguous() or out.get_device() < 0:
         _need(out, _BF16, name)
-    if out.shape != (M, ncol) or out.device != dev:
+    if out.shape != (M, ncol) or out.get_device() != d:
         raise ValueError("%s must be [%d, %d] on X's device" % (name, M, ncol))
     return out
 
 
 def _prepare(f, X, Wq, scales, zeros, out, swiglu):
-    M, K, N = _inputs(f, X, Wq, scales, zeros)
-    return M, K, N, _output(out, M, N // 2 if swiglu else N, X.device)
+    M, K, N, d = _inputs(f, X, Wq, scales, zeros)
+    return M, K, N, _output(out, M, N // 2 if swiglu else N, d)
 
 
 def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swiglu=False):
@@ -338,16 +341,22 @@ def _linear(cname: str, fmt, X, Wq, scales, zeros, out, workspace, stream, swigl
     # shapes are checked here (the library sees raw pointers); alignment, size limits and the
     # workspace size in C.
     f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
-    M, K, N, out = _prepare(f, X, Wq, scales, zeros, out, swiglu)
-    dev = X.device
+    M, K, N, d = _inputs(f, X, Wq, scales, zeros)
+    out = _output(out, M, N // 2 if swiglu else N, d)
     # a caller's workspace is checked by the library itself (WQ_ERR_WORKSPACE when too small)
-    if workspace is not None and (not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous()):
+    if workspace is not None and (workspace.get_device() != d or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor on X's device")
-    ws = workspace if workspace is not None else _workspace_for(dev, gemm_workspace_bytes(f, M, K, N), None)
+    ws = workspace if workspace is not None else _workspace_for(X.device, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    if stream is not None:
+        sh = stream.cuda_stream
+    elif _raw_current_stream is not None:
+        sh = _raw_current_stream(d)
+    else:
+        sh = torch.cuda.current_stream(X.device).cuda_stream
     st = _fn(cname)(f, X.data_ptr(), M, K, N // 2 if swiglu else N, Wq.data_ptr(), scales.data_ptr(),
                     None if zeros is None else zeros.data_ptr(), out.data_ptr(),
-                    None if ws is None else ws.data_ptr(), ws_bytes, _stream(stream, dev))
+                    None if ws is None else ws.data_ptr(), ws_bytes, sh)
     if st:
         _check(st, cname)
     return out
@@ -437,15 +446,15 @@ def gemm_w4a16_qkv(fmt, X, Wq, scales, zeros=None, Nq=None, Nkv=None, out=None, 
     stacked packed weight [W_Q; W_K; W_V] of Nq + 2 Nkv rows; dispatches like ``gemm_w4a16``.
     ``out`` may be a tuple of three preallocated bf16 tensors."""
     f = fmt if fmt.__class__ is int else _FMT_NAMES[fmt]
-    M, K, N = _inputs(f, X, Wq, scales, zeros)
+    M, K, N, d = _inputs(f, X, Wq, scales, zeros)
     if Nq is None or Nkv is None or Nq < 1 or Nkv < 1 or Nq + 2 * Nkv != N:
         raise ValueError("Nq, Nkv >= 1 with Nq + 2 Nkv == Wq.shape[0] required")
     dev = X.device
     if out is not None and len(out) != 3:
         raise ValueError("out must be three tensors (Q, K, V)")
-    out = tuple(_output(None if out is None else out[i], M, n, dev, "out " + nm)
+    out = tuple(_output(None if out is None else out[i], M, n, d, "out " + nm)
                 for i, (n, nm) in enumerate(((Nq, "Q"), (Nkv, "K"), (Nkv, "V"))))
-    if workspace is not None and (not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous()):
+    if workspace is not None and (workspace.get_device() != d or not workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor on X's device")
     ws = workspace if workspace is not None else _workspace_for(dev, gemm_workspace_bytes(f, M, K, N), None)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
@@ -526,7 +535,7 @@ def gemm_fp8(Xq, sx, Wq, sw, out=None, stream=None):
     if sx.shape != (M,) or sx.device != Xq.device:
         raise ValueError("s_x must be [M] on Xq's device")
     N = _fp8_operands(Wq, sw, K, Xq.device)
-    Y = _output(out, M, N, Xq.device, "out")
+    Y = _output(out, M, N, Xq.get_device(), "out")
     _check(load_library().wq_gemm_fp8(_ptr(Xq), _ptr(sx), M, K, N, _ptr(Wq), _ptr(sw), _ptr(Y), _stream(stream, Xq.device)),
            "wq_gemm_fp8")
     return Y
@@ -537,7 +546,7 @@ def gemm_w8a8_fp8(X, Wq, sw, out=None, workspace=None, stream=None):
     _need(X, _BF16, "X")
     M, K = X.shape
     N = _fp8_operands(Wq, sw, K, X.device)
-    Y = _output(out, M, N, X.device, "out")
+    Y = _output(out, M, N, X.get_device(), "out")
     lib = load_library()
     need = lib.wq_gemm_w8a8_fp8_workspace_bytes(M, K)
     ws = workspace if workspace is not None else Workspace(X.device).get(need)
@@ -581,7 +590,7 @@ def gemm_w4a4_mxfp4(X, Wq8, sw, out=None, workspace=None, stream=None):
     _need(X, _BF16, "X")
     M, K = X.shape
     N = _fp8_operands(Wq8, sw, K, X.device)
-    Y = _output(out, M, N, X.device, "out")
+    Y = _output(out, M, N, X.get_device(), "out")
     lib = load_library()
     need = lib.wq_gemm_w8a8_fp8_workspace_bytes(M, K)
     ws = workspace if workspace is not None else Workspace(X.device).get(need)
