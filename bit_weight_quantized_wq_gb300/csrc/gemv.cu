@@ -1091,21 +1091,7 @@ static cudaError_t launch_gemv_slice(int fmt, const uint16_t* X, int64_t M, int6
   if (p.bands > kWsMaxCounters || U > (1LL << 30)) return cudaErrorInvalidValue;
   p.U = static_cast<int>(U);
   p.P = gemv::num_ctas(U);
-  {
-    // ustart[c] = floor(U c / P) (P <= U: no range is empty), as c q + floor(c r / P) with a
-    // running remainder instead of a division per CTA
-    const long long q = U / p.P, r = U % p.P;
-    long long base = 0, rem = 0;
-    for (int c = 0; c <= p.P; ++c) {
-      p.ustart[c] = static_cast<int>(base);
-      base += q;
-      rem += r;
-      if (rem >= p.P) {
-        base += 1;
-        rem -= p.P;
-      }
-    }
-  }
+  for (int c = 0; c <= p.P; ++c) p.ustart[c] = static_cast<int>((U * c) / p.P);   // P <= U: none empty
   if (ws_bytes < gemv_mma_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
