@@ -998,7 +998,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 int num_ctas(long long U) {
   long long sms = device_sm_count();
   if (sms > kMaxCtas) sms = kMaxCtas;
-  return static_cast<int>(U < sms ? U : sms);
+  if (U <= sms) return static_cast<int>(U);
+  // as few CTAs as keep the longest range at ceil(U / sms) stages: the same critical path,
+  // fewer CTAs sharing each band
+  const long long per = (U + sms - 1) / sms;
+  return static_cast<int>((U + per - 1) / per);
 }
 
 }  // namespace gemv
