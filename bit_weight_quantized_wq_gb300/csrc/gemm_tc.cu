@@ -586,9 +586,9 @@ size_t gemm_tc_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   using namespace tc;
   const TcPlan pl = plan_tc(M, K, N);
   const size_t part = static_cast<size_t>(pl.nsplit) * pl.splits * BN * pl.bmt * sizeof(float);
-  if (fmt != kInt4G128) return part ? kWsCounterBytes + part : 0;
+  if (fmt != kInt4G128) return part ? kWsHeaderBytes + part : 0;
   const size_t xh = round256(static_cast<size_t>(M) * K * 2);
-  return kWsCounterBytes + xh + round256(static_cast<size_t>(M) * 4) + part;
+  return kWsHeaderBytes + xh + round256(static_cast<size_t>(M) * 4) + part;
 }
 
 cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N, const int32_t* Wq,
@@ -617,13 +617,13 @@ cudaError_t launch_gemm_tc(int fmt, const uint16_t* X, int64_t M, int64_t K, int
   p.cnt = reinterpret_cast<uint32_t*>(ws);
   p.part = nullptr;
   if (pl.nsplit) {
-    size_t off = kWsCounterBytes;
+    size_t off = kWsHeaderBytes;
     if (fmt == kInt4G128) off += round256(static_cast<size_t>(M) * K * 2) + round256(static_cast<size_t>(M) * 4);
     p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + off);
   }
   const void* xsrc = X;
   if (fmt == kInt4G128) {
-    uint8_t* base = reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes;  // never touch the counter header
+    uint8_t* base = reinterpret_cast<uint8_t*>(ws) + kWsHeaderBytes;  // never touch the header
     uint16_t* Xh = reinterpret_cast<uint16_t*>(base);
     float* xs = reinterpret_cast<float*>(base + ((static_cast<size_t>(M) * K * 2 + 255) / 256) * 256);
     cudaLaunchConfig_t cfg{};

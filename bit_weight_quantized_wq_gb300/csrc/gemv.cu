@@ -38,11 +38,13 @@
 // band covered by one CTA is written directly as bf16.  A band shared by several CTAs is
 // reduced by the CTA holding its first unit: that range ends inside the band, so it
 // finishes the band last, while every other contributor starts its range inside the band
-// and posts its fp32 partial sums early (one release-ordered counter increment per warp).
-// The reducer adds the partial sums to its own in CTA order (deterministic), writes bf16
-// and resets the band's counter for the next call.  A reducer only ever waits on CTAs of
-// higher index, which post before they wait themselves, so the wait always ends as long as
-// those CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is bounded).
+// and posts its fp32 partial sums early.  A posted value carries its own "written" mark (a
+// word that is never 0, below), so the reducer waits on the partial sums themselves: no
+// counter, fence or second read.  It adds them to its own in CTA order (deterministic),
+// writes bf16 and puts the words back to 0 for the next call.  A reducer only ever waits on
+// CTAs of higher index, which post before they wait themselves, so the wait always ends as
+// long as those CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is
+// bounded).
 #include <mutex>
 
 #include "decode_util.cuh"
@@ -52,10 +54,16 @@ namespace wq {
 
 __device__ uint32_t g_gemv_err;
 
+static void noalloc_scratch_reset();
+
 uint32_t gemv_read_and_clear_error() {
   uint32_t v = 0, z = 0;
   cudaMemcpyFromSymbol(&v, g_gemv_err, sizeof(v));
   cudaMemcpyToSymbol(g_gemv_err, &z, sizeof(z));
+  // A reduction that gave up may leave posted partial sums behind (a contributor that came
+  // later than the wait): the library-owned exchange area of the no-workspace entry point is
+  // zeroed again here, as a caller zeroes its own workspace after such an error.
+  if (v & kErrWaitReduce) noalloc_scratch_reset();
   return v;
 }
 
@@ -99,8 +107,7 @@ struct Params {
   const uint16_t* zeros;
   uint16_t* Y;
   OutSplit split;     // EPI == kEpiSplit3: three output tensors by column range
-  float* part;        // [P][MT][kBand] fp32 partial sums of each CTA's first band
-  uint32_t* cnt;      // [bands] counters (warps of other CTAs that posted their partial sums)
+  uint32_t* part;     // [P][MT][kBand] tagged fp32 partial sums of each CTA's first band (0: not posted)
   int M, K, N;
   int G;              // 128-k groups per row (ceil(K / 128))
   int GP;             // group pairs per row (ceil(G / 2)) -- one pair per stage
@@ -128,7 +135,6 @@ struct Smem {
   uint64_t empty_w[WS];
   uint64_t full_x[XS];
   uint64_t empty_x[XS];
-  int reduce_ok;                             // the reducer's wait for the other CTAs ended
 };
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
@@ -137,31 +143,42 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return v;
 }
 
-// Split-K publication: a contributor warp's partial sums are ordered before its counter
-// increment (release, GPU scope); the reducer reads the counter with acquire semantics before
-// it reads the partial sums.
-__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// Split-K exchange.  A contributor posts each fp32 partial sum as its bits XOR kPartTag, a
+// signalling-NaN pattern that no arithmetic result has (a NaN produced by an fp32 operation
+// is the canonical 0x7fffffff, and the partial sums are all results of fp32 operations), so a
+// posted word is never 0.  The exchange area is all zeros between calls; the reducer polls a
+// word until it is non-zero, which is then the value itself (one 32-bit access: no ordering
+// between a flag and the data is needed), and writes the 0 back.
+constexpr uint32_t kPartTag = 0x7fbadbadu;
+__device__ __forceinline__ uint32_t tag_partial(float v) { return __float_as_uint(v) ^ kPartTag; }
+__device__ __forceinline__ float untag_partial(uint32_t w) { return __uint_as_float(w ^ kPartTag); }
+__device__ __forceinline__ void st_relaxed_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ uint4 ld_relaxed_gpu_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
   return v;
 }
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+__device__ __forceinline__ void st_relaxed_gpu_v4_zero(uint32_t* p) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%1,%1,%1};" ::"l"(p), "r"(0u) : "memory");
 }
-__device__ __forceinline__ float4 ld_cg_f32x4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ bool all_posted(const uint4& v) { return v.x != 0u && v.y != 0u && v.z != 0u && v.w != 0u; }
 
 // One share of the reduction of a shared band by its reducer CTA: for the float4 slots idx =
 // first, first + step, ... of the M x kBand outputs, the reducer's own partial sums (`own`,
-// shared memory, [MT][kBand]) plus those of CTAs c_lo + 1 .. c_hi (global, in CTA order:
-// deterministic); bf16 results to the outputs.
+// shared memory, [MT][kBand]) plus those posted by CTAs c_lo + 1 .. c_hi (global, added in
+// CTA order: deterministic), each waited for until posted and then cleared; bf16 results to
+// the outputs.  The wait ends kWaitLimitNs after the share starts at the latest (error flag
+// set; the lanes keep going so that every warp stays converged).
 template <int MT, int EPI>
 __device__ __forceinline__ void reduce_band_share(const Params& p, int band, const float* own, int c_lo, int c_hi,
                                                   int first, int step) {
+  const uint64_t t0 = globaltimer_ns();
+  bool live = true;
   for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
     int m, r4;
     if constexpr (EPI == kEpiSwiglu) {
@@ -175,17 +192,31 @@ __device__ __forceinline__ void reduce_band_share(const Params& p, int band, con
       r4 = 4 * (idx % (kBand / 4));
     }
     float4 acc4 = *reinterpret_cast<const float4*>(own + m * kBand + r4);
-    const float* base = p.part + static_cast<long long>(m) * kBand + r4;
+    uint32_t* base = p.part + static_cast<long long>(m) * kBand + r4;
     for (int c = c_lo + 1; c <= c_hi; c += 8) {
-      float4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
+      uint4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        v[q] = (c + q <= c_hi) ? ld_cg_f32x4(base + static_cast<long long>(c + q) * MT * kBand)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = (c + q <= c_hi) ? ld_relaxed_gpu_v4(base + static_cast<long long>(c + q) * MT * kBand)
+                               : make_uint4(1u, 1u, 1u, 1u);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        while (live && !all_posted(v[q])) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(&g_gemv_err, kErrWaitReduce);
+            live = false;
+          } else {
+            v[q] = ld_relaxed_gpu_v4(base + static_cast<long long>(c + q) * MT * kBand);
+          }
+        }
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         if (c + q <= c_hi) {
-          acc4.x += v[q].x; acc4.y += v[q].y; acc4.z += v[q].z; acc4.w += v[q].w;
+          acc4.x += untag_partial(v[q].x);
+          acc4.y += untag_partial(v[q].y);
+          acc4.z += untag_partial(v[q].z);
+          acc4.w += untag_partial(v[q].w);
+          st_relaxed_gpu_v4_zero(base + static_cast<long long>(c + q) * MT * kBand);
         }
     }
     const float o4[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
@@ -308,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.full_x[s], 32);
       mbar_init(&sm.empty_x[s], 32 * kConsumerWarps);
     }
-    sm.reduce_ok = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -551,14 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int last_band = (u1 - 1) / p.GP;
     const int red_band = (u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
     float* own = reinterpret_cast<float*>(&sm.w[0][0]);
-    int pending = -1;       // band whose partial sums are stored but not yet published
-    auto publish = [&]() {
-      // the stores were issued a stage ago, so the release rarely waits
-      __syncwarp();
-      if (lane == 0) red_release_gpu_add(p.cnt + pending, 1u);
-      pending = -1;
-    };
-    pdl_wait();   // outputs, partial sums and counters may be in use by the previous kernel
+    pdl_wait();   // outputs and the exchange area may be in use by the previous kernel
     for (int i = 0; i < nstages; ++i, st.next()) {
       const int ws = i % WS;
       const uint32_t wph = (i / WS) & 1;
@@ -920,7 +943,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       mbar_arrive(&sm.empty_w[ws]);   // weights consumed: the producer may refill the slot
-      if (pending >= 0) publish();
 
       // Band end.  A band shared with other CTAs is either this CTA's first (its range
       // started inside the band: publish the partial sums) or its last (this CTA holds the
@@ -933,15 +955,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (st.seg_start == bs) {
             store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
           } else {
-            float* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
+            uint32_t* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int m = 2 * t + (e & 1) + 8 * nt;
-                if (m < p.M) __stcg(slotp + m * kBand + ((e >> 1) ? r1 : r0), acc[nt][e]);
+                if (m < p.M) st_relaxed_gpu(slotp + m * kBand + ((e >> 1) ? r1 : r0), tag_partial(acc[nt][e]));
               }
-            pending = band;   // published after the next stage's math
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -951,7 +972,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&sm.empty_x[xs]);   // activations consumed
     }
-    if (pending >= 0) publish();
     // ---------------------------------------------------------------- shared last band
     if (red_band >= 0) {
       // every consumer warp is past its loop (those that gave up on a wait too): the weight
@@ -967,30 +987,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int be = (red_band + 1) * p.GP;
       int c_hi = cta;
       while (c_hi + 1 < p.P && p.ustart[c_hi + 1] < be) ++c_hi;
-      if (cw == 0 && lane == 0) {
-        // each consumer warp of CTAs cta + 1 .. c_hi posts once
-        const uint32_t want = static_cast<uint32_t>(c_hi - cta) * kConsumerWarps;
-        int ok = 1;
-        if (ld_relaxed_gpu(p.cnt + red_band) < want) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_relaxed_gpu(p.cnt + red_band) < want) {
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-              atomicOr(&g_gemv_err, kErrWaitReduce);
-              ok = 0;
-              break;
-            }
-          }
-        }
-        // One acquire load of the final count (it reads the last of the contributors' release
-        // increments, so it synchronizes with all of them): the posted partial sums are
-        // visible from here on, at the cost of a load rather than a GPU-scope fence.
-        (void)ld_acquire_gpu(p.cnt + red_band);
-        if (ok) p.cnt[red_band] = 0u;    // ready for the next call (its contributors post after this grid ends)
-        sm.reduce_ok = ok;
-      }
       named_bar_sync(1, 32 * kConsumerWarps);
-      if (sm.reduce_ok)
-        reduce_band_share<MT, EPI>(p, red_band, own, cta, c_hi, cw * 32 + lane, 32 * kConsumerWarps);
+      reduce_band_share<MT, EPI>(p, red_band, own, cta, c_hi, cw * 32 + lane, 32 * kConsumerWarps);
     }
   }
 }
@@ -1009,6 +1007,10 @@ int num_ctas(long long U) {
 
 // Activation rows per launch: tiles of 8, 16 or 32; larger M runs as 32-row slices.
 static int tile_rows(int64_t M) { return M <= 8 ? 8 : M <= 16 ? 16 : 32; }
+
+// The exchange area of the largest launch (kMaxCtas CTAs, 32-row tiles) fits the header's.
+static_assert(static_cast<size_t>(gemv::kMaxCtas) * 32 * gemv::kBand * sizeof(uint32_t) <= kWsDecodeBytes,
+              "decode exchange area over its share of the workspace header");
 
 size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   if (M < 1 || M > kDecodeMaxM || N < 1 || K < 1) return 0;
@@ -1097,8 +1099,7 @@ static cudaError_t launch_gemv_slice(int fmt, const uint16_t* X, int64_t M, int6
   p.P = gemv::num_ctas(U);
   for (int c = 0; c <= p.P; ++c) p.ustart[c] = static_cast<int>((U * c) / p.P);   // P <= U: none empty
   if (ws_bytes < gemv_mma_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
-  p.cnt = reinterpret_cast<uint32_t*>(ws);
-  p.part = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
+  p.part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
   CUtensorMap tw, ts, tz;
   cudaError_t e = make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, static_cast<uint64_t>(K / 2),
@@ -1162,16 +1163,24 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
 // ---------------------------------------------------------------------------------------
 // The decode kernel for callers that cannot allocate device memory.
 //
-// The split-K scratch of the decode kernel (reduction counters and fp32 partial sums) lives
-// here in one fixed, library-owned device array instead of a caller-provided workspace.  It
-// is sized for every decode shape the kernel accepts (M <= 16, N <= 2097152) on a device with
-// at most gemv::kMaxCtas CTAs: 64 KiB of counters + 2.5 MiB of partials.  Every GPU that loads
-// the library keeps this array until the process exits.
+// The split-K exchange area of the decode kernel lives here in one fixed, library-owned
+// device array instead of a caller-provided workspace, in the workspace layout (64 KiB header
+// of tensor-core counters, unused here, then the exchange area).  It is sized for every
+// decode shape the kernel accepts (M <= 16, N <= 2097152) on a device with at most
+// gemv::kMaxCtas CTAs: 64 KiB + 2.5 MiB.  It starts zeroed (a __device__ array), and every
+// call that completes leaves it at zero.  Every GPU that loads the library keeps this array
+// until the process exits.
 // ---------------------------------------------------------------------------------------
 constexpr size_t kNoAllocScratchBytes =
     kWsCounterBytes + static_cast<size_t>(gemv::kMaxCtas) * 16 * gemv::kBand * sizeof(float);
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static void noalloc_scratch_reset() {
+  void* a = nullptr;
+  if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess) return;
+  if (cudaMemset(a, 0, kNoAllocScratchBytes) == cudaSuccess) cudaDeviceSynchronize();
+}
 
 size_t gemv_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
@@ -1201,10 +1210,6 @@ cudaError_t launch_gemv_noalloc(int fmt, const uint16_t* X, int64_t M, int64_t K
     scratch = addr[dev];
   }
   if (gemv_workspace_bytes(fmt, M, K, N) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
-  // The array keeps whatever the previous call left; the counters must start at zero.
-  const size_t bands = static_cast<size_t>((N + gemv::kBand - 1) / gemv::kBand);
-  e = cudaMemsetAsync(scratch, 0, bands * sizeof(uint32_t), stream);
-  if (e != cudaSuccess) return e;
   return launch_gemv(fmt, X, M, K, N, Wq, scales, zeros, Y, scratch, kNoAllocScratchBytes, stream);
 }
 

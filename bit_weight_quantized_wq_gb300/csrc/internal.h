@@ -51,13 +51,20 @@ CUcontext current_context();
 // device); thread-safe.
 cudaError_t set_smem_attr_once(const void* kern, size_t smem_bytes);
 
-// Every workspace layout starts with this fixed header of split-K counters (the decode
-// kernel's bands, the tensor-core kernel's split last-wave tiles).  Every call that completes
-// leaves it at zero, so one workspace zeroed once can be shared by calls of any shape and by
-// both kernels.
+// Every workspace layout starts with the same fixed header:
+//   [0, kWsCounterBytes)               split-K counters of the tensor-core kernel's split
+//                                      last-wave tiles
+//   [kWsCounterBytes, kWsHeaderBytes)  the decode kernel's split-K exchange area (tagged
+//                                      partial sums: at most 160 CTAs x 32 rows x 256 columns
+//                                      of 4 bytes)
+// and the tensor-core kernel's other scratch follows it.  Every call that completes leaves
+// the header at zero, so one workspace zeroed once can be shared by calls of any shape and
+// by both kernels.
 constexpr size_t kWsCounterBytes = 64 * 1024;
 constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
-// Weight rows per split-K band of the decode kernel: N <= kWsMaxCounters * kDecodeBand.
+constexpr size_t kWsDecodeBytes = static_cast<size_t>(160) * 32 * 256 * 4;
+constexpr size_t kWsHeaderBytes = kWsCounterBytes + kWsDecodeBytes;
+// The decode entry points accept N <= kWsMaxCounters * kDecodeBand (2097152 weight rows).
 constexpr int64_t kDecodeBand = 128;
 // Activation rows the decode kernel accepts (tiles of 8, 16, 32 or 64 rows).
 constexpr int64_t kDecodeMaxM = 64;

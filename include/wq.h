@@ -182,14 +182,16 @@ wq_status wq_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X,
 
 /*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
- * Every layout starts with the same 64 KiB header of split-K counters (used by the decode
- * kernel, and by the tensor-core kernel when it splits the tiles of a last, partial wave
- * along K; the size depends on the device's SM count, so query it on the device that runs
- * the call).  Zero the workspace once before its first use; every call that completes leaves
- * the header at zero again, so one workspace can serve calls of any shape and either kernel
- * (after a call that reported a timed-out wait, zero it again).  One workspace must not be
- * used by two calls that can run at the same time.  Returns 0 for invalid arguments, and 0
- * when the shape needs no workspace.
+ * Every layout starts with the same header: 64 KiB of split-K counters (the tensor-core
+ * kernel's, when it splits the tiles of a last, partial wave along K), then 5 MiB for the
+ * decode kernel's split-K exchange (the partial sums of CTAs sharing a band, where 0 means
+ * "not posted yet"); the decode kernel uses only the part of it its shape needs, the
+ * tensor-core kernel's other scratch comes after it.  The size depends on the device's SM
+ * count, so query it on the device that runs the call.  Zero the workspace once before its
+ * first use; every call that completes leaves the header at zero again, so one workspace can
+ * serve calls of any shape and either kernel (after a call that reported a timed-out wait,
+ * zero it again).  One workspace must not be used by two calls that can run at the same
+ * time.  Returns 0 for invalid arguments, and 0 when the shape needs no workspace.
  */
 size_t wq_gemm_workspace_bytes(wq_fmt fmt, int64_t M, int64_t K, int64_t N);
 
@@ -233,8 +235,9 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * the synchronisation a cudaMalloc implies is not acceptable.  The pages have no counterpart:
  * this is a deployment convenience of this library, not part of the method.
  * Same arguments, results and errors as wq_gemv_w4a16 minus workspace/ws_bytes; allocates
- * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (split-K
- * counters + fp32 partials) is one library-owned device array of 64 KiB + 2.5 MiB, held by
+ * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (the split-K
+ * exchange area, in the workspace layout) is one library-owned device array of 64 KiB +
+ * 2.5 MiB, held by
  * every GPU that loads the library until the process exits; it covers M <= 16 and
  * N <= 2097152 (one CTA per SM, at most 160), and a shape it cannot hold (M > 16) is refused
  * with WQ_ERR_SHAPE before anything is enqueued.
@@ -242,10 +245,11 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * with that device current); make that first call before any stream capture.  The address is
  * looked up again when the device's current context has changed since (cudaDeviceReset
  * unloads the module, and the array may come back elsewhere); after a reset, make one call
- * outside any capture again before capturing.  Each call
- * clears the counters it needs on `stream` before the kernel.  All calls on a device share
- * the one array: calls that can overlap on the GPU (other streams, other threads) race and
- * corrupt each other's results -- serialise them.
+ * outside any capture again before capturing.  The array starts zeroed and each call that
+ * completes leaves it so (the call enqueues the kernel alone); after a call that reported a
+ * timed-out wait, wq_read_error_flags zeroes it again.  All calls on a device share the one
+ * array: calls that can overlap on the GPU (other streams, other threads) race and corrupt
+ * each other's results -- serialise them.
  */
 wq_status wq_gemv_w4a16_noalloc(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int64_t N,
                                 const int32_t* Wq, const void* scales, const uint16_t* zeros,
@@ -345,7 +349,8 @@ const char* wq_status_str(wq_status s);
 
 /*
  * Reads (and clears) the device-side error word of the current device: 0 when no bounded
- * wait ran out since the last read.  Synchronizes the device.
+ * wait ran out since the last read.  Synchronizes the device.  When a decode kernel's split-K
+ * wait ran out (bit 1 << 3), it also zeroes the scratch array of wq_gemv_w4a16_noalloc.
  */
 wq_status wq_read_error_flags(uint32_t* out);
 

@@ -1,9 +1,11 @@
 """The workspace contract of the layer entry points: a workspace zeroed once serves calls of
-any shape and either kernel, because every call that completes leaves the split-K counter
-header (the first 64 KiB) at zero again.  Checked after calls whose bands or tiles are split
-between CTAs (decode split-K, tensor-core split tiles), with every epilogue, and with one
-workspace shared by consecutive calls of different shapes; each output against the float64
-oracle, so a counter left behind (which would make a later call skip or double a reduction)
+any shape and either kernel, because every call that completes leaves the workspace header
+at zero again: the tensor-core kernel's split-K counters (64 KiB) and the decode kernel's
+split-K exchange area after them (5 MiB of tagged partial sums, where 0 means "not posted").
+Checked after calls whose bands or tiles are split between CTAs (decode split-K,
+tensor-core split tiles), with every epilogue, and with one workspace shared by consecutive
+calls of different shapes; each output against the float64 oracle, so a counter or a
+partial sum left behind (which would make a later call skip, double or mix up a reduction)
 shows up as a wrong result too."""
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ from tests._util import assert_close, to_dev, x_to_dev, y_to_host
 
 pytestmark = pytest.mark.gpu
 
-HEADER = 64 * 1024
+HEADER = 64 * 1024 + 160 * 32 * 256 * 4   # counters + the decode exchange area
 
 
 @pytest.fixture(scope="module")
@@ -57,7 +59,7 @@ def test_counters_back_at_zero_after_a_call(B, fmt, M, K, N, entry):
     ws = torch.zeros(max(B.gemm_workspace_bytes(fmt, M, K, N), HEADER), dtype=torch.uint8, device="cuda")
     fn = B.gemv_w4a16 if entry == "gemv" else B.gemm_tc_w4a16
     Y = fn(fmt, x_to_dev(xb), *_dev(fmt, pk), workspace=ws)
-    assert _header_zero(ws) == 0, "split-K counters left non-zero"
+    assert _header_zero(ws) == 0, "split-K counters or partial sums left non-zero"
     assert_close(y_to_host(Y), linear.linear_w4a16(fmt, xf, *pk), "%s %s M=%d" % (entry, fmt, M))
     assert B.read_error_flags() == 0
 
@@ -91,5 +93,5 @@ def test_one_workspace_across_shapes_and_epilogues(B):
             q, k, v = B.gemm_w4a16_qkv(fmt, X, *_dev(fmt, pk), Nq=1024, Nkv=Nkv, workspace=ws)
             for t, (lo, hi) in zip((q, k, v), ((0, 1024), (1024, 1024 + Nkv), (1024 + Nkv, N))):
                 assert_close(y_to_host(t), ref[:, lo:hi], "call %d (QKV)" % i)
-        assert _header_zero(ws) == 0, "call %d left split-K counters non-zero" % i
+        assert _header_zero(ws) == 0, "call %d left split-K counters or partial sums non-zero" % i
     assert B.read_error_flags() == 0
