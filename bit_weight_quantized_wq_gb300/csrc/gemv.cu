@@ -35,15 +35,15 @@
 //
 // Work split: the (256-row band, 256-k group pair) units -- one per pipeline stage -- are
 // split evenly over the CTAs in band-major order (the host computes each CTA's range).  A
-// band covered by one CTA is written directly as bf16.  A band shared by several CTAs is
-// reduced by the CTA holding its first unit: that range ends inside the band, so it
-// finishes the band last, while every other contributor starts its range inside the band
-// and posts its fp32 partial sums early.  A posted value carries its own "written" mark (a
-// word that is never 0, below), so the reducer waits on the partial sums themselves: no
-// counter, fence or second read.  It adds them to its own in CTA order (deterministic),
-// writes bf16 and puts the words back to 0 for the next call.  A reducer only ever waits on
-// CTAs of higher index, which post before they wait themselves, so the wait always ends as
-// long as those CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is
+// band covered by one CTA is written directly as bf16.  A band shared by several CTAs (only
+// a range's first and last band can be) is reduced by all of them: each posts its fp32
+// partial sums when its part of the band is done; after its loop each adds up its share of
+// the band's outputs (an equal split of them), taking the posted sums of every CTA of the
+// band in CTA order (deterministic), writes bf16 and puts the words back to 0 for the next
+// call.  A posted value carries its own "written" mark (a word that is never 0, below), so a
+// CTA waits on the partial sums themselves: no counter, fence or second read.  Every CTA
+// posts all its partial sums before it waits for any, so the wait always ends as long as the
+// band's CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is
 // bounded).
 #include <mutex>
 
@@ -107,7 +107,9 @@ struct Params {
   const uint16_t* zeros;
   uint16_t* Y;
   OutSplit split;     // EPI == kEpiSplit3: three output tensors by column range
-  uint32_t* part;     // [P][MT][kBand] tagged fp32 partial sums of each CTA's first band (0: not posted)
+  uint32_t* part;     // [2P][MT][kBand] tagged fp32 partial sums (0: not posted): tile c holds CTA c's
+                      // first band when its range starts inside it, tile P + c its last band when
+                      // it holds that band's first unit
   int M, K, N;
   int G;              // 128-k groups per row (ceil(K / 128))
   int GP;             // group pairs per row (ceil(G / 2)) -- one pair per stage
@@ -168,55 +170,91 @@ __device__ __forceinline__ void st_relaxed_gpu_v4_zero(uint32_t* p) {
 }
 __device__ __forceinline__ bool all_posted(const uint4& v) { return v.x != 0u && v.y != 0u && v.z != 0u && v.w != 0u; }
 
-// One share of the reduction of a shared band by its reducer CTA: for the float4 slots idx =
-// first, first + step, ... of the M x kBand outputs, the reducer's own partial sums (`own`,
-// shared memory, [MT][kBand]) plus those posted by CTAs c_lo + 1 .. c_hi (global, added in
-// CTA order: deterministic), each waited for until posted and then cleared; bf16 results to
-// the outputs.  The wait ends kWaitLimitNs after the share starts at the latest (error flag
-// set; the lanes keep going so that every warp stays converged).
+// Posted words in flight per reduction slot (a band's CTAs are read in chunks of this many, in
+// CTA order).
+constexpr int kChunk = 12;
+
+// Reduction slot idx of a shared band: activation row m and the first of its four output
+// rows r4 inside the band.
+template <int EPI>
+__device__ __forceinline__ void reduce_slot(int idx, int& m, int& r4) {
+  if constexpr (EPI == kEpiSwiglu) {
+    // slots idx and idx ^ 1 (lanes l and l ^ 1 of one warp): gate rows 16q + 4h .. + 3 and
+    // the up rows 8 below them
+    const int pr = idx >> 1, k = pr % (kBand / 8);
+    m = pr / (kBand / 8);
+    r4 = 16 * (k >> 1) + 4 * (k & 1) + 8 * (idx & 1);
+  } else {
+    m = idx / (kBand / 4);
+    r4 = 4 * (idx % (kBand / 4));
+  }
+}
+
+// Exchange tile of CTA c for a shared band: c + P where c holds the band's first unit (the
+// band is the last of its range), c where its range starts inside the band.
+__device__ __forceinline__ long long part_tile(int c, int c_first, int P) { return c == c_first ? c + P : c; }
+
+// Reads of one slot's posted words of CTAs c .. min(c + kChunk - 1, c_last) (base: the slot's
+// word in tile 0); the entries past c_last read as posted dummies.
+__device__ __forceinline__ void load_chunk(uint4 (&v)[kChunk], const uint32_t* base, long long stride, int c,
+                                           int c_first, int c_last, int P) {
+#pragma unroll
+  for (int q = 0; q < kChunk; ++q)
+    v[q] = (c + q <= c_last) ? ld_relaxed_gpu_v4(base + part_tile(c + q, c_first, P) * stride)
+                             : make_uint4(1u, 1u, 1u, 1u);
+}
+
+// The slots lo + tid, lo + tid + nthreads, ... below hi of a shared band's M x kBand / 4
+// float4 slots: the partial sums of the band's CTAs c_first .. c_last added in CTA order
+// (deterministic), CTA c_first's from `own` (shared memory, [MT][kBand]) when given, else
+// from its posted tile; every posted word is waited for until posted and then cleared; bf16
+// results to the outputs.  With `fresh`, v holds on entry the reads of the first slot's first
+// chunk, issued by the caller.  Each round of the wait re-reads every word of the chunk not
+// posted yet, all reads in flight together.  The wait ends kWaitLimitNs after the call at the
+// latest (error flag set; the lanes keep going so that every warp stays converged: lo and
+// nthreads are multiples of 32).
 template <int MT, int EPI>
-__device__ __forceinline__ void reduce_band_share(const Params& p, int band, const float* own, int c_lo, int c_hi,
-                                                  int first, int step) {
+__device__ __forceinline__ void reduce_slots(const Params& p, int band, const float* own, int c_first, int c_last,
+                                             int lo, int hi, int tid, int nthreads, uint4 (&v)[kChunk], bool fresh) {
   const uint64_t t0 = globaltimer_ns();
+  constexpr long long kStride = static_cast<long long>(MT) * kBand;
+  const int c_post = own ? c_first + 1 : c_first;   // the first CTA read from its posted tile
   bool live = true;
-  for (int idx = first; idx < p.M * (kBand / 4); idx += step) {
+  for (int idx = lo + tid; idx < hi; idx += nthreads) {
     int m, r4;
-    if constexpr (EPI == kEpiSwiglu) {
-      // slots idx and idx ^ 1 (lanes l and l ^ 1 of one warp): gate rows 16q + 4h .. + 3 and
-      // the up rows 8 below them
-      const int pr = idx >> 1, k = pr % (kBand / 8);
-      m = pr / (kBand / 8);
-      r4 = 16 * (k >> 1) + 4 * (k & 1) + 8 * (idx & 1);
-    } else {
-      m = idx / (kBand / 4);
-      r4 = 4 * (idx % (kBand / 4));
-    }
-    float4 acc4 = *reinterpret_cast<const float4*>(own + m * kBand + r4);
+    reduce_slot<EPI>(idx, m, r4);
+    float4 acc4 = own ? *reinterpret_cast<const float4*>(own + m * kBand + r4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    bool started = own != nullptr;
     uint32_t* base = p.part + static_cast<long long>(m) * kBand + r4;
-    for (int c = c_lo + 1; c <= c_hi; c += 8) {
-      uint4 v[8];   // up to eight contributors' loads in flight, summed in CTA order
+    for (int c = c_post; c <= c_last; c += kChunk) {
+      if (!fresh) load_chunk(v, base, kStride, c, c_first, c_last, p.P);
+      fresh = false;
+      while (live) {
+        bool all = true;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        v[q] = (c + q <= c_hi) ? ld_relaxed_gpu_v4(base + static_cast<long long>(c + q) * MT * kBand)
-                               : make_uint4(1u, 1u, 1u, 1u);
+        for (int q = 0; q < kChunk; ++q) all = all && all_posted(v[q]);
+        if (all) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(&g_gemv_err, kErrWaitReduce);
+          live = false;
+        } else {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        while (live && !all_posted(v[q])) {
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(&g_gemv_err, kErrWaitReduce);
-            live = false;
-          } else {
-            v[q] = ld_relaxed_gpu_v4(base + static_cast<long long>(c + q) * MT * kBand);
-          }
+          for (int q = 0; q < kChunk; ++q)
+            if (!all_posted(v[q])) v[q] = ld_relaxed_gpu_v4(base + part_tile(c + q, c_first, p.P) * kStride);
         }
+      }
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (c + q <= c_hi) {
-          acc4.x += untag_partial(v[q].x);
-          acc4.y += untag_partial(v[q].y);
-          acc4.z += untag_partial(v[q].z);
-          acc4.w += untag_partial(v[q].w);
-          st_relaxed_gpu_v4_zero(base + static_cast<long long>(c + q) * MT * kBand);
+      for (int q = 0; q < kChunk; ++q)
+        if (c + q <= c_last) {
+          const float4 f = make_float4(untag_partial(v[q].x), untag_partial(v[q].y), untag_partial(v[q].z),
+                                       untag_partial(v[q].w));
+          if (!started) {
+            acc4 = f;   // the first CTA's sums start the chain (not 0 + x: keeps a -0)
+            started = true;
+          } else {
+            acc4.x += f.x; acc4.y += f.y; acc4.z += f.z; acc4.w += f.w;
+          }
+          st_relaxed_gpu_v4_zero(base + part_tile(c + q, c_first, p.P) * kStride);
         }
     }
     const float o4[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
@@ -320,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // tiles, where it saves unpack instructions; bf16 (128 + q, raw activations) for 16-row
   // tiles, where each unpacked weight feeds two MMAs and the leaner activation prep wins.
   constexpr bool kF16 = (FMT == kInt4G128) && (MT == 8);
+  // Split-K reduction of a shared band by all of its CTAs (16 and 32-row tiles, whose partial
+  // tiles are large) or by the CTA holding its first unit alone (8-row tiles).
+  constexpr bool kAllReduce = MT >= 16;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   S& sm = *reinterpret_cast<S*>(smem_raw + smem_align_pad(smem_raw));
 
@@ -576,11 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     Cursor st;
     st.init(u0, u1, p.GP);
-    // The CTA's last band is reduced here when the range ends inside it and holds its first
-    // unit; the first band is published when the range starts inside it.
+    // 8-row tiles: the CTA holding a shared band's first unit reduces the whole band (its
+    // range ends inside the band, so it gets there last; the band is the range's last and its
+    // sums stay in acc past the loop).  Larger tiles: every CTA of the band reduces a share.
     const int last_band = (u1 - 1) / p.GP;
-    const int red_band = (u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
-    float* own = reinterpret_cast<float*>(&sm.w[0][0]);
+    const int red_band =
+        (!kAllReduce && u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
     pdl_wait();   // outputs and the exchange area may be in use by the previous kernel
     for (int i = 0; i < nstages; ++i, st.next()) {
       const int ws = i % WS;
@@ -944,38 +986,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(&sm.empty_w[ws]);   // weights consumed: the producer may refill the slot
 
-      // Band end.  A band shared with other CTAs is either this CTA's first (its range
-      // started inside the band: publish the partial sums) or its last (this CTA holds the
-      // band's first unit: reduce after the loop, once the others have published).
-      if (st.seg_last()) {
+      // Band end.  A band this CTA covers whole is written as bf16; a band shared with other
+      // CTAs (only the range's first or last can be) has its partial sums posted, in tile
+      // cta + P when this CTA holds the band's first unit, else in tile cta, and is reduced
+      // after the loop -- except the band this CTA reduces alone (red_band).
+      if (st.seg_last() && st.band != red_band) {
         const int band = st.band;
         const int bs = band * p.GP;
-        // (the reducer's band is its range's last: acc keeps its partial sums past the loop)
-        if (st.seg_start != bs || st.seg_end == bs + p.GP) {
-          if (st.seg_start == bs) {
-            store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
-          } else {
-            uint32_t* slotp = p.part + static_cast<long long>(cta) * MT * kBand;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int m = 2 * t + (e & 1) + 8 * nt;
-                if (m < p.M) st_relaxed_gpu(slotp + m * kBand + ((e >> 1) ? r1 : r0), tag_partial(acc[nt][e]));
-              }
-          }
+        if (st.seg_start == bs && st.seg_end == bs + p.GP) {
+          store_outputs<MT, EPI>(p, band, r0, r1, t, acc);
+        } else {
+          uint32_t* slotp = p.part + (st.seg_start == bs ? cta + p.P : cta) * static_cast<long long>(MT) * kBand;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+            for (int e = 0; e < 4; ++e) {
+              const int m = 2 * t + (e & 1) + 8 * nt;
+              if (m < p.M) st_relaxed_gpu(slotp + m * kBand + ((e >> 1) ? r1 : r0), tag_partial(acc[nt][e]));
+            }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
       }
       mbar_arrive(&sm.empty_x[xs]);   // activations consumed
     }
-    // ---------------------------------------------------------------- shared last band
-    if (red_band >= 0) {
+    // ---------------------------------------------------------------- shared bands
+    // Every CTA has posted all its partial sums before it waits for any other's.
+    constexpr int kSlotsPerRow = kBand / 4;
+    const int tid = cw * 32 + lane;
+    uint4 v[kChunk];
+    if constexpr (kAllReduce) {
+      const int fb = u0 / p.GP;
+#pragma unroll 1
+      for (int b = fb; b <= last_band; b += (last_band > fb ? last_band - fb : 1)) {
+        if (u0 <= b * p.GP && u1 >= (b + 1) * p.GP) continue;   // covered whole: written above
+        int c_first = cta, c_last = cta;
+        while (c_first > 0 && p.ustart[c_first] > b * p.GP) --c_first;
+        while (c_last + 1 < p.P && p.ustart[c_last + 1] < (b + 1) * p.GP) ++c_last;
+        // CTA i of the band's n takes the 32-slot chunks [i nch / n, (i + 1) nch / n)
+        const int n = c_last - c_first + 1, i = cta - c_first, nch = p.M * kSlotsPerRow / 32;
+        reduce_slots<MT, EPI>(p, b, nullptr, c_first, c_last, 32 * ((i * nch) / n), 32 * (((i + 1) * nch) / n),
+                              tid, 32 * kConsumerWarps, v, false);
+      }
+    } else if (red_band >= 0) {
+      // the band's other CTAs: cta + 1 .. c_hi
+      const int be = (red_band + 1) * p.GP;
+      int c_hi = cta;
+      while (c_hi + 1 < p.P && p.ustart[c_hi + 1] < be) ++c_hi;
+      // this thread's first slot: the reads of its first chunk go out now, while the other
+      // consumer warps finish their loops
+      if (tid < p.M * kSlotsPerRow) {
+        int m, r4;
+        reduce_slot<EPI>(tid, m, r4);
+        load_chunk(v, p.part + static_cast<long long>(m) * kBand + r4, static_cast<long long>(MT) * kBand, cta + 1,
+                   cta, c_hi, p.P);
+      }
       // every consumer warp is past its loop (those that gave up on a wait too): the weight
       // ring is idle, and slot 0 holds this CTA's own partial sums for the coalesced pass
+      float* own = reinterpret_cast<float*>(&sm.w[0][0]);
       named_bar_sync(1, 32 * kConsumerWarps);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -984,11 +1054,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = 2 * t + (e & 1) + 8 * nt;
           if (m < p.M) own[m * kBand + ((e >> 1) ? r1 : r0)] = acc[nt][e];
         }
-      const int be = (red_band + 1) * p.GP;
-      int c_hi = cta;
-      while (c_hi + 1 < p.P && p.ustart[c_hi + 1] < be) ++c_hi;
       named_bar_sync(1, 32 * kConsumerWarps);
-      reduce_band_share<MT, EPI>(p, red_band, own, cta, c_hi, cw * 32 + lane, 32 * kConsumerWarps);
+      reduce_slots<MT, EPI>(p, red_band, own, cta, c_hi, 0, p.M * kSlotsPerRow, tid, 32 * kConsumerWarps, v, true);
     }
   }
 }
@@ -1008,8 +1075,9 @@ int num_ctas(long long U) {
 // Activation rows per launch: tiles of 8, 16 or 32; larger M runs as 32-row slices.
 static int tile_rows(int64_t M) { return M <= 8 ? 8 : M <= 16 ? 16 : 32; }
 
-// The exchange area of the largest launch (kMaxCtas CTAs, 32-row tiles) fits the header's.
-static_assert(static_cast<size_t>(gemv::kMaxCtas) * 32 * gemv::kBand * sizeof(uint32_t) <= kWsDecodeBytes,
+// The exchange area of the largest launch (two tiles for each of kMaxCtas CTAs, 32-row tiles)
+// fits the header's.
+static_assert(2 * static_cast<size_t>(gemv::kMaxCtas) * 32 * gemv::kBand * sizeof(uint32_t) <= kWsDecodeBytes,
               "decode exchange area over its share of the workspace header");
 
 size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
@@ -1019,7 +1087,7 @@ size_t gemv_mma_workspace_bytes(int fmt, int64_t M, int64_t K, int64_t N) {
   const long long bands = (N + gemv::kBand - 1) / gemv::kBand;
   const int P = gemv::num_ctas(bands * ((G + 1) / 2));
   (void)fmt;
-  return kWsCounterBytes + static_cast<size_t>(P) * MT * gemv::kBand * sizeof(float);
+  return kWsCounterBytes + 2 * static_cast<size_t>(P) * MT * gemv::kBand * sizeof(uint32_t);
 }
 
 template <int FMT, int MT, int EPI>
@@ -1027,7 +1095,6 @@ static cudaError_t launch_gemv_t(const CUtensorMap& tw, const CUtensorMap& ts, c
                                  const gemv::Params& p, cudaStream_t stream) {
   using S = gemv::Smem<FMT, MT>;
   static_assert(sizeof(S) + 1024 <= gemv::kSmemLimit, "decode kernel shared memory over the per-CTA limit");
-  static_assert(MT * gemv::kBand * sizeof(float) <= sizeof(S::w), "reducer's partial sums must fit the weight ring");
   const size_t smem = sizeof(S) + 1024;
   auto kern = gemv::k_gemv<FMT, MT, EPI>;
   cudaError_t ea = set_smem_attr_once(reinterpret_cast<const void*>(kern), smem);
@@ -1167,12 +1234,12 @@ cudaError_t launch_gemv(int fmt, const uint16_t* X, int64_t M, int64_t K, int64_
 // device array instead of a caller-provided workspace, in the workspace layout (64 KiB header
 // of tensor-core counters, unused here, then the exchange area).  It is sized for every
 // decode shape the kernel accepts (M <= 16, N <= 2097152) on a device with at most
-// gemv::kMaxCtas CTAs: 64 KiB + 2.5 MiB.  It starts zeroed (a __device__ array), and every
+// gemv::kMaxCtas CTAs: 64 KiB + 5 MiB.  It starts zeroed (a __device__ array), and every
 // call that completes leaves it at zero.  Every GPU that loads the library keeps this array
 // until the process exits.
 // ---------------------------------------------------------------------------------------
 constexpr size_t kNoAllocScratchBytes =
-    kWsCounterBytes + static_cast<size_t>(gemv::kMaxCtas) * 16 * gemv::kBand * sizeof(float);
+    kWsCounterBytes + 2 * static_cast<size_t>(gemv::kMaxCtas) * 16 * gemv::kBand * sizeof(uint32_t);
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

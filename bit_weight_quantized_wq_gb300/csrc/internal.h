@@ -55,14 +55,14 @@ cudaError_t set_smem_attr_once(const void* kern, size_t smem_bytes);
 //   [0, kWsCounterBytes)               split-K counters of the tensor-core kernel's split
 //                                      last-wave tiles
 //   [kWsCounterBytes, kWsHeaderBytes)  the decode kernel's split-K exchange area (tagged
-//                                      partial sums: at most 160 CTAs x 32 rows x 256 columns
-//                                      of 4 bytes)
+//                                      partial sums: at most two tiles for each of 160 CTAs,
+//                                      32 rows x 256 columns of 4 bytes each)
 // and the tensor-core kernel's other scratch follows it.  Every call that completes leaves
 // the header at zero, so one workspace zeroed once can be shared by calls of any shape and
 // by both kernels.
 constexpr size_t kWsCounterBytes = 64 * 1024;
 constexpr int64_t kWsMaxCounters = kWsCounterBytes / 4;
-constexpr size_t kWsDecodeBytes = static_cast<size_t>(160) * 32 * 256 * 4;
+constexpr size_t kWsDecodeBytes = static_cast<size_t>(2) * 160 * 32 * 256 * 4;
 constexpr size_t kWsHeaderBytes = kWsCounterBytes + kWsDecodeBytes;
 // The decode entry points accept N <= kWsMaxCounters * kDecodeBand (2097152 weight rows).
 constexpr int64_t kDecodeBand = 128;

@@ -183,7 +183,7 @@ wq_status wq_awq_int4_g128(const float* W, int64_t N, int64_t K, const float* X,
 /*
  * Bytes of workspace wq_gemm_w4a16 / wq_gemv_w4a16 / wq_gemm_tc_w4a16 need for this shape.
  * Every layout starts with the same header: 64 KiB of split-K counters (the tensor-core
- * kernel's, when it splits the tiles of a last, partial wave along K), then 5 MiB for the
+ * kernel's, when it splits the tiles of a last, partial wave along K), then 10 MiB for the
  * decode kernel's split-K exchange (the partial sums of CTAs sharing a band, where 0 means
  * "not posted yet"); the decode kernel uses only the part of it its shape needs, the
  * tensor-core kernel's other scratch comes after it.  The size depends on the device's SM
@@ -237,7 +237,7 @@ wq_status wq_gemv_w4a16(wq_fmt fmt, const uint16_t* X, int64_t M, int64_t K, int
  * Same arguments, results and errors as wq_gemv_w4a16 minus workspace/ws_bytes; allocates
  * nothing (no cudaMalloc/cudaFree, no allocating library call).  Its scratch (the split-K
  * exchange area, in the workspace layout) is one library-owned device array of 64 KiB +
- * 2.5 MiB, held by
+ * 5 MiB, held by
  * every GPU that loads the library until the process exits; it covers M <= 16 and
  * N <= 2097152 (one CTA per SM, at most 160), and a shape it cannot hold (M > 16) is refused
  * with WQ_ERR_SHAPE before anything is enqueued.

@@ -1,7 +1,7 @@
 """The workspace contract of the layer entry points: a workspace zeroed once serves calls of
 any shape and either kernel, because every call that completes leaves the workspace header
 at zero again: the tensor-core kernel's split-K counters (64 KiB) and the decode kernel's
-split-K exchange area after them (5 MiB of tagged partial sums, where 0 means "not posted").
+split-K exchange area after them (10 MiB of tagged partial sums, where 0 means "not posted").
 Checked after calls whose bands or tiles are split between CTAs (decode split-K,
 tensor-core split tiles), with every epilogue, and with one workspace shared by consecutive
 calls of different shapes; each output against the float64 oracle, so a counter or a
@@ -16,7 +16,7 @@ from tests._util import assert_close, to_dev, x_to_dev, y_to_host
 
 pytestmark = pytest.mark.gpu
 
-HEADER = 64 * 1024 + 160 * 32 * 256 * 4   # counters + the decode exchange area
+HEADER = 64 * 1024 + 2 * 160 * 32 * 256 * 4   # counters + the decode exchange area
 
 
 @pytest.fixture(scope="module")
