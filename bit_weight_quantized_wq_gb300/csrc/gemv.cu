@@ -190,6 +190,15 @@ __device__ __forceinline__ void reduce_slot(int idx, int& m, int& r4) {
   }
 }
 
+// Warp-wide max of the packed row-maximum pairs mxp[0 .. NQ-1] (two bf16 magnitudes per word).
+template <int NQ>
+__device__ __forceinline__ void warp_max_pairs(uint32_t (&mxp)[4]) {
+#pragma unroll
+  for (int sh = 1; sh < 32; sh <<= 1)
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) mxp[q] = __vmaxu2(mxp[q], __shfl_xor_sync(0xffffffffu, mxp[q], sh));
+}
+
 // Exchange tile of CTA c for a shared band: c + P where c holds the band's first unit (the
 // band is the last of its range), c where its range starts inside the band.
 __device__ __forceinline__ long long part_tile(int c, int c_first, int P) { return c == c_first ? c + P : c; }
@@ -448,6 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor st;
     st.init(u0, u1, p.GP);
     for (int q = 0; q < pw && q < nstages; ++q) st.next();
+    // Activation rows M .. MT-1 of a tile are zeros in every stage: this warp's ring slots get
+    // them (and a unit row factor, zero group sums) once, here, and each stage converts rows
+    // below M only.
+    for (int slot = pw; slot < S::XS; slot += kPrepWarps) {
+      uint4* xs = &sm.x[slot][0][0][0][0];
+      for (int q = lane; q < NT * 2 * 4 * 32; q += 32) xs[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < MT) {
+        sm.xf[slot][lane] = 1.f;
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {
+          sm.xsum[slot][hg][lane] = 0.f;
+          sm.xoff[slot][hg][lane] = 0.f;
+        }
+      }
+    }
+    __syncwarp();
     pdl_wait();
     for (int i = pw; i < nstages; i += kPrepWarps) {
       const int slot = i % S::XS;
@@ -479,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scaled up); only values more than 2^31 below their row's largest lose bits, as fp16
         // subnormals.  max |x| per row: bf16 magnitudes order like integers; two rows' maxima
         // share a word for the warp reduction.
+        const int nrow = p.M - 8 * nt;   // rows of this 8-row tile in use (warp-uniform)
+        if (nrow <= 0) continue;          // an all-zero tile: its slot rows stay zero
         float inv[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) inv[r] = 1.f;
@@ -496,19 +523,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mxp[q] = m2[0] | (m2[1] << 16);
           }
-#pragma unroll
-          for (int sh = 1; sh < 32; sh <<= 1)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) mxp[q] = __vmaxu2(mxp[q], __shfl_xor_sync(0xffffffffu, mxp[q], sh));
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
+          if (nrow <= 2) warp_max_pairs<1>(mxp);
+          else if (nrow <= 4) warp_max_pairs<2>(mxp);
+          else warp_max_pairs<4>(mxp);
+          auto row_scale = [&](int r) {
             const int kk = bf16_to_f16_exponent((mxp[r >> 1] >> (16 * (r & 1))) & 0xffffu);
             inv[r] = pow2_normal(-kk);
             if (lane == r) sm.xf[slot][8 * nt + r] = pow2_normal(kk);
+          };
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r >= nrow) break;
+            row_scale(r);
           }
         }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
+        // One row of the tile into its B-fragment slots.
+        auto put_row = [&](int r) {
           uint4* dst = &sm.x[slot][nt][h][fv][4 * r + ft];
           const uint4 x = cur[kCurTile * nt + r];
           const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
@@ -544,6 +574,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
           }
+        };
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r >= nrow) break;
+          put_row(r);
         }
         if constexpr (FMT == kInt4G128 && !kF16) {
           // Per-group activation sums of the tile's 8 rows on the tensor core: an all-ones A
