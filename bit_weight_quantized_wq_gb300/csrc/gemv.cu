@@ -413,13 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_m = l2_policy_evict_last();
       Cursor st;
       st.init(u0, u1, p.GP);
-      {
-        // While the previous kernel of the stream finishes: pull the first stages' weights
-        // into L2 (a hint only; every read that lands in shared memory follows the wait).
-        Cursor pf = st;
-        for (int q = 0; q < WS && q < nstages; ++q, pf.next())
-          tma_prefetch_l2_2d(&tmap_w, pf.j * 128, pf.band * kBand);
-      }
+      // While the previous kernel of the stream finishes: pull the first stage's weight tile
+      // into L2 (a hint only; every read that lands in shared memory follows the wait).  One
+      // tile: hints for more stages, or for the metadata tiles, hold up this thread's first
+      // loads after the wait by more than they save.
+      tma_prefetch_l2_2d(&tmap_w, st.j * 128, st.band * kBand);
       pdl_wait();
       int i = 0;
       for (; i < nstages; ++i, st.next()) {
