@@ -45,6 +45,30 @@ def test_gemv_small(B, fmt, M, N, K):
     assert_close(y_to_host(Y), ref, "%s M=%d N=%d K=%d" % (fmt, M, N, K))
 
 
+# One or two 256-row bands over a long K: every band is shared by 28-56 CTAs (one stage each).
+# 8-row tiles: the band's first CTA reads the others' posted sums in several chunks of 12;
+# 16- and 32-row tiles: more CTAs share the band than it has 32-slot chunks, so some reduce
+# nothing.  Run twice on one workspace: the exchange area is back at zero after each call.
+@pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
+@pytest.mark.parametrize("M", [1, 4, 16, 24])
+@pytest.mark.parametrize("N,K", [(256, 14336), (300, 7168)])
+def test_gemv_band_shared_by_many_ctas(B, fmt, M, N, K):
+    import torch
+    W = inputs.weights(N + 3 * K, N, K, 0.05)
+    pk = _pack(fmt, W)
+    xb, xf = inputs.activations(M * 5 + K, M, K)
+    ref = linear.linear_w4a16(fmt, xf, *pk)
+    ws = torch.zeros(B.gemm_workspace_bytes(fmt, M, K, N), dtype=torch.uint8, device="cuda")
+    X = x_to_dev(xb)
+    d = [to_dev(a) for a in pk]
+    for rep in range(2):
+        Y = B.gemv_w4a16(fmt, X, d[0], d[1], d[2] if fmt == "int4_g128" else None, workspace=ws)
+        assert_close(y_to_host(Y), ref, "%s M=%d N=%d K=%d call %d" % (fmt, M, N, K, rep))
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(ws)) == 0, "split-K exchange words left behind"
+    assert B.read_error_flags() == 0
+
+
 @pytest.mark.parametrize("M", [1, 5, 16])
 @pytest.mark.parametrize("K", [32, 96, 160, 1056])
 def test_gemv_mxfp4_k_tail(B, M, K):
