@@ -190,15 +190,6 @@ __device__ __forceinline__ void reduce_slot(int idx, int& m, int& r4) {
   }
 }
 
-// Warp-wide max of the packed row-maximum pairs mxp[0 .. NQ-1] (two bf16 magnitudes per word).
-template <int NQ>
-__device__ __forceinline__ void warp_max_pairs(uint32_t (&mxp)[4]) {
-#pragma unroll
-  for (int sh = 1; sh < 32; sh <<= 1)
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) mxp[q] = __vmaxu2(mxp[q], __shfl_xor_sync(0xffffffffu, mxp[q], sh));
-}
-
 // Exchange tile of CTA c for a shared band: c + P where c holds the band's first unit (the
 // band is the last of its range), c where its range starts inside the band.
 __device__ __forceinline__ long long part_tile(int c, int c_first, int P) { return c == c_first ? c + P : c; }
@@ -500,32 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One power-of-two scale 2^-k per stage and activation row carries every operand into
         // fp16 exactly (bf16_to_f16_exponent: the row's largest in [2^14, 2^15), small rows
         // scaled up); only values more than 2^31 below their row's largest lose bits, as fp16
-        // subnormals.  max |x| per row: bf16 magnitudes order like integers; two rows' maxima
-        // share a word for the warp reduction.
+        // subnormals.  max |x| per row: bf16 magnitudes order like integers.
         const int nrow = p.M - 8 * nt;   // rows of this 8-row tile in use (warp-uniform)
         if (nrow <= 0) continue;          // an all-zero tile: its slot rows stay zero
         float inv[8];
 #pragma unroll
         for (int r = 0; r < 8; ++r) inv[r] = 1.f;
         if constexpr (FMT != kInt4G128 || kF16) {
-          uint32_t mxp[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t m2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const uint4 x = cur[kCurTile * nt + 2 * q + u];
-              const uint32_t v = __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
-                                          __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
-              m2[u] = max(v & 0xffffu, v >> 16);
-            }
-            mxp[q] = m2[0] | (m2[1] << 16);
-          }
-          if (nrow <= 2) warp_max_pairs<1>(mxp);
-          else if (nrow <= 4) warp_max_pairs<2>(mxp);
-          else warp_max_pairs<4>(mxp);
+          // this lane's max per row, then one warp-wide max reduction per row in use
           auto row_scale = [&](int r) {
-            const int kk = bf16_to_f16_exponent((mxp[r >> 1] >> (16 * (r & 1))) & 0xffffu);
+            const uint4 x = cur[kCurTile * nt + r];
+            const uint32_t v = __vmaxu2(__vmaxu2(x.x & 0x7fff7fffu, x.y & 0x7fff7fffu),
+                                        __vmaxu2(x.z & 0x7fff7fffu, x.w & 0x7fff7fffu));
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, max(v & 0xffffu, v >> 16));
+            const int kk = bf16_to_f16_exponent(mx);
             inv[r] = pow2_normal(-kk);
             if (lane == r) sm.xf[slot][8 * nt + r] = pow2_normal(kk);
           };
@@ -1159,7 +1138,7 @@ cudaError_t launch_gemv_mma(int fmt, const uint16_t* X, int64_t M, int64_t K, in
   if (epi == kEpiSwiglu && N % 16 != 0) return cudaErrorInvalidValue;
   if (epi == kEpiSplit3 && !split) return cudaErrorInvalidValue;
   // M > 32: consecutive 32-row slices of X and of the outputs, one launch each, in order on
-  // the stream (they share the workspace; each leaves its counters at zero).
+  // the stream (they share the workspace; each leaves its exchange area at zero).
   constexpr int64_t kSlice = 32;
   const int64_t ldy = epi == kEpiSwiglu ? N / 2 : N;
   for (int64_t m0 = 0; m0 < M; m0 += kSlice) {
