@@ -45,13 +45,13 @@ def test_gemv_small(B, fmt, M, N, K):
     assert_close(y_to_host(Y), ref, "%s M=%d N=%d K=%d" % (fmt, M, N, K))
 
 
-# One or two 256-row bands over a long K: every band is shared by 28-56 CTAs (one stage each).
-# 8-row tiles: the band's first CTA reads the others' posted sums in several chunks of 12;
-# 16- and 32-row tiles: more CTAs share the band than it has 32-slot chunks, so some reduce
-# nothing.  Run twice on one workspace: the exchange area is back at zero after each call.
+# One or two 256-row bands over a long K: every band is shared by 28-64 CTAs.  8-row tiles:
+# the band's first CTA reads the others' posted sums in several chunks of 12; 16- and 32-row
+# tiles: more CTAs share the band than it has 32-slot chunks, so some reduce nothing.  Run
+# twice on one workspace: the exchange area is back at zero after each call.
 @pytest.mark.parametrize("fmt", ["int4_g128", "mxfp4"])
 @pytest.mark.parametrize("M", [1, 4, 16, 24])
-@pytest.mark.parametrize("N,K", [(256, 14336), (300, 7168)])
+@pytest.mark.parametrize("N,K", [(256, 14336), (300, 7168), (512, 32768)])
 def test_gemv_band_shared_by_many_ctas(B, fmt, M, N, K):
     import torch
     W = inputs.weights(N + 3 * K, N, K, 0.05)
