@@ -88,6 +88,7 @@ constexpr int kGroupK = 128;                         // k per group (INT4 group;
 constexpr int kSmemLimit = 227 * 1024;               // dynamic shared memory per CTA
 constexpr int kSmemReserve = 1024 + 512;             // alignment pad + barriers and flags
 constexpr int kMaxCtas = 160;                        // CTAs per launch (one per SM, at most)
+static_assert(kMaxCtas <= 256, "CTA indices are stored in bytes");
 
 // Raw metadata tile(s) per weight stage: INT4 scales + zeros boxes of 8 groups x 256 rows
 // (fp16); MXFP4 one box of 16 E8M0 bytes x 256 rows.
@@ -119,6 +120,9 @@ struct Params {
   int P;              // CTAs
   int meta_tma;       // 1: metadata tiles arrive by TMA with the weights; 0: consumers gather them
   int ustart[kMaxCtas + 1];   // CTA c owns units [ustart[c], ustart[c + 1])
+  // The CTAs holding the first and the last unit of CTA c's first band, and the last unit of
+  // its last band (the host's answer, so no CTA scans ustart after its loop).
+  uint8_t fb_first[kMaxCtas], fb_last[kMaxCtas], lb_last[kMaxCtas];
 };
 
 template <int FMT, int MT>
@@ -1034,9 +1038,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int b = fb; b <= last_band; b += (last_band > fb ? last_band - fb : 1)) {
         if (u0 <= b * p.GP && u1 >= (b + 1) * p.GP) continue;   // covered whole: written above
-        int c_first = cta, c_last = cta;
-        while (c_first > 0 && p.ustart[c_first] > b * p.GP) --c_first;
-        while (c_last + 1 < p.P && p.ustart[c_last + 1] < (b + 1) * p.GP) ++c_last;
+        // the band's CTAs: this CTA holds the last band's first unit when that band is not its first
+        const int c_first = (b == fb) ? p.fb_first[cta] : cta;
+        const int c_last = (b == fb) ? p.fb_last[cta] : p.lb_last[cta];
         // CTA i of the band's n takes the 32-slot chunks [i nch / n, (i + 1) nch / n)
         const int n = c_last - c_first + 1, i = cta - c_first, nch = p.M * kSlotsPerRow / 32;
         reduce_slots<MT, EPI>(p, b, nullptr, c_first, c_last, 32 * ((i * nch) / n), 32 * (((i + 1) * nch) / n),
@@ -1044,9 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (red_band >= 0) {
       // the band's other CTAs: cta + 1 .. c_hi
-      const int be = (red_band + 1) * p.GP;
-      int c_hi = cta;
-      while (c_hi + 1 < p.P && p.ustart[c_hi + 1] < be) ++c_hi;
+      const int c_hi = p.lb_last[cta];
       // this thread's first slot: the reads of its first chunk go out now, while the other
       // consumer warps finish their loops
       if (tid < p.M * kSlotsPerRow) {
@@ -1177,6 +1179,26 @@ static cudaError_t launch_gemv_slice(int fmt, const uint16_t* X, int64_t M, int6
   p.U = static_cast<int>(U);
   p.P = gemv::num_ctas(U);
   for (int c = 0; c <= p.P; ++c) p.ustart[c] = static_cast<int>((U * c) / p.P);   // P <= U: none empty
+  {
+    // owner(x): the CTA holding unit x (ranges are increasing: walk forward from a lower bound)
+    auto owner = [&](long long x, int from) {
+      int c = from;
+      while (c + 1 < p.P && p.ustart[c + 1] <= x) ++c;
+      return c;
+    };
+    // all three are nondecreasing in c, and the last two are >= c: each walk resumes where it
+    // stopped, O(P) in all
+    int lo = 0, hf = 0, hl = 0;
+    for (int c = 0; c < p.P; ++c) {
+      const long long fb = p.ustart[c] / p.GP, lb = (p.ustart[c + 1] - 1) / p.GP;
+      lo = owner(fb * p.GP, lo);
+      hf = owner(fb * p.GP + p.GP - 1, hf > c ? hf : c);
+      hl = owner(lb * p.GP + p.GP - 1, hl > c ? hl : c);
+      p.fb_first[c] = static_cast<uint8_t>(lo);
+      p.fb_last[c] = static_cast<uint8_t>(hf);
+      p.lb_last[c] = static_cast<uint8_t>(hl);
+    }
+  }
   if (ws_bytes < gemv_mma_workspace_bytes(fmt, M, K, N)) return cudaErrorInvalidValue;
   p.part = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(ws) + kWsCounterBytes);
 
