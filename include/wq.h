@@ -17,7 +17,8 @@
  *   - Every pointer is a DEVICE pointer on the current CUDA device, owned by the caller, and
  *     must be 16-byte aligned.  The library never allocates or frees device memory, never
  *     synchronizes, and enqueues work only on `stream` (a cudaStream_t; NULL = legacy
- *     default stream).
+ *     default stream) -- except wq_read_error_flags, which synchronizes the device to read
+ *     the error word (and zeroes the library's own scratch array after a timed-out wait).
  *   - Argument errors are detected on the host before anything is enqueued and returned as
  *     a wq_status; nothing is launched then.  Launch failures return WQ_ERR_CUDA.  Device-side
  *     faults surface, as usual in CUDA, at the caller's next synchronization.
