@@ -143,12 +143,6 @@ struct Smem {
   uint64_t empty_x[XS];
 };
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
 // Split-K exchange.  A contributor posts each fp32 partial sum as its bits XOR kPartTag, a
 // signalling-NaN pattern that no arithmetic result has (a NaN produced by an fp32 operation
 // is the canonical 0x7fffffff, and the partial sums are all results of fp32 operations), so a
