@@ -35,16 +35,19 @@
 //
 // Work split: the (256-row band, 256-k group pair) units -- one per pipeline stage -- are
 // split evenly over the CTAs in band-major order (the host computes each CTA's range).  A
-// band covered by one CTA is written directly as bf16.  A band shared by several CTAs (only
-// a range's first and last band can be) is reduced by all of them: each posts its fp32
-// partial sums when its part of the band is done; after its loop each adds up its share of
-// the band's outputs (an equal split of them), taking the posted sums of every CTA of the
-// band in CTA order (deterministic), writes bf16 and puts the words back to 0 for the next
-// call.  A posted value carries its own "written" mark (a word that is never 0, below), so a
-// CTA waits on the partial sums themselves: no counter, fence or second read.  Every CTA
-// posts all its partial sums before it waits for any, so the wait always ends as long as the
-// band's CTAs get an SM (one CTA per SM, at most one CTA per SM launched; the wait is
-// bounded).
+// band covered by one CTA is written directly as bf16.  For a band shared by several CTAs
+// (only a range's first and last band can be), each CTA posts its fp32 partial sums when its
+// part of the band is done, and the band is reduced after the loops:
+//   8-row tiles: by the CTA holding its first unit alone (its range ends inside the band, so
+//     it gets there last; its own sums stay on chip and the others exit after posting);
+//   16- and 32-row tiles, whose partial tiles are large: by all of its CTAs, each adding up
+//     an equal share of the band's outputs.
+// Either way the posted sums of the band's CTAs are added in CTA order (deterministic), the
+// results written as bf16 and the words put back to 0 for the next call.  A posted value
+// carries its own "written" mark (a word that is never 0, below), so a CTA waits on the
+// partial sums themselves: no counter, fence or second read.  Every CTA posts all its
+// partial sums before it waits for any, so the wait always ends as long as the band's CTAs
+// get an SM (one CTA per SM, at most one CTA per SM launched; the wait is bounded).
 #include <mutex>
 
 #include "decode_util.cuh"
@@ -146,8 +149,8 @@ struct Smem {
 // Split-K exchange.  A contributor posts each fp32 partial sum as its bits XOR kPartTag, a
 // signalling-NaN pattern that no arithmetic result has (a NaN produced by an fp32 operation
 // is the canonical 0x7fffffff, and the partial sums are all results of fp32 operations), so a
-// posted word is never 0.  The exchange area is all zeros between calls; the reducer polls a
-// word until it is non-zero, which is then the value itself (one 32-bit access: no ordering
+// posted word is never 0.  The exchange area is all zeros between calls; a reducing CTA polls
+// a word until it is non-zero, which is then the value itself (one 32-bit access: no ordering
 // between a flag and the data is needed), and writes the 0 back.
 constexpr uint32_t kPartTag = 0x7fbadbadu;
 __device__ __forceinline__ uint32_t tag_partial(float v) { return __float_as_uint(v) ^ kPartTag; }
