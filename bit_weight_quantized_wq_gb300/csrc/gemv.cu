@@ -39,7 +39,7 @@
 // (only a range's first and last band can be), each CTA posts its fp32 partial sums when its
 // part of the band is done, and the band is reduced after the loops:
 //   8-row tiles: by the CTA holding its first unit alone (its range ends inside the band, so
-//     it gets there last; its own sums stay on chip and the others exit after posting);
+//     it gets there last; the others exit after posting);
 //   16- and 32-row tiles, whose partial tiles are large: by all of its CTAs, each adding up
 //     an equal share of the band's outputs.
 // Either way the posted sums of the band's CTAs are added in CTA order (deterministic), the
@@ -206,28 +206,26 @@ __device__ __forceinline__ void load_chunk(uint4 (&v)[kChunk], const uint32_t* b
 }
 
 // The slots lo + tid, lo + tid + nthreads, ... below hi of a shared band's M x kBand / 4
-// float4 slots: the partial sums of the band's CTAs c_first .. c_last added in CTA order
-// (deterministic), CTA c_first's from `own` (shared memory, [MT][kBand]) when given, else
-// from its posted tile; every posted word is waited for until posted and then cleared; bf16
+// float4 slots: the posted partial sums of the band's CTAs c_first .. c_last added in CTA
+// order (deterministic); every word is waited for until posted and then cleared; bf16
 // results to the outputs.  With `fresh`, v holds on entry the reads of the first slot's first
 // chunk, issued by the caller.  Each round of the wait re-reads every word of the chunk not
 // posted yet, all reads in flight together.  The wait ends kWaitLimitNs after the call at the
 // latest (error flag set; the lanes keep going so that every warp stays converged: lo and
 // nthreads are multiples of 32).
 template <int MT, int EPI>
-__device__ __forceinline__ void reduce_slots(const Params& p, int band, const float* own, int c_first, int c_last,
-                                             int lo, int hi, int tid, int nthreads, uint4 (&v)[kChunk], bool fresh) {
+__device__ __forceinline__ void reduce_slots(const Params& p, int band, int c_first, int c_last, int lo, int hi,
+                                             int tid, int nthreads, uint4 (&v)[kChunk], bool fresh) {
   const uint64_t t0 = globaltimer_ns();
   constexpr long long kStride = static_cast<long long>(MT) * kBand;
-  const int c_post = own ? c_first + 1 : c_first;   // the first CTA read from its posted tile
   bool live = true;
   for (int idx = lo + tid; idx < hi; idx += nthreads) {
     int m, r4;
     reduce_slot<EPI>(idx, m, r4);
-    float4 acc4 = own ? *reinterpret_cast<const float4*>(own + m * kBand + r4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    bool started = own != nullptr;
+    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    bool started = false;
     uint32_t* base = p.part + static_cast<long long>(m) * kBand + r4;
-    for (int c = c_post; c <= c_last; c += kChunk) {
+    for (int c = c_first; c <= c_last; c += kChunk) {
       if (!fresh) load_chunk(v, base, kStride, c, c_first, c_last, p.P);
       fresh = false;
       while (live) {
@@ -631,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor st;
     st.init(u0, u1, p.GP);
     // 8-row tiles: the CTA holding a shared band's first unit reduces the whole band (its
-    // range ends inside the band, so it gets there last; the band is the range's last and its
-    // sums stay in acc past the loop).  Larger tiles: every CTA of the band reduces a share.
+    // range ends inside the band, so it gets there last; the band is the range's last).
+    // Larger tiles: every CTA of the band reduces a share.
     const int last_band = (u1 - 1) / p.GP;
     const int red_band =
         (!kAllReduce && u0 <= last_band * p.GP && u1 < (last_band + 1) * p.GP) ? last_band : -1;
@@ -1002,8 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Band end.  A band this CTA covers whole is written as bf16; a band shared with other
       // CTAs (only the range's first or last can be) has its partial sums posted, in tile
       // cta + P when this CTA holds the band's first unit, else in tile cta, and is reduced
-      // after the loop -- except the band this CTA reduces alone (red_band).
-      if (st.seg_last() && st.band != red_band) {
+      // after the loop.
+      if (st.seg_last()) {
         const int band = st.band;
         const int bs = band * p.GP;
         if (st.seg_start == bs && st.seg_end == bs + p.GP) {
@@ -1040,33 +1038,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int c_last = (b == fb) ? p.fb_last[cta] : p.lb_last[cta];
         // CTA i of the band's n takes the 32-slot chunks [i nch / n, (i + 1) nch / n)
         const int n = c_last - c_first + 1, i = cta - c_first, nch = p.M * kSlotsPerRow / 32;
-        reduce_slots<MT, EPI>(p, b, nullptr, c_first, c_last, 32 * ((i * nch) / n), 32 * (((i + 1) * nch) / n),
-                              tid, 32 * kConsumerWarps, v, false);
+        reduce_slots<MT, EPI>(p, b, c_first, c_last, 32 * ((i * nch) / n), 32 * (((i + 1) * nch) / n), tid,
+                              32 * kConsumerWarps, v, false);
       }
     } else if (red_band >= 0) {
-      // the band's other CTAs: cta + 1 .. c_hi
+      // the band's CTAs: this one and cta + 1 .. c_hi.  Each reading thread waits only for the
+      // words of its own slots (its rows come from one consumer warp of each CTA), so no
+      // barrier gathers this CTA's warps; the first chunk's reads go out at once.
       const int c_hi = p.lb_last[cta];
-      // this thread's first slot: the reads of its first chunk go out now, while the other
-      // consumer warps finish their loops
       if (tid < p.M * kSlotsPerRow) {
         int m, r4;
         reduce_slot<EPI>(tid, m, r4);
-        load_chunk(v, p.part + static_cast<long long>(m) * kBand + r4, static_cast<long long>(MT) * kBand, cta + 1,
+        load_chunk(v, p.part + static_cast<long long>(m) * kBand + r4, static_cast<long long>(MT) * kBand, cta,
                    cta, c_hi, p.P);
       }
-      // every consumer warp is past its loop (those that gave up on a wait too): the weight
-      // ring is idle, and slot 0 holds this CTA's own partial sums for the coalesced pass
-      float* own = reinterpret_cast<float*>(&sm.w[0][0]);
-      named_bar_sync(1, 32 * kConsumerWarps);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int m = 2 * t + (e & 1) + 8 * nt;
-          if (m < p.M) own[m * kBand + ((e >> 1) ? r1 : r0)] = acc[nt][e];
-        }
-      named_bar_sync(1, 32 * kConsumerWarps);
-      reduce_slots<MT, EPI>(p, red_band, own, cta, c_hi, 0, p.M * kSlotsPerRow, tid, 32 * kConsumerWarps, v, true);
+      reduce_slots<MT, EPI>(p, red_band, cta, c_hi, 0, p.M * kSlotsPerRow, tid, 32 * kConsumerWarps, v, true);
     }
   }
 }
